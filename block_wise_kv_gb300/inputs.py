@@ -1,0 +1,244 @@
+"""Seeded synthetic inputs for the per-layer inner denoising step.
+
+This module is the only piece shared by the CUDA path's tests/bench and the
+oracle: it draws numbers and lays out the batch, and holds none of the
+method's arithmetic.  Everything is generated on the CPU with
+``torch.Generator`` seeded through SplitMix64, so both sides see identical
+bf16 values.
+
+Workloads (named after the shapes they have):
+
+* ``tiny``: 1 sequence, d_model 256, 4 heads x 64, RoPE theta 1e4, prompt 64,
+  gen 256 = 8 blocks of 32, 4 inner steps per block.  Rows are embeddings of
+  token ids (table N(0,1) [1024, 256], mask id 0, prompt ids uniform in
+  1..1023, block ids re-drawn every inner step uniform in 0..1023).
+* ``llada_single``: LLaDA-8B-shaped layer, 1 sequence, d_model 4096, 32 x 128,
+  theta 5e5, prompt 512, gen 256, block 32, 8 inner steps per block.
+* ``stack``: 32 independent LLaDA-8B-shaped layers, 16 sequences, prompt
+  1024, gen 512, block 32, 16 inner steps.
+* ``long``: 4 sequences, prompt 4096, gen 1024, block 64, 32 inner steps.
+* ``ragged``: 32 sequences, prompt uniform in [128, 4096], gen in {256, 512},
+  block in {16, 32, 64}, each at a random block index, pages shuffled.
+
+Non-embedding workloads draw every row of x from N(0, 1) (bf16): prompt rows
+per position, decoded blocks from the seed of their last inner step, the
+current block from the seed of the current step, and every suffix row equal
+to one shared "mask" row.  Weights are N(0, 0.02) bf16 and the RMSNorm gain
+is 1.
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+_M64 = (1 << 64) - 1
+PAGE = 64
+
+# role ids folded into seeds
+_R_WEIGHT, _R_PROMPT, _R_BLOCK, _R_MASK, _R_EMBED, _R_IDS_PROMPT, _R_IDS_BLOCK, _R_SHAPE, _R_PAGES = range(1, 10)
+
+
+def splitmix64(x: int) -> int:
+    """One SplitMix64 output for state x (Steele, Lea & Flood 2014)."""
+    x = (x + 0x9E3779B97F4A7C15) & _M64
+    z = x
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def derive_seed(*keys: int) -> int:
+    s = 0x5EED
+    for k in keys:
+        s = splitmix64(s ^ (int(k) & _M64))
+    return s & ((1 << 63) - 1)
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def randn_bf16(shape, seed: int, std: float = 1.0) -> torch.Tensor:
+    t = torch.randn(*shape, generator=_gen(seed), dtype=torch.float32)
+    if std != 1.0:
+        t = t * std
+    return t.to(torch.bfloat16)
+
+
+@dataclass
+class Config:
+    name: str
+    d_model: int
+    n_heads: int
+    head_dim: int
+    rope_theta: float
+    t_prefix: list
+    gen_len: list
+    block: list
+    block_index: list
+    steps_per_block: int
+    layers: int = 1
+    rms_eps: float = 1e-5
+    embedding: bool = False
+    vocab: int = 1024
+    mask_id: int = 0
+    shuffle_pages: bool = True
+    spare_pages: int = 3
+    seed: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.t_prefix)
+
+    def seq_len(self, b: int) -> int:
+        return self.t_prefix[b] + self.gen_len[b]
+
+    def block_start(self, b: int, k: int | None = None) -> int:
+        k = self.block_index[b] if k is None else k
+        return self.t_prefix[b] + k * self.block[b]
+
+    def num_blocks(self, b: int) -> int:
+        return self.gen_len[b] // self.block[b]
+
+    def with_(self, **kw) -> "Config":
+        return dataclasses.replace(self, **kw)
+
+
+def make_config(name: str, **overrides) -> Config:
+    """The named workloads.  `overrides` replace fields (e.g. block_index)."""
+    if name == "tiny":
+        c = Config("tiny", 256, 4, 64, 1e4, [64], [256], [32], [0], 4, embedding=True)
+    elif name == "llada_single":
+        c = Config("llada_single", 4096, 32, 128, 5e5, [512], [256], [32], [0], 8)
+    elif name == "stack":
+        c = Config("stack", 4096, 32, 128, 5e5, [1024] * 16, [512] * 16, [32] * 16, [0] * 16, 16, layers=32)
+    elif name == "long":
+        c = Config("long", 4096, 32, 128, 5e5, [4096] * 4, [1024] * 4, [64] * 4, [0] * 4, 32)
+    elif name == "ragged":
+        g = np.random.default_rng(derive_seed(_R_SHAPE, 5))
+        tp = [int(v) for v in g.integers(128, 4097, size=32)]
+        gl = [int(v) for v in g.choice([256, 512], size=32)]
+        bl = [int(v) for v in g.choice([16, 32, 64], size=32)]
+        bi = [int(g.integers(0, gl[i] // bl[i])) for i in range(32)]
+        c = Config("ragged", 4096, 32, 128, 5e5, tp, gl, bl, bi, 8)
+    else:
+        raise KeyError(name)
+    if overrides:
+        c = c.with_(**overrides)
+    return c
+
+
+class Workload:
+    """Deterministic generator of weights, rows and the paged layout."""
+
+    def __init__(self, cfg: Config):
+        self.cfg = cfg
+        self._embed = None
+
+    # --------------------------------------------------------------- weights
+    def weights(self, layer: int = 0):
+        """(W_qkv bf16 [3*H*d, D] ~ N(0, 0.02), gain bf16 [D] = 1)."""
+        c = self.cfg
+        HD = c.n_heads * c.head_dim
+        W = randn_bf16((3 * HD, c.d_model), derive_seed(c.seed, _R_WEIGHT, layer), std=0.02)
+        g = torch.ones(c.d_model, dtype=torch.bfloat16)
+        return W, g
+
+    # ------------------------------------------------------------------ rows
+    def _embedding(self) -> torch.Tensor:
+        if self._embed is None:
+            c = self.cfg
+            self._embed = randn_bf16((c.vocab, c.d_model), derive_seed(c.seed, _R_EMBED))
+        return self._embed
+
+    def _rows_prompt(self, layer: int, b: int) -> torch.Tensor:
+        c = self.cfg
+        if c.embedding:
+            ids = torch.randint(1, c.vocab, (c.t_prefix[b],), generator=_gen(derive_seed(c.seed, _R_IDS_PROMPT, b)))
+            return self._embedding()[ids]
+        return randn_bf16((c.t_prefix[b], c.d_model), derive_seed(c.seed, _R_PROMPT, layer, b))
+
+    def _rows_block(self, layer: int, b: int, k: int, step: int) -> torch.Tensor:
+        c = self.cfg
+        if c.embedding:
+            ids = torch.randint(0, c.vocab, (c.block[b],), generator=_gen(derive_seed(c.seed, _R_IDS_BLOCK, b, k, step)))
+            return self._embedding()[ids]
+        return randn_bf16((c.block[b], c.d_model), derive_seed(c.seed, _R_BLOCK, layer, b, k, step))
+
+    def _row_mask(self, layer: int, b: int) -> torch.Tensor:
+        c = self.cfg
+        if c.embedding:
+            return self._embedding()[c.mask_id:c.mask_id + 1]
+        return randn_bf16((1, c.d_model), derive_seed(c.seed, _R_MASK, layer, b))
+
+    def seq_rows(self, layer: int, b: int, k: int | None = None, step: int = 0) -> torch.Tensor:
+        """Every row [N_b, D] of sequence b while block k is at inner step
+        `step`: prompt | decoded blocks (their last step) | block k (this
+        step) | mask rows."""
+        c = self.cfg
+        k = c.block_index[b] if k is None else k
+        parts = [self._rows_prompt(layer, b)]
+        for j in range(k):
+            parts.append(self._rows_block(layer, b, j, c.steps_per_block - 1))
+        parts.append(self._rows_block(layer, b, k, step))
+        n_suffix = c.gen_len[b] - (k + 1) * c.block[b]
+        if n_suffix > 0:
+            parts.append(self._row_mask(layer, b).expand(n_suffix, c.d_model))
+        return torch.cat(parts, dim=0).contiguous()
+
+    def block_rows(self, layer: int, b: int, k: int | None = None, step: int = 0) -> torch.Tensor:
+        c = self.cfg
+        k = c.block_index[b] if k is None else k
+        return self._rows_block(layer, b, k, step).contiguous()
+
+    def batch_rows(self, layer: int = 0, step: int = 0, blocks=None):
+        """(x_full [R, D], x_block [M, D]) packed in sequence order."""
+        c = self.cfg
+        blocks = c.block_index if blocks is None else blocks
+        full = [self.seq_rows(layer, b, blocks[b], step) for b in range(c.batch)]
+        blk = [self.block_rows(layer, b, blocks[b], step) for b in range(c.batch)]
+        return torch.cat(full, 0).contiguous(), torch.cat(blk, 0).contiguous()
+
+    # ---------------------------------------------------------------- layout
+    def page_lists(self):
+        """Physical page ids of each sequence (a seeded permutation of the
+        pool's pages when shuffle_pages), and the pool size."""
+        c = self.cfg
+        need = [(c.seq_len(b) + PAGE - 1) // PAGE for b in range(c.batch)]
+        total = sum(need) + c.spare_pages
+        if c.shuffle_pages:
+            perm = np.random.default_rng(derive_seed(c.seed, _R_PAGES)).permutation(total)
+        else:
+            perm = np.arange(total)
+        out, at = [], 0
+        for n in need:
+            out.append([int(p) for p in perm[at:at + n]])
+            at += n
+        return out, total
+
+
+def layout(cfg: Config, blocks=None):
+    """Host-side metadata of the batch as int32 numpy arrays: block_table
+    [batch, max_pages] (unused entries -1), seq_len, block_start, block_len,
+    cu_block, cu_seq, and num_pages."""
+    wl = Workload(cfg)
+    blocks = cfg.block_index if blocks is None else blocks
+    pages, total = wl.page_lists()
+    B = cfg.batch
+    maxp = max((len(p) for p in pages), default=1)
+    bt = np.full((B, max(maxp, 1)), -1, dtype=np.int32)
+    for b, pl in enumerate(pages):
+        bt[b, :len(pl)] = pl
+    seq_len = np.array([cfg.seq_len(b) for b in range(B)], dtype=np.int32)
+    bstart = np.array([cfg.block_start(b, blocks[b]) for b in range(B)], dtype=np.int32)
+    blen = np.array(cfg.block, dtype=np.int32)
+    cu_block = np.concatenate([[0], np.cumsum(blen)]).astype(np.int32)
+    cu_seq = np.concatenate([[0], np.cumsum(seq_len)]).astype(np.int32)
+    return dict(block_table=bt, seq_len=seq_len, block_start=bstart, block_len=blen, cu_block=cu_block,
+                cu_seq=cu_seq, num_pages=total)

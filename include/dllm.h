@@ -1,0 +1,209 @@
+/* dllm.h — C ABI of the GB300 (sm_103a) per-layer inner denoising step of
+ * block-wise (semi-autoregressive) diffusion-LLM decoding.
+ *
+ * One inner step of one layer, for a batch of sequences that are each in the
+ * middle of decoding block C_b = [s_b, s_b + B_b) of N_b tokens:
+ *
+ *   dllm_block_qkv_rope_write  RMSNorm -> QKV projection -> RoPE for the B_b
+ *                              block rows only, with K/V written once into the
+ *                              paged bf16 cache and Q into q_block.
+ *   dllm_block_attention       bidirectional attention of the block rows over
+ *                              [prefix KV | fresh block KV | suffix KV].
+ *   dllm_state_merge           output rows of the invariant set U (prefix and
+ *                              suffix): cached online-softmax state (m, l, O~)
+ *                              merged exactly with the fresh block keys.
+ *
+ * and, once per block boundary, dllm_cache_build, which fills the paged cache
+ * for all rows and the per-row state (m, l, O~) of every row of U over the
+ * keys of U.  Sources (page titles):
+ *   - "LaCache: Exact Caching and Precision-Adaptive Inference for Diffusion
+ *     Large Language Models": §3.3.2 Eq. (1) (token-wise operators and their
+ *     cache), §3.3.3 Eq. (2)-(6) and Algorithm 1 (FACache).
+ *   - "Flash-dLLM: IO-aware KV caching ..." news write-up, section
+ *     "Flash-Cache: Fusing Projection, RoPE, and Cache Writes into One Kernel"
+ *     (fused projection + RoPE + single KV write; block table for ragged
+ *     batches; flat pre-allocated cache).
+ *   - "Fast-dLLM Block-wise DualCache" docs: sections "Block-wise Generation",
+ *     "DualCache Data Structure", "Building the Dual Cache Manually".
+ *
+ * Conventions for every entry point
+ *   - Memory: the caller owns every buffer.  The library allocates nothing and
+ *     keeps no global mutable state.  Pointers named "device" must be device
+ *     memory of the current device; structs are read on the host during the
+ *     call only.
+ *   - Execution: asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream).  No call synchronises or reads device
+ *     memory on the host; host scalars in dllm_batch size the launch grids.
+ *   - Errors: arguments are validated on the host before any launch; on a
+ *     failed validation the call returns a non-zero status and launches
+ *     nothing.  A launch failure returns DLLM_ERR_CUDA.  Device-side checks
+ *     (block-table entries outside [0, num_pages), per-sequence metadata that
+ *     contradicts the host bounds, a bounded wait that ran out) skip the
+ *     offending access and OR a DLLM_DEVERR_* bit into *batch->error_flag
+ *     when that pointer is non-NULL; outputs are then undefined.
+ *   - Thread safety: calls on different streams are safe when their outputs
+ *     do not overlap.
+ *
+ * Layouts (all row-major, little-endian, bf16 = IEEE bfloat16)
+ *   page      = 64 consecutive token positions of one sequence.
+ *   k_pool, v_pool, q_pool: bf16 [num_pages][n_heads][64][head_dim]
+ *   m_pool, l_pool:         fp32 [num_pages][n_heads][64]
+ *   o_pool:                 fp32 [num_pages][n_heads][64][head_dim]
+ *   token at position p of sequence b lives at page block_table[b][p / 64],
+ *   slot p % 64.
+ *   w_qkv:   bf16 [3 * n_heads * head_dim][d_model]; rows are Q heads, then K
+ *            heads, then V heads, head-major, head_dim rows per head.
+ *   rms_gain: bf16 [d_model].
+ *   rope_table: fp32 [rope_max_pos][head_dim / 2][2] = (cos, sin) of
+ *            p * rope_theta^(-2i/head_dim); filled by dllm_rope_table_build.
+ *   x_block, q_block: rows of the current blocks packed in sequence order,
+ *            cu_block[b] .. cu_block[b+1]-1.  x_block bf16 [M][d_model],
+ *            q_block bf16 [M][n_heads][head_dim].
+ *   x_full, o_full: all rows of all sequences packed in sequence order,
+ *            cu_seq[b] .. cu_seq[b+1]-1.  x_full bf16 [R][d_model],
+ *            o_full bf16 [R][n_heads][head_dim], lse fp32 [R][n_heads].
+ */
+#ifndef DLLM_H_
+#define DLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dllm_status {
+  DLLM_OK = 0,
+  DLLM_ERR_INVALID_ARGUMENT = 1,     /* NULL/misaligned pointer, inconsistent sizes */
+  DLLM_ERR_UNSUPPORTED = 2,          /* head_dim not in {64,128}, page_size != 64, ... */
+  DLLM_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below dllm_workspace_size() */
+  DLLM_ERR_CUDA = 4,                 /* a CUDA runtime/driver call or launch failed */
+  DLLM_ERR_TIMEOUT = 5               /* reserved for host-observed device timeouts */
+} dllm_status;
+
+/* Bits a kernel ORs into *dllm_batch.error_flag (device int32). */
+#define DLLM_DEVERR_TIMEOUT 1   /* a bounded on-chip wait gave up */
+#define DLLM_DEVERR_BAD_PAGE 2  /* block_table entry outside [0, num_pages) */
+#define DLLM_DEVERR_BAD_SHAPE 4 /* seq_len/block_start/block_len/cu_* contradict the host bounds */
+
+/* Shape of one attention layer. */
+typedef struct dllm_layer_desc {
+  int32_t d_model;     /* D: multiple of 64 */
+  int32_t n_heads;     /* H: 3*H*head_dim must be a multiple of 128 */
+  int32_t head_dim;    /* d: 64 or 128 */
+  int32_t page_size;   /* tokens per cache page: must be 64 */
+  float rope_theta;    /* RoPE base (e.g. 10000, 500000) */
+  float rms_eps;       /* RMSNorm epsilon */
+  float softmax_scale; /* scale of q.k; 0 selects 1/sqrt(head_dim) */
+} dllm_layer_desc;
+
+/* The paged cache of one layer (device buffers, caller-owned). */
+typedef struct dllm_cache {
+  void* k_pool;      /* bf16 [num_pages][H][64][d]: RoPE'd keys of every position */
+  void* v_pool;      /* bf16 [num_pages][H][64][d]: values */
+  void* q_pool;      /* bf16 [num_pages][H][64][d]: RoPE'd queries of U rows */
+  float* m_pool;     /* fp32 [num_pages][H][64]: cached row max over U keys (natural units of scale*q.k) */
+  float* l_pool;     /* fp32 [num_pages][H][64]: cached sum of exp(S - m) over U keys */
+  float* o_pool;     /* fp32 [num_pages][H][64][d]: cached unnormalised sum of exp(S - m) v over U keys */
+  int32_t num_pages; /* pages in each pool; num_pages*H*64 < 2^31 */
+} dllm_cache;
+
+/* A ragged batch.  Host scalars bound the device arrays and size the grids. */
+typedef struct dllm_batch {
+  int32_t batch;             /* number of sequences (>= 0) */
+  int32_t max_pages_per_seq; /* row stride of block_table; >= ceil(N_b / 64) for every b */
+  int32_t total_block_rows;  /* M = sum_b B_b = cu_block[batch] */
+  int32_t total_seq_rows;    /* R = sum_b N_b = cu_seq[batch] */
+  int32_t max_block_len;     /* >= every B_b; at most 64 */
+  int32_t max_seq_len;       /* >= every N_b */
+  const int32_t* block_table; /* device int32 [batch][max_pages_per_seq]: physical page ids */
+  const int32_t* seq_len;     /* device int32 [batch]: N_b >= 1 */
+  const int32_t* block_start; /* device int32 [batch]: s_b, 0 <= s_b, s_b + B_b <= N_b */
+  const int32_t* block_len;   /* device int32 [batch]: B_b, 1 <= B_b <= max_block_len */
+  const int32_t* cu_block;    /* device int32 [batch + 1]: prefix sums of B_b */
+  const int32_t* cu_seq;      /* device int32 [batch + 1]: prefix sums of N_b */
+  int32_t* error_flag;        /* device int32, nullable: DLLM_DEVERR_* bits are ORed in */
+} dllm_batch;
+
+/* Operation ids for dllm_workspace_size. */
+#define DLLM_OP_CACHE_BUILD 0
+#define DLLM_OP_BLOCK_QKV_ROPE_WRITE 1
+#define DLLM_OP_BLOCK_ATTENTION 2
+#define DLLM_OP_STATE_MERGE 3
+
+/* Bytes of device workspace `op` needs for this layer and batch (0 if none).
+ * The workspace is scratch owned by the caller, 256-byte aligned, and may be
+ * reused once the call's work on its stream has completed. */
+dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t op, size_t* bytes);
+
+/* Fill the RoPE table (device fp32 [max_pos][head_dim/2][2]) with
+ * (cos, sin) of p * rope_theta^(-2i/head_dim), computed in fp64 on the device
+ * and rounded to fp32.  RoPE: LaCache Eq. (1); rotate-half pairs (i, i+d/2). */
+dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, float* rope_table, void* stream);
+
+/* Block boundary (LaCache Algorithm 1 with GenStep = True; Fast-dLLM
+ * compute_block_dual_cache).  For every row of every sequence:
+ *   x^ = RMSNorm(x) (fp32, rounded to bf16), [q k v] = x^ W_qkv^T (fp32
+ *   accumulation), RoPE(q, k) at position p, and k, v (and q for rows of U)
+ *   written as bf16 into the pools.  Pool positions p >= N_b of each
+ *   sequence's last page are set to zero.
+ * Then for every row r of U_b = [0, N_b) \ [s_b, s_b + B_b) and head h, the
+ * online-softmax state over the keys of U_b only (LaCache §3.3.3):
+ *   m = max_{j in U} S_rj, l = sum_{j in U} exp(S_rj - m),
+ *   O~ = sum_{j in U} exp(S_rj - m) v_j,   S_rj = scale * q_r . k_j,
+ * written to m_pool, l_pool, o_pool at row r's slot.  If U_b is empty for a
+ * row's keys, m = -inf, l = 0, O~ = 0.
+ *   x_full: device bf16 [R][d_model]; rms_gain: device bf16 [d_model];
+ *   w_qkv: device bf16 [3*H*d][d_model]; rope_table: device fp32, rope_max_pos
+ *   >= max_seq_len positions; ws: device scratch of
+ *   dllm_workspace_size(DLLM_OP_CACHE_BUILD) bytes. */
+dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_full,
+                             const void* rms_gain, const void* w_qkv, const float* rope_table, int32_t rope_max_pos,
+                             const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream);
+
+/* Inner step, part 1 (LaCache §3.3.2 Eq. (1); Flash-dLLM Flash-Cache): for
+ * the B_b rows of each current block only, x^ = RMSNorm(x_block) rounded to
+ * bf16, [q k v] = x^ W_qkv^T with fp32 accumulation, RoPE(q, k) at absolute
+ * position p = s_b + i, then one write: k, v as bf16 into k_pool / v_pool at
+ * (block_table[b][p/64], h, p%64) and q as bf16 into q_block [M][H][d].
+ *   x_block: device bf16 [M][d_model]; q_block: device bf16 [M][H][d];
+ *   ws: dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) bytes. */
+dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_block,
+                                      const void* rms_gain, const void* w_qkv, const float* rope_table,
+                                      int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/* Inner step, part 2 (LaCache Eq. (2)-(6); Fast-dLLM DualCache "Inner step on
+ * block k"): for each block row i of sequence b and head h,
+ *   O = sum_j softmax_j(scale * q_i . k_j) v_j over ALL keys j in [0, N_b)
+ * read through block_table (prefix | fresh block | suffix), written as bf16 to
+ * o_full row cu_seq[b] + s_b + i, and L = m + ln l to lse (nullable) at the
+ * same row.  q_block as written by dllm_block_qkv_rope_write; the pools as
+ * written by dllm_cache_build and this step's dllm_block_qkv_rope_write.
+ *   ws: dllm_workspace_size(DLLM_OP_BLOCK_ATTENTION) bytes (currently 0). */
+dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Inner step, part 3 (LaCache §3.3.3 and Algorithm 1 with GenStep = False):
+ * for every row r of U_b and head h, start from the cached state (m, l, O~)
+ * of dllm_cache_build, stream only the B_b fresh block keys (read through
+ * block_table at positions s_b .. s_b+B_b-1):
+ *   m' = max_c S_rc, l' = sum_c exp(S_rc - m'), O' = sum_c exp(S_rc - m') v_c,
+ *   m* = max(m, m'), l* = e^(m-m*) l + e^(m'-m*) l',
+ *   O_r = (e^(m-m*) O~ + e^(m'-m*) O') / l*,  L_r = m* + ln l*,
+ * and write O_r as bf16 to o_full row cu_seq[b] + r (and L_r to lse when
+ * non-NULL).  The cache is read-only.
+ *   ws: dllm_workspace_size(DLLM_OP_STATE_MERGE) bytes (currently 0). */
+dllm_status dllm_state_merge(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_cache* cache,
+                             void* o_full, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* dllm_status_string(dllm_status status);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* DLLM_H_ */
