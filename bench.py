@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Throughput of the per-layer inner denoising step of block-wise
+diffusion-LLM decoding on GB300.
+
+One step = one pass of the whole hot path for one layer: the fused RMSNorm +
+QKV projection + RoPE + paged K/V write of the block rows, the block
+attention over [prefix | block | suffix], and the FACache merge of every
+invariant row.  The metric is block-query tokens per second per layer-step
+(block rows of all sequences / step time).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: the LLaDA-8B-shaped single layer (batch 1, d_model 4096, 32 heads
+x 128, RoPE theta 5e5, prompt 512, gen 256, block 32), synthetic seeded
+bf16 inputs and N(0, 0.02) weights.  Steps rotate over several independent
+layer instances (about 140 MB each), so no step finds its inputs in the
+129 MB L2.  Each step is three CUDA-graph launches (one per C-ABI call) with
+CUDA events between them on the launching stream; the projection call's
+events give its live duration for the roofline.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload
+(sequences are independent units: weak scaling, no collective on the data
+path); the time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (full recompute of the step) on
+the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llada_single"
+METRIC = "block-query tokens/s per layer-step"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def step_bytes_flops(cfg, st):
+    """Algorithmic bytes and flops of one layer-step (what the method must
+    move and compute), per part."""
+    D, H, d = cfg.d_model, cfg.n_heads, cfg.head_dim
+    HD = H * d
+    lay = st.batch.host
+    M = int(lay["block_len"].sum())
+    N = lay["seq_len"].astype(np.int64)
+    B = lay["block_len"].astype(np.int64)
+    NU = N - B
+    qkv_bytes = 3 * HD * D * 2 + M * D * 2 + 3 * M * HD * 2
+    qkv_flops = 6 * M * D * HD
+    att_bytes = int((N * HD * 4).sum()) + 2 * M * HD * 2
+    att_flops = int((4 * B * N * HD).sum())
+    mrg_bytes = int((NU * HD * 8).sum()) + int(NU.sum()) * H * 8
+    mrg_flops = int((4 * NU * B * HD).sum())
+    return dict(qkv=(qkv_bytes, qkv_flops), attention=(att_bytes, att_flops), merge=(mrg_bytes, mrg_flops))
+
+
+def run_ours(args, rank, ws, local):
+    from block_wise_kv_gb300 import build, dllm
+    from block_wise_kv_gb300.inputs import Workload, make_config
+    from block_wise_kv_gb300.step import LayerStep, block_rows_of, full_rows_of
+
+    if rank == 0:
+        build.build()
+    _barrier(ws)
+    dllm.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = make_config(args.config)
+    wl = Workload(cfg.with_(seed=rank))
+    blocks = cfg.block_index
+    L = args.layers
+    inst = []
+    for layer in range(L):
+        st = LayerStep(cfg, layer=layer)
+        st.boundary(full_rows_of(wl, layer, 0, blocks).to(dev))
+        xb = block_rows_of(wl, layer, 1, blocks).to(dev)
+        inst.append((st, xb))
+    torch.cuda.synchronize()
+    for st, _ in inst:
+        assert st.batch.error_bits() == 0, "device-side error during setup"
+    M = inst[0][0].batch.total_block_rows
+
+    # one graph per C-ABI call of each instance
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for st, xb in inst:
+            st.step(xb)
+        stream.synchronize()
+        for st, xb in inst:
+            gs = []
+            for fn in (lambda: st.qkv(xb), lambda: st.attention(), lambda: st.merge()):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                gs.append(g)
+            graphs.append(gs)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        for g in graphs[i % L]:
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks, torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        for i in range(K):
+            e = ev[i]
+            gq, ga, gm = graphs[i % L]
+            e[0].record(stream)
+            gq.replay()
+            e[1].record(stream)
+            ga.replay()
+            e[2].record(stream)
+            gm.replay()
+            e[3].record(stream)
+        stream.synchronize()
+        t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    total_ms = ev[0][0].elapsed_time(ev[-1][3])
+    part_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j in range(3)]
+    total_ms = _max_over_ranks(total_ms, ws)
+    for st, _ in inst:
+        assert st.batch.error_bits() == 0, "device-side error during the timed steps"
+
+    # end to end through the public API: pinned host input -> step -> host output
+    x_host = [xb.cpu().pin_memory() for _, xb in inst]
+    o_host = [torch.empty_like(st.o_full, device="cpu").pin_memory() for st, _ in inst]
+    x_dev = [torch.empty_like(xb) for _, xb in inst]
+    Ke = max(1, min(K, args.e2e_steps))
+    for i in range(min(W, 8)):
+        st, _ = inst[i % L]
+        x_dev[i % L].copy_(x_host[i % L], non_blocking=True)
+        st.step(x_dev[i % L])
+        o_host[i % L].copy_(st.o_full, non_blocking=True)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(Ke):
+        j = i % L
+        st, _ = inst[j]
+        x_dev[j].copy_(x_host[j], non_blocking=True)
+        st.step(x_dev[j])
+        o_host[j].copy_(st.o_full, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
+    h2d = x_host[0].numel() * x_host[0].element_size()
+    d2h = o_host[0].numel() * o_host[0].element_size()
+
+    if rank != 0:
+        return None
+    hbm, tf_burst, tf_sus, peak_kind = _peaks()
+    bf = step_bytes_flops(cfg, inst[0][0])
+    qkv_bytes, qkv_flops = bf["qkv"]
+    t_qkv = part_ms[0] * 1e-3
+    achieved = qkv_bytes / t_qkv / 1e9
+    value = K * M * ws / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: 1 layer, batch 1, d_model 4096, 32x128 heads, prompt 512, gen 256, "
+                               "block 32 (M=32, N=768)",
+                   "l2": f"inputs larger than L2: {L} rotating layer instances (~140 MB each)",
+                   "parallelism": f"replicas x{ws} (sequences are independent units)"},
+        "parts_us": {"qkv_rope_write": part_ms[0] * 1e3, "block_attention": part_ms[1] * 1e3,
+                     "state_merge": part_ms[2] * 1e3},
+        "roofline": {"kernel": "dllm_block_qkv_rope_write (RMSNorm + tcgen05 QKV GEMM with RoPE/paged-write "
+                               "epilogue)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "algorithmic_bytes": qkv_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(Ke * M * ws / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": 4 * K,
+        "host_wall_s": t1 - t0,
+    }
+    cl = clocks.summary()
+    line["clocks"] = cl
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    return line
+
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(cfg, wl, step):
+    """fp64 inputs of the oracle for sequence 0 at the given inner step
+    (generated once, outside any timed region)."""
+    key = (cfg.name, step)
+    if key not in _ORACLE_INPUTS:
+        W, g = wl.weights(0)
+        x = wl.seq_rows(0, 0, cfg.block_index[0], step).double().numpy()
+        _ORACLE_INPUTS[key] = (x, g.double().numpy(), W.double().numpy())
+    return _ORACLE_INPUTS[key]
+
+
+def _oracle_sample(cfg, wl, heads, step):
+    """The oracle's full-recompute layer step restricted to `heads` (every
+    row's output for those heads; RMSNorm, K/V of all rows, attention)."""
+    import oracle as orc
+
+    x, g, W = _oracle_inputs(cfg, wl, step)
+    return orc.layer_step(x, g, W, cfg.n_heads, cfg.head_dim, cfg.rope_theta, cfg.rms_eps, heads=heads)
+
+
+def cpu_baseline(cfg, seconds: float):
+    """The oracle as it stands, timed on this host's cores on a bounded
+    sample: the full step for one head at a time, repeated for about
+    `seconds`, scaled to all heads."""
+    import oracle as orc
+    from block_wise_kv_gb300.inputs import Workload
+
+    wl = Workload(cfg)
+    M = sum(cfg.block)
+    _oracle_sample(cfg, wl, [0], 1)  # warm: builds/loads the library, generates the inputs
+    n, t = 0, 0.0
+    while t < seconds and n < cfg.n_heads:
+        t0 = time.perf_counter()
+        _oracle_sample(cfg, wl, [n % cfg.n_heads], 1)
+        t += time.perf_counter() - t0
+        n += 1
+    per_step = t / n * cfg.n_heads
+    return {"value": round(M / per_step, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"full-recompute layer step (fp64) for {n} of {cfg.n_heads} heads of {WORKLOAD}, "
+                      f"{t:.1f} s, scaled to all heads"}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    import oracle as orc
+    from block_wise_kv_gb300.inputs import Workload, make_config
+
+    cfg = make_config(args.config)
+    wl = Workload(cfg)
+    M = sum(cfg.block)
+    _oracle_inputs(cfg, wl, 1)
+    K, W = args.steps_ref, args.warmup_ref
+    for i in range(W):
+        _oracle_sample(cfg, wl, [i % cfg.n_heads], 1)
+    t0 = time.perf_counter()
+    for i in range(K):
+        _oracle_sample(cfg, wl, [i % cfg.n_heads], 1)
+    t = time.perf_counter() - t0
+    per_step = t / K * cfg.n_heads
+    value = M / per_step
+    sample = f"each step: full-recompute layer step (fp64) for one head of {cfg.n_heads}, scaled to all heads"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+            "steps": K, "warmup": W, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: 1 layer, batch 1, d_model 4096, 32x128 heads, prompt 512, gen "
+                                   "256, block 32 (M=32, N=768)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--layers", type=int, default=4, help="rotating layer instances (inputs larger than L2)")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, ws, local = _dist()
+    if args.impl == "reference":
+        # each reference step is one head's full recompute: keep the run to minutes
+        args.steps_ref = max(1, min(args.steps, 32))
+        args.warmup_ref = max(1, min(args.warmup, 2))
+        line = run_reference(args, rank, ws)
+    else:
+        if ws != args.gpus and rank == 0:
+            print(f"note: --gpus {args.gpus} but WORLD_SIZE {ws}", file=sys.stderr)
+        line = run_ours(args, rank, ws, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

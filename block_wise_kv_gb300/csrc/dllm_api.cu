@@ -1,0 +1,282 @@
+// dllm_api.cu — the C ABI declared in include/dllm.h: host-side validation,
+// workspace sizing and the launch sequence of each entry point.  Every check
+// runs before the first launch, so a rejected call launches nothing.
+#include <math.h>
+#include <stdint.h>
+
+#include "dllm.h"
+#include "kernels.cuh"
+
+using namespace dllm;
+
+namespace {
+
+constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;
+
+bool aligned(const void* p, uintptr_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+dllm_status check_desc(const dllm_layer_desc* d) {
+  if (d == nullptr) return DLLM_ERR_INVALID_ARGUMENT;
+  if (d->head_dim != 64 && d->head_dim != 128) return DLLM_ERR_UNSUPPORTED;
+  if (d->page_size != kPage) return DLLM_ERR_UNSUPPORTED;
+  if (d->d_model <= 0 || d->n_heads <= 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (d->d_model % 64 != 0) return DLLM_ERR_UNSUPPORTED;
+  if ((static_cast<int64_t>(d->n_heads) * d->head_dim) % 128 != 0) return DLLM_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->n_heads) * d->head_dim * 3 > 65535 * 128) return DLLM_ERR_UNSUPPORTED;
+  if (!(d->rope_theta > 0.f) || !isfinite(d->rope_theta)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(d->rms_eps >= 0.f) || !isfinite(d->rms_eps)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!(d->softmax_scale >= 0.f) || !isfinite(d->softmax_scale)) return DLLM_ERR_INVALID_ARGUMENT;
+  return DLLM_OK;
+}
+
+dllm_status check_batch(const dllm_batch* b) {
+  if (b == nullptr || b->batch < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->batch == 0) return DLLM_OK;
+  if (b->batch > 65535) return DLLM_ERR_UNSUPPORTED;
+  if (!aligned(b->block_table, 4) || !aligned(b->seq_len, 4) || !aligned(b->block_start, 4) ||
+      !aligned(b->block_len, 4) || !aligned(b->cu_block, 4) || !aligned(b->cu_seq, 4))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->error_flag != nullptr && !aligned(b->error_flag, 4)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->max_pages_per_seq < 1 || b->max_seq_len < 1 || b->max_block_len < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->max_block_len > 64) return DLLM_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(b->max_pages_per_seq) * kPage < b->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->max_seq_len > 65535 * kPage) return DLLM_ERR_UNSUPPORTED;
+  if (b->total_block_rows < 0 || b->total_seq_rows < 0) return DLLM_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(b->total_block_rows) > static_cast<int64_t>(b->batch) * b->max_block_len)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(b->total_seq_rows) > static_cast<int64_t>(b->batch) * b->max_seq_len)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (b->total_block_rows > b->total_seq_rows) return DLLM_ERR_INVALID_ARGUMENT;
+  return DLLM_OK;
+}
+
+dllm_status check_cache(const dllm_cache* c, const dllm_layer_desc* d, bool need_q, bool need_state) {
+  if (c == nullptr || c->num_pages < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(c->num_pages) * d->n_heads * kPage > kMaxRows) return DLLM_ERR_UNSUPPORTED;
+  if (!aligned(c->k_pool, 16) || !aligned(c->v_pool, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (need_q && !aligned(c->q_pool, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (need_state && (!aligned(c->m_pool, 16) || !aligned(c->l_pool, 16) || !aligned(c->o_pool, 16)))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  return DLLM_OK;
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+BatchArgs batch_args(const dllm_batch* b, const dllm_cache* c) {
+  BatchArgs a;
+  a.block_table = b->block_table;
+  a.seq_len = b->seq_len;
+  a.block_start = b->block_start;
+  a.block_len = b->block_len;
+  a.cu_block = b->cu_block;
+  a.cu_seq = b->cu_seq;
+  a.err = b->error_flag;
+  a.batch = b->batch;
+  a.max_pages = b->max_pages_per_seq;
+  a.num_pages = c->num_pages;
+  a.max_block_len = b->max_block_len;
+  a.max_seq_len = b->max_seq_len;
+  a.total_block_rows = b->total_block_rows;
+  a.total_seq_rows = b->total_seq_rows;
+  return a;
+}
+
+float softmax_scale(const dllm_layer_desc* d) {
+  return d->softmax_scale > 0.f ? d->softmax_scale : static_cast<float>(1.0 / sqrt(static_cast<double>(d->head_dim)));
+}
+
+AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache* c) {
+  AttnArgs a;
+  a.bt = batch_args(b, c);
+  a.q_block = nullptr;
+  a.k_pool = c->k_pool;
+  a.v_pool = c->v_pool;
+  a.q_pool = c->q_pool;
+  a.m_pool = c->m_pool;
+  a.l_pool = c->l_pool;
+  a.o_pool = c->o_pool;
+  a.o_full = nullptr;
+  a.lse = nullptr;
+  a.n_heads = d->n_heads;
+  a.head_dim = d->head_dim;
+  a.scale_log2 = softmax_scale(d) * 1.4426950408889634f;
+  return a;
+}
+
+QkvArgs qkv_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache* c, const float* rope,
+                 int32_t rope_max_pos, int mode, int n_tok) {
+  QkvArgs a;
+  a.bt = batch_args(b, c);
+  a.k_pool = c->k_pool;
+  a.v_pool = c->v_pool;
+  a.q_pool = c->q_pool;
+  a.q_block = nullptr;
+  a.rope = rope;
+  a.rope_max_pos = rope_max_pos;
+  a.n_heads = d->n_heads;
+  a.head_dim = d->head_dim;
+  a.d_model = d->d_model;
+  a.n_tok = n_tok;
+  a.mode = mode;
+  return a;
+}
+
+dllm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA; }
+
+#define DLLM_TRY(expr)                     \
+  do {                                     \
+    const dllm_status s_ = (expr);         \
+    if (s_ != DLLM_OK) return s_;          \
+  } while (0)
+
+#define DLLM_CUDA_TRY(expr)                \
+  do {                                     \
+    const cudaError_t e_ = (expr);         \
+    if (e_ != cudaSuccess) return DLLM_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t op, size_t* bytes) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (bytes == nullptr) return DLLM_ERR_INVALID_ARGUMENT;
+  const size_t row = static_cast<size_t>(desc->d_model) * 2;
+  switch (op) {
+    case DLLM_OP_CACHE_BUILD:
+      *bytes = batch->batch > 0 ? align256(static_cast<size_t>(batch->total_seq_rows) * row) : 0;
+      return DLLM_OK;
+    case DLLM_OP_BLOCK_QKV_ROPE_WRITE:
+      *bytes = batch->batch > 0 ? align256(static_cast<size_t>(batch->total_block_rows) * row) : 0;
+      return DLLM_OK;
+    case DLLM_OP_BLOCK_ATTENTION:
+    case DLLM_OP_STATE_MERGE:
+      *bytes = 0;
+      return DLLM_OK;
+    default:
+      return DLLM_ERR_INVALID_ARGUMENT;
+  }
+}
+
+dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, float* rope_table, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  if (max_pos < 1 || !aligned(rope_table, 8)) return DLLM_ERR_INVALID_ARGUMENT;
+  return cuda_status(launch_rope_table(rope_table, max_pos, desc->head_dim, static_cast<double>(desc->rope_theta),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_full,
+                             const void* rms_gain, const void* w_qkv, const float* rope_table, int32_t rope_max_pos,
+                             const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, true, true));
+  if (!aligned(x_full, 16) || !aligned(rms_gain, 16) || !aligned(w_qkv, 16) || !aligned(rope_table, 8))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
+  size_t need = 0;
+  DLLM_TRY(dllm_workspace_size(desc, batch, DLLM_OP_CACHE_BUILD, &need));
+  if (ws_bytes < need) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const BatchArgs bt = batch_args(batch, cache);
+  DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
+  DLLM_CUDA_TRY(launch_rmsnorm(x_full, rms_gain, ws, batch->total_seq_rows, desc->d_model, desc->rms_eps, s));
+  const QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBoundary, batch->total_seq_rows);
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, device_sms(), s));
+  const AttnArgs aa = attn_args(desc, batch, cache);
+  DLLM_CUDA_TRY(launch_state_build(aa, s));
+  return DLLM_OK;
+}
+
+dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_block,
+                                      const void* rms_gain, const void* w_qkv, const float* rope_table,
+                                      int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, false, false));
+  if (!aligned(x_block, 16) || !aligned(rms_gain, 16) || !aligned(w_qkv, 16) || !aligned(rope_table, 8) ||
+      !aligned(q_block, 16))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
+  size_t need = 0;
+  DLLM_TRY(dllm_workspace_size(desc, batch, DLLM_OP_BLOCK_QKV_ROPE_WRITE, &need));
+  if (ws_bytes < need) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  DLLM_CUDA_TRY(launch_rmsnorm(x_block, rms_gain, ws, batch->total_block_rows, desc->d_model, desc->rms_eps, s));
+  QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBlock, batch->total_block_rows);
+  qa.q_block = q_block;
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, device_sms(), s));
+  return DLLM_OK;
+}
+
+dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, false, false));
+  if (!aligned(q_block, 16) || !aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (lse != nullptr && !aligned(lse, 4)) return DLLM_ERR_INVALID_ARGUMENT;
+  AttnArgs aa = attn_args(desc, batch, cache);
+  aa.q_block = q_block;
+  aa.o_full = o_full;
+  aa.lse = lse;
+  DLLM_CUDA_TRY(launch_block_attention(aa, device_sms(), static_cast<cudaStream_t>(stream)));
+  return DLLM_OK;
+}
+
+dllm_status dllm_state_merge(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_cache* cache,
+                             void* o_full, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, true, true));
+  if (!aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (lse != nullptr && !aligned(lse, 4)) return DLLM_ERR_INVALID_ARGUMENT;
+  AttnArgs aa = attn_args(desc, batch, cache);
+  aa.o_full = o_full;
+  aa.lse = lse;
+  DLLM_CUDA_TRY(launch_state_merge(aa, static_cast<cudaStream_t>(stream)));
+  return DLLM_OK;
+}
+
+const char* dllm_status_string(dllm_status status) {
+  switch (status) {
+    case DLLM_OK:
+      return "ok";
+    case DLLM_ERR_INVALID_ARGUMENT:
+      return "invalid argument";
+    case DLLM_ERR_UNSUPPORTED:
+      return "unsupported shape or configuration";
+    case DLLM_ERR_WORKSPACE_TOO_SMALL:
+      return "workspace too small";
+    case DLLM_ERR_CUDA:
+      return "CUDA error";
+    case DLLM_ERR_TIMEOUT:
+      return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// kernels.cuh — internal interface between the C ABI (dllm_api.cu) and the
+// kernel translation units.  Not installed; include/dllm.h is the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dllm {
+
+constexpr int kPage = 64;  // tokens per cache page
+
+// Batch metadata as the kernels see it: device arrays plus the host bounds
+// that every device-side check compares against.
+struct BatchArgs {
+  const int32_t* block_table;  // [batch][max_pages]
+  const int32_t* seq_len;      // [batch]
+  const int32_t* block_start;  // [batch]
+  const int32_t* block_len;    // [batch]
+  const int32_t* cu_block;     // [batch + 1]
+  const int32_t* cu_seq;       // [batch + 1]
+  int32_t* err;                // nullable error word
+  int32_t batch;
+  int32_t max_pages;
+  int32_t num_pages;
+  int32_t max_block_len;
+  int32_t max_seq_len;
+  int32_t total_block_rows;  // rows of x_block / q_block
+  int32_t total_seq_rows;    // rows of x_full / o_full / lse
+};
+
+// Arguments of the fused projection kernel's epilogue.
+struct QkvArgs {
+  BatchArgs bt;
+  void* k_pool;                // bf16 [P][H][64][d]
+  void* v_pool;
+  void* q_pool;                // boundary mode: queries of U rows
+  void* q_block;               // step mode: bf16 [M][H][d]
+  const float* rope;           // fp32 [rope_max_pos][d/2][2]
+  int32_t rope_max_pos;
+  int32_t n_heads;
+  int32_t head_dim;
+  int32_t d_model;
+  int32_t n_tok;               // rows of the x^ operand
+  int32_t mode;                // kModeBlock or kModeBoundary
+};
+constexpr int kModeBlock = 0;     // tokens are the packed block rows (cu_block)
+constexpr int kModeBoundary = 1;  // tokens are all rows of every sequence (cu_seq)
+
+struct AttnArgs {
+  BatchArgs bt;
+  const void* q_block;  // block attention: bf16 [M][H][d]
+  const void* k_pool;   // bf16 [P][H][64][d]
+  const void* v_pool;
+  const void* q_pool;
+  float* m_pool;        // fp32 [P][H][64]: written by the state build, read by the merge
+  float* l_pool;
+  float* o_pool;        // fp32 [P][H][64][d]
+  void* o_full;         // bf16 [R][H][d]
+  float* lse;           // fp32 [R][H], nullable
+  int32_t n_heads;
+  int32_t head_dim;
+  float scale_log2;     // softmax_scale * log2(e)
+};
+
+// ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
+// Each launcher encodes the TMA tensor maps it needs from the raw pointers.
+cudaError_t launch_rmsnorm(const void* x, const void* gain, void* out, int rows, int d_model, float eps,
+                           cudaStream_t stream);
+cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double theta, cudaStream_t stream);
+cudaError_t launch_zero_tails(const BatchArgs& bt, void* k_pool, void* v_pool, void* q_pool, int n_heads,
+                              int head_dim, cudaStream_t stream);
+cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_block_attention(const AttnArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_state_build(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_state_merge(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace dllm

@@ -1,0 +1,95 @@
+"""Device state of one layer for one ragged batch, and the call sequence of
+a block boundary and of an inner denoising step through the C ABI.
+
+Nothing here computes: it allocates with torch, fills the C structs and
+calls ``dllm_*`` in the order the method defines (Fast-dLLM DualCache,
+"Building the Dual Cache Manually": the cache is built at each block
+boundary, then every inner step runs on the block rows only).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import dllm
+from .inputs import Config, Workload, layout
+
+
+class LayerStep:
+    """One layer's weights, RoPE table, paged cache, workspaces and outputs
+    for the batch layout of `cfg` (block k_b of each sequence)."""
+
+    def __init__(self, cfg: Config, layer: int = 0, blocks=None, device: str = "cuda", cache_fill=None,
+                 weights=None, rope_max_pos: int | None = None):
+        self.cfg = cfg
+        self.device = device
+        wl = Workload(cfg)
+        W, g = weights if weights is not None else wl.weights(layer)
+        self.w_qkv = W.to(device).contiguous()
+        self.gain = g.to(device).contiguous()
+        lay = layout(cfg, blocks)
+        self.host_layout = lay
+        self.batch = dllm.BatchLayout(lay["block_table"], lay["seq_len"], lay["block_start"], lay["block_len"],
+                                      device=device)
+        self.desc = dllm.layer_desc(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.rope_theta, cfg.rms_eps)
+        self.rope_max_pos = int(rope_max_pos or self.batch.max_seq_len)
+        self.rope = torch.empty(self.rope_max_pos, cfg.head_dim // 2, 2, dtype=torch.float32, device=device)
+        dllm.dllm_rope_table_build(self.desc, self.rope_max_pos, self.rope)
+        self.cache = dllm.PagedCache(lay["num_pages"], cfg.n_heads, cfg.head_dim, device=device, fill=cache_fill)
+        self.ws_build = dllm.workspace(dllm.dllm_workspace_size(self.desc, self.batch.c, dllm.DLLM_OP_CACHE_BUILD),
+                                       device)
+        self.ws_step = dllm.workspace(
+            dllm.dllm_workspace_size(self.desc, self.batch.c, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE), device)
+        H, d = cfg.n_heads, cfg.head_dim
+        self.q_block = torch.zeros(self.batch.total_block_rows, H, d, dtype=torch.bfloat16, device=device)
+        self.o_full = torch.zeros(self.batch.total_seq_rows, H, d, dtype=torch.bfloat16, device=device)
+        self.lse = torch.zeros(self.batch.total_seq_rows, H, dtype=torch.float32, device=device)
+
+    # ------------------------------------------------------------ the calls
+    def boundary(self, x_full: torch.Tensor, stream=None) -> None:
+        dllm.dllm_cache_build(self.desc, self.batch.c, x_full, self.gain, self.w_qkv, self.rope, self.rope_max_pos,
+                              self.cache.c, self.ws_build, stream)
+
+    def qkv(self, x_block: torch.Tensor, stream=None) -> None:
+        dllm.dllm_block_qkv_rope_write(self.desc, self.batch.c, x_block, self.gain, self.w_qkv, self.rope,
+                                       self.rope_max_pos, self.cache.c, self.q_block, self.ws_step, stream)
+
+    def attention(self, stream=None, lse: bool = True) -> None:
+        dllm.dllm_block_attention(self.desc, self.batch.c, self.q_block, self.cache.c, self.o_full,
+                                  self.lse if lse else None, None, stream)
+
+    def merge(self, stream=None, lse: bool = True) -> None:
+        dllm.dllm_state_merge(self.desc, self.batch.c, self.cache.c, self.o_full, self.lse if lse else None, None,
+                              stream)
+
+    def step(self, x_block: torch.Tensor, stream=None, lse: bool = True) -> None:
+        """One inner denoising step of this layer: fused projection, block
+        attention, and the FACache merge for the invariant rows."""
+        self.qkv(x_block, stream)
+        self.attention(stream, lse)
+        self.merge(stream, lse)
+
+    # ---------------------------------------------------------- inspection
+    def seq_slice(self, b: int) -> slice:
+        cu = self.batch.host["cu_seq"]
+        return slice(int(cu[b]), int(cu[b + 1]))
+
+    def block_slice(self, b: int) -> slice:
+        cu = self.batch.host["cu_block"]
+        return slice(int(cu[b]), int(cu[b + 1]))
+
+    def pool_rows(self, pool: torch.Tensor, b: int) -> torch.Tensor:
+        n = int(self.batch.host["seq_len"][b])
+        return dllm.gather_rows(pool, self.batch.host["block_table"], b, n)
+
+
+def block_rows_of(wl: Workload, layer: int, step: int, blocks) -> torch.Tensor:
+    cfg = wl.cfg
+    return torch.cat([wl.block_rows(layer, b, blocks[b], step) for b in range(cfg.batch)], 0).contiguous()
+
+
+def full_rows_of(wl: Workload, layer: int, step: int, blocks) -> torch.Tensor:
+    cfg = wl.cfg
+    return torch.cat([wl.seq_rows(layer, b, blocks[b], step) for b in range(cfg.batch)], 0).contiguous()
+
+
+__all__ = ["LayerStep", "block_rows_of", "full_rows_of"]

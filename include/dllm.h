@@ -90,7 +90,7 @@ typedef enum dllm_status {
 /* Shape of one attention layer. */
 typedef struct dllm_layer_desc {
   int32_t d_model;     /* D: multiple of 64 */
-  int32_t n_heads;     /* H: 3*H*head_dim must be a multiple of 128 */
+  int32_t n_heads;     /* H: H*head_dim must be a multiple of 128 */
   int32_t head_dim;    /* d: 64 or 128 */
   int32_t page_size;   /* tokens per cache page: must be 64 */
   float rope_theta;    /* RoPE base (e.g. 10000, 500000) */

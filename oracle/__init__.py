@@ -135,7 +135,7 @@ def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
 
 
 def linear(x: np.ndarray, W: np.ndarray) -> np.ndarray:
-    """x [rows, D] times W^T, W stored [nout, D]."""
+    """x [rows, D] times W^T, W stored [nout, D]: the plain C triple loop."""
     x, W = _c(x), _c(W)
     rows, D = x.shape
     nout = W.shape[0]
@@ -220,6 +220,13 @@ def alg1(q, k, v, scale: float, c_lo: int, c_hi: int, br: int, bc: int, genstep:
     return O, L, (mc, lc, Oc)
 
 
+def project(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """x [rows, D] times W^T through numpy's fp64 matmul (a library primitive,
+    used for the projection at full model sizes; the plain loop `linear`
+    pins it on small inputs)."""
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T)
+
+
 # ---------------------------------------------------------------- the step
 def qkv(x, g, W, n_heads: int, head_dim: int, theta: float, eps: float, pos, mirror: bool = True):
     """Token-wise part of the step (LaCache Eq. (1)) for the given rows:
@@ -229,7 +236,7 @@ def qkv(x, g, W, n_heads: int, head_dim: int, theta: float, eps: float, pos, mir
     xh = rmsnorm(x, g, eps)
     if mirror:
         xh = bf16_round(xh)
-    y = linear(xh, W)
+    y = project(xh, W)
     rows = y.shape[0]
     q = y[:, :HD].reshape(rows, n_heads, head_dim)
     k = y[:, HD:2 * HD].reshape(rows, n_heads, head_dim)
@@ -242,13 +249,14 @@ def qkv(x, g, W, n_heads: int, head_dim: int, theta: float, eps: float, pos, mir
 
 
 def layer_step(x, g, W, n_heads: int, head_dim: int, theta: float, eps: float, scale: float | None = None,
-               rows=None, mirror: bool = True):
+               rows=None, mirror: bool = True, heads=None):
     """The full-recompute definition of one layer step for ONE sequence.
 
     x [N, D] holds every row of the sequence at this step ([prefix | block |
     suffix]).  Returns dict(q, k, v, O, L) where q, O, L cover `rows` (all rows
     by default) and k, v cover all N rows.  Attention is bidirectional over all
-    N keys; positions are 0..N-1."""
+    N keys; positions are 0..N-1.  `heads` restricts the step to a subset of
+    heads (their projection rows and their attention), all heads by default."""
     x = np.asarray(x, dtype=np.float64)
     N = x.shape[0]
     if scale is None:
@@ -256,16 +264,21 @@ def layer_step(x, g, W, n_heads: int, head_dim: int, theta: float, eps: float, s
     if rows is None:
         rows = np.arange(N)
     rows = np.asarray(rows, dtype=np.int64)
-    H, d = n_heads, head_dim
-    HD = H * d
+    d = head_dim
+    HD = n_heads * d
     W = np.asarray(W, dtype=np.float64)
+    if heads is None:
+        heads = np.arange(n_heads)
+    sel = np.concatenate([np.arange(h * d, (h + 1) * d) for h in heads])
+    Wq, Wk, Wv = W[sel], W[HD + sel], W[2 * HD + sel]
+    H = len(heads)
     xh = rmsnorm(x, g, eps)
     if mirror:
         xh = bf16_round(xh)
     # K and V for every row, Q only for the requested rows.
-    k = rope(linear(xh, W[HD:2 * HD]).reshape(N, H, d), np.arange(N), theta)
-    v = linear(xh, W[2 * HD:]).reshape(N, H, d)
-    q = rope(linear(xh[rows], W[:HD]).reshape(len(rows), H, d), rows, theta)
+    k = rope(project(xh, Wk).reshape(N, H, d), np.arange(N), theta)
+    v = project(xh, Wv).reshape(N, H, d)
+    q = rope(project(xh[rows], Wq).reshape(len(rows), H, d), rows, theta)
     if mirror:
         q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
     O, L = attention(q, k, v, scale)

@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every entry point include/dllm.h declares, and rejects bad arguments on the
+host before any launch (no compute call needs a device here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_wise_kv_gb300 import build, dllm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return dllm.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dllm.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:dllm_status|const char\*)\s+(dllm_\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(dllm.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(**kw):
+    d = dict(d_model=4096, n_heads=32, head_dim=128, rope_theta=5e5)
+    d.update(kw)
+    return dllm.layer_desc(**d)
+
+
+def _batch(batch=2, max_pages=12, M=64, R=1536, max_block=32, max_seq=768):
+    fake = 0x10000  # never dereferenced: validation fails or no launch happens in these tests
+    return dllm.BatchC(batch, max_pages, M, R, max_block, max_seq, fake, fake, fake, fake, fake, fake, None)
+
+
+def test_workspace_sizes(lib):
+    d, b = _desc(), _batch()
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) == 64 * 4096 * 2
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1536 * 4096 * 2
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == 0
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STATE_MERGE) == 0
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_workspace_size(d, b, 17)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), dllm.DLLM_ERR_UNSUPPORTED),
+    (dict(d_model=4000), dllm.DLLM_ERR_UNSUPPORTED),
+    (dict(n_heads=3, head_dim=64), dllm.DLLM_ERR_UNSUPPORTED),
+    (dict(rope_theta=0.0), dllm.DLLM_ERR_INVALID_ARGUMENT),
+    (dict(rms_eps=-1.0), dllm.DLLM_ERR_INVALID_ARGUMENT),
+])
+def test_bad_layer_desc(lib, kw, status):
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_workspace_size(_desc(**kw), _batch(), dllm.DLLM_OP_BLOCK_ATTENTION)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=-1), dllm.DLLM_ERR_INVALID_ARGUMENT),
+    (dict(max_block=65), dllm.DLLM_ERR_UNSUPPORTED),
+    (dict(max_pages=2), dllm.DLLM_ERR_INVALID_ARGUMENT),   # 2 pages cannot hold 768 tokens
+    (dict(M=100), dllm.DLLM_ERR_INVALID_ARGUMENT),         # more block rows than batch * max_block_len
+    (dict(R=2000), dllm.DLLM_ERR_INVALID_ARGUMENT),        # more rows than batch * max_seq_len
+])
+def test_bad_batch(lib, kw, status):
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_workspace_size(_desc(), _batch(**kw), dllm.DLLM_OP_BLOCK_ATTENTION)
+    assert e.value.status == status
+
+
+def test_calls_reject_before_launch(lib):
+    d = _desc()
+    b = _batch()
+    cache = dllm.CacheC(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 24)
+    # misaligned output pointer
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_block_attention(d, b, 0x10000, cache, 0x10002, None, None, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+    # workspace too small
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_block_qkv_rope_write(d, b, 0x10000, 0x10000, 0x10000, 0x10000, 1024, cache, 0x10000, 0x10000, 0)
+    assert e.value.status == dllm.DLLM_ERR_WORKSPACE_TOO_SMALL
+    # RoPE table shorter than the longest sequence
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_cache_build(d, b, 0x10000, 0x10000, 0x10000, 0x10000, 100, cache, 0x10000, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+    # no cache pages
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_state_merge(d, b, dllm.CacheC(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0), 0x10000,
+                              None, None, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+
+
+def test_empty_batch_is_a_no_op(lib):
+    d = _desc()
+    b = _batch(batch=0, M=0, R=0)
+    cache = dllm.CacheC(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 0x10000, 24)
+    dllm.dllm_block_attention(d, b, 0x10000, cache, 0x10000, None, None, 0)
+    dllm.dllm_state_merge(d, b, cache, 0x10000, None, None, 0)
+
+
+def test_status_strings(lib):
+    assert dllm.dllm_status_string(dllm.DLLM_OK) == "ok"
+    assert "workspace" in dllm.dllm_status_string(dllm.DLLM_ERR_WORKSPACE_TOO_SMALL)
+    assert dllm.dllm_status_string(99) == "unknown status"

@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle.
+
+Every test runs the block boundary (dllm_cache_build) and inner steps
+(dllm_block_qkv_rope_write -> dllm_block_attention -> dllm_state_merge) on
+seeded synthetic inputs and compares all rows' outputs with the oracle's
+full recompute of the same step.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_wise_kv_gb300 import dllm
+from block_wise_kv_gb300.inputs import Config, Workload, make_config
+from block_wise_kv_gb300.step import LayerStep, block_rows_of, full_rows_of
+from parity_util import assert_bf16_close, assert_close, oracle_cache_state, oracle_step, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from block_wise_kv_gb300 import build
+
+    build.build()
+    dllm.load()
+    torch.cuda.init()
+
+
+def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=True, rows_of=None, seqs=None):
+    """Boundary of the blocks `k_of` (one per sequence) then the given inner
+    steps; every listed sequence is compared with the oracle after each step."""
+    wl = Workload(cfg)
+    W, g = wl.weights(layer)
+    st = LayerStep(cfg, layer=layer, blocks=k_of, weights=(W, g))
+    st.boundary(full_rows_of(wl, layer, 0, k_of).cuda())
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() == 0
+    seqs = range(cfg.batch) if seqs is None else seqs
+    H, d = cfg.n_heads, cfg.head_dim
+    if check_cache:
+        for b in seqs:
+            U, m, l, Ot = oracle_cache_state(wl, layer, b, k_of[b], W, g)
+            if len(U) == 0:
+                continue
+            gm = to_np(st.pool_rows(st.cache.m, b))[U]
+            gl = to_np(st.pool_rows(st.cache.l, b))[U]
+            go = to_np(st.pool_rows(st.cache.o, b))[U]
+            assert_close(gm, m, f"cache m seq {b}", max_abs=2e-2, rel=1e-3)
+            assert_close(gl / np.exp(m - gm), l, f"cache l seq {b}", max_abs=np.inf, rel=5e-3)
+            assert_close(go / gl[..., None], Ot / l[..., None], f"cache O~/l seq {b}")
+    for s in steps:
+        st.step(block_rows_of(wl, layer, s, k_of).cuda())
+        torch.cuda.synchronize()
+        assert st.batch.error_bits() == 0
+        for b in seqs:
+            rows = None if rows_of is None else rows_of(b)
+            ref = oracle_step(wl, layer, b, k_of[b], s, rows=rows, W=W, g=g)
+            o = to_np(st.o_full[st.seq_slice(b)])
+            lse = to_np(st.lse[st.seq_slice(b)])
+            sel = slice(None) if rows is None else rows
+            assert_close(o[sel], ref["O"], f"O seq {b} block {k_of[b]} step {s}")
+            assert_close(lse[sel], ref["L"], f"LSE seq {b} step {s}", max_abs=2e-2, rel=1e-3)
+            if check_qkv:
+                c0 = cfg.block_start(b, k_of[b])
+                blk = slice(c0, c0 + cfg.block[b])
+                kk = to_np(st.pool_rows(st.cache.k, b))
+                vv = to_np(st.pool_rows(st.cache.v, b))
+                assert_bf16_close(kk[blk], ref["k"][blk], f"k block rows seq {b}")
+                assert_bf16_close(vv[blk], ref["v"][blk], f"v block rows seq {b}")
+                if rows is None:
+                    qb = to_np(st.q_block[st.block_slice(b)])
+                    assert_bf16_close(qb, ref["q"][blk], f"q_block seq {b}")
+    return st
+
+
+def test_tiny_every_block_every_step():
+    cfg = make_config("tiny")
+    for k in range(cfg.num_blocks(0)):
+        _run_block(cfg, [k], range(cfg.steps_per_block))
+
+
+def test_rmsnorm_operand_is_correctly_rounded():
+    """The projection's bf16 operand (the step workspace after the call)
+    equals the oracle's x^ rounded to bf16, bit for bit."""
+    import oracle as orc
+
+    cfg = make_config("llada_single")
+    wl = Workload(cfg)
+    st = LayerStep(cfg)
+    xb = block_rows_of(wl, 0, 3, cfg.block_index)
+    st.qkv(xb.cuda())
+    torch.cuda.synchronize()
+    M, D = xb.shape
+    got = st.ws_step[:M * D * 2].view(torch.bfloat16).view(M, D).double().cpu().numpy()
+    want = orc.bf16_round(orc.rmsnorm(xb.double().numpy(), st.gain.double().cpu().numpy(), cfg.rms_eps))
+    assert np.array_equal(got, want), f"{int((got != want).sum())} elements differ"
+
+
+def test_llada_single_blocks():
+    cfg = make_config("llada_single")
+    for k in (0, 3, cfg.num_blocks(0) - 1):
+        _run_block(cfg, [k], (0, cfg.steps_per_block - 1), check_cache=(k == 3))
+
+
+def _mini_ragged(**kw):
+    # edge cases: empty prefix, last block (empty suffix), page-unaligned
+    # blocks, blocks straddling pages, partial last pages, odd block sizes,
+    # a sequence made of its block only (no invariant rows).
+    return Config("mini_ragged", 256, 4, 64, 1e4,
+                  t_prefix=[0, 100, 37, 10, 300, 5, 0, 64],
+                  gen_len=[64, 96, 128, 64, 240, 20, 32, 128],
+                  block=[32, 32, 16, 64, 48, 20, 32, 64],
+                  block_index=[0, 2, 3, 0, 1, 0, 0, 1],
+                  steps_per_block=2).with_(**kw)
+
+
+def test_mini_ragged_edge_cases():
+    cfg = _mini_ragged()
+    _run_block(cfg, cfg.block_index, (0, 1))
+
+
+def test_mini_ragged_head_dim_128():
+    cfg = _mini_ragged(d_model=512, n_heads=2, head_dim=128, rope_theta=5e5)
+    _run_block(cfg, cfg.block_index, (1,))
+
+
+def test_placement_is_bit_exact_and_sentinels_survive():
+    """A shuffled physical page order (with a consistent block table) gives
+    byte-identical outputs and gathered cache contents; pages no sequence
+    owns keep their sentinel."""
+    outs = []
+    for shuffle in (False, True):
+        cfg = _mini_ragged(shuffle_pages=shuffle, spare_pages=5)
+        wl = Workload(cfg)
+        st = LayerStep(cfg, cache_fill=3.0)
+        k_of = cfg.block_index
+        st.boundary(full_rows_of(wl, 0, 0, k_of).cuda())
+        st.step(block_rows_of(wl, 0, 1, k_of).cuda())
+        torch.cuda.synchronize()
+        assert st.batch.error_bits() == 0
+        gathered = {}
+        for b in range(cfg.batch):
+            n = cfg.seq_len(b)
+            s0, e0 = cfg.block_start(b), cfg.block_start(b) + cfg.block[b]
+            U = np.r_[0:s0, e0:n]
+            for name in ("k", "v"):
+                gathered[(name, b)] = st.pool_rows(getattr(st.cache, name), b).cpu()
+            for name in ("q", "m", "l", "o"):
+                gathered[(name, b)] = st.pool_rows(getattr(st.cache, name), b).cpu()[U]
+        used = set(int(p) for p in st.host_layout["block_table"].ravel() if p >= 0)
+        spare = [p for p in range(st.cache.num_pages) if p not in used]
+        assert len(spare) == 5
+        for name in ("k", "v", "q", "m", "l", "o"):
+            pool = getattr(st.cache, name)[spare]
+            assert torch.all(pool == 3.0), f"spare pages of {name}_pool were written"
+        outs.append((st.o_full.cpu(), st.lse.cpu(), st.q_block.cpu(), gathered))
+    (o0, l0, q0, g0), (o1, l1, q1, g1) = outs
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(l0.view(torch.int32), l1.view(torch.int32))
+    assert torch.equal(q0.view(torch.int16), q1.view(torch.int16))
+    for key in g0:
+        a, b = g0[key], g1[key]
+        iv = torch.int16 if a.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(a.contiguous().view(iv), b.contiguous().view(iv)), key
+
+
+def test_bad_block_table_entry_is_reported_not_faulted():
+    cfg = _mini_ragged()
+    wl = Workload(cfg)
+    st = LayerStep(cfg)
+    k_of = cfg.block_index
+    st.boundary(full_rows_of(wl, 0, 0, k_of).cuda())
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() == 0
+    # corrupt one entry on the device: every kernel must skip or clamp it
+    st.batch.dev["block_table"][1, 0] = st.cache.num_pages + 7
+    st.step(block_rows_of(wl, 0, 0, k_of).cuda())
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() & dllm.DLLM_DEVERR_BAD_PAGE
+    # inconsistent metadata: a block that runs past the end of its sequence
+    st.batch.error.zero_()
+    st.batch.dev["block_table"][1, 0] = int(st.host_layout["block_table"][1, 0])
+    st.batch.dev["block_start"][2] = cfg.seq_len(2)
+    st.step(block_rows_of(wl, 0, 0, k_of).cuda())
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() & dllm.DLLM_DEVERR_BAD_SHAPE
+    torch.cuda.synchronize()
+
+
+def test_host_validation_rejects_before_launch():
+    cfg = _mini_ragged()
+    st = LayerStep(cfg)
+    bad = dllm.layer_desc(cfg.d_model, cfg.n_heads, 96, cfg.rope_theta)
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_block_attention(bad, st.batch.c, st.q_block, st.cache.c, st.o_full)
+    assert e.value.status == dllm.DLLM_ERR_UNSUPPORTED
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_block_qkv_rope_write(st.desc, st.batch.c, st.q_block, st.gain, st.w_qkv, st.rope, st.rope_max_pos,
+                                       st.cache.c, st.q_block, st.ws_step[:16])
+    assert e.value.status == dllm.DLLM_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_block_attention(st.desc, st.batch.c, st.q_block.data_ptr() + 2, st.cache.c, st.o_full)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT

@@ -82,10 +82,12 @@ def test_rmsnorm_constant_and_scale_invariance():
 
 # ---------------------------------------------------------------- linear ----
 def test_linear_matches_numpy():
+    # the plain C loop and numpy's matmul (used by the step at full size) agree
     g = _rng(4)
     x = g.standard_normal((9, 48))
     W = g.standard_normal((30, 48))
     np.testing.assert_allclose(orc.linear(x, W), x @ W.T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(orc.project(x, W), orc.linear(x, W), rtol=1e-13, atol=1e-13)
 
 
 # ------------------------------------------------------------------ RoPE ----
