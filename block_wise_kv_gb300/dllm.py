@@ -42,7 +42,7 @@ PAGE = 64
 
 # Every symbol include/dllm.h declares.
 EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_cache_build", "dllm_block_qkv_rope_write",
-           "dllm_block_attention", "dllm_state_merge", "dllm_status_string")
+           "dllm_block_qkv_rope_write_noalloc", "dllm_block_attention", "dllm_state_merge", "dllm_status_string")
 
 
 class DllmError(RuntimeError):
@@ -94,6 +94,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                 "dllm_cache_build": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, sz, vp],
                 "dllm_block_qkv_rope_write": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, vp, sz,
                                               vp],
+                "dllm_block_qkv_rope_write_noalloc": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp,
+                                                      vp],
                 "dllm_block_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
                 "dllm_state_merge": [P(LayerDescC), P(BatchC), P(CacheC), vp, vp, vp, sz, vp],
             }
@@ -160,6 +162,15 @@ def dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_qkv, rope_table,
     _check("dllm_block_qkv_rope_write", load().dllm_block_qkv_rope_write(
         ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
         int(rope_max_pos), ctypes.byref(cache), _ptr(q_block), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def dllm_block_qkv_rope_write_noalloc(desc, batch, x_block, rms_gain, w_qkv, rope_table, rope_max_pos, cache,
+                                      q_block, stream=None):
+    """dllm_block_qkv_rope_write without a workspace: for callers that cannot
+    allocate device memory (the library's fixed 4 MiB scratch is used)."""
+    _check("dllm_block_qkv_rope_write_noalloc", load().dllm_block_qkv_rope_write_noalloc(
+        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
+        int(rope_max_pos), ctypes.byref(cache), _ptr(q_block), _stream(stream)))
 
 
 def dllm_block_attention(desc, batch, q_block, cache, o_full, lse=None, ws=None, stream=None):

@@ -174,6 +174,26 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
                                       int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
                                       size_t ws_bytes, void* stream);
 
+/* The same call as dllm_block_qkv_rope_write for callers that cannot
+ * allocate device memory (no counterpart in the pages; an addition of this
+ * library).  Some callers cannot hand the library a workspace: a plugin host
+ * that passes only inputs and outputs, a server with a fixed memory budget
+ * reserved at start-up that forbids allocation on the serving path, or code
+ * running where cudaMalloc is not allowed.  This variant allocates nothing and
+ * takes no workspace: its scratch is a fixed 4 MiB array in the library's own
+ * device memory (held by every GPU that loads the library until exit), so
+ * total_block_rows * d_model * 2 bytes must not exceed 4 MiB; a larger batch
+ * returns DLLM_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call
+ * on each device looks up the array's device address with that device
+ * current (make that first call before any stream capture).  All calls share
+ * the array: calls whose GPU work may overlap (different streams without
+ * ordering) race on it.  Arguments, layouts and results are otherwise those
+ * of dllm_block_qkv_rope_write. */
+dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* desc, const dllm_batch* batch,
+                                              const void* x_block, const void* rms_gain, const void* w_qkv,
+                                              const float* rope_table, int32_t rope_max_pos,
+                                              const dllm_cache* cache, void* q_block, void* stream);
+
 /* Inner step, part 2 (LaCache Eq. (2)-(6); Fast-dLLM DualCache "Inner step on
  * block k"): for each block row i of sequence b and head h,
  *   O = sum_j softmax_j(scale * q_i . k_j) v_j over ALL keys j in [0, N_b)
