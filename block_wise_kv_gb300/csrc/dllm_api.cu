@@ -15,8 +15,6 @@ constexpr int64_t kMaxRows = (int64_t{1} << 31) - 1;
 
 bool aligned(const void* p, uintptr_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 dllm_status check_desc(const dllm_layer_desc* d) {
   if (d == nullptr) return DLLM_ERR_INVALID_ARGUMENT;
   if (d->head_dim != 64 && d->head_dim != 128) return DLLM_ERR_UNSUPPORTED;
@@ -125,7 +123,20 @@ QkvArgs qkv_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache
   a.d_model = d->d_model;
   a.n_tok = n_tok;
   a.mode = mode;
+  a.partials = nullptr;
+  a.counters = nullptr;
+  a.max_contrib = 0;
   return a;
+}
+
+// Point the projection at its workspace: x^ first, then (stream-K) the fp32
+// partial tiles and the arrival counters the RMSNorm kernel zeroes.
+void bind_workspace(QkvArgs* a, const QkvPlan& plan, void* ws) {
+  if (!plan.streamk) return;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a->partials = reinterpret_cast<float*>(base + plan.part_offset);
+  a->counters = reinterpret_cast<int32_t*>(base + plan.counter_offset);
+  a->max_contrib = plan.max_contrib;
 }
 
 dllm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA; }
@@ -150,13 +161,18 @@ dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* b
   DLLM_TRY(check_desc(desc));
   DLLM_TRY(check_batch(batch));
   if (bytes == nullptr) return DLLM_ERR_INVALID_ARGUMENT;
-  const size_t row = static_cast<size_t>(desc->d_model) * 2;
   switch (op) {
     case DLLM_OP_CACHE_BUILD:
-      *bytes = batch->batch > 0 ? align256(static_cast<size_t>(batch->total_seq_rows) * row) : 0;
+      *bytes = batch->batch > 0 && batch->total_seq_rows > 0
+                   ? qkv_plan(batch->total_seq_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms())
+                         .total_bytes
+                   : 0;
       return DLLM_OK;
     case DLLM_OP_BLOCK_QKV_ROPE_WRITE:
-      *bytes = batch->batch > 0 ? align256(static_cast<size_t>(batch->total_block_rows) * row) : 0;
+      *bytes = batch->batch > 0 && batch->total_block_rows > 0
+                   ? qkv_plan(batch->total_block_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms())
+                         .total_bytes
+                   : 0;
       return DLLM_OK;
     case DLLM_OP_BLOCK_ATTENTION:
     case DLLM_OP_STATE_MERGE:
@@ -191,10 +207,13 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   const BatchArgs bt = batch_args(batch, cache);
+  const QkvPlan plan = qkv_plan(batch->total_seq_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms());
+  QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBoundary, batch->total_seq_rows);
+  bind_workspace(&qa, plan, ws);
   DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
-  DLLM_CUDA_TRY(launch_rmsnorm(x_full, rms_gain, ws, batch->total_seq_rows, desc->d_model, desc->rms_eps, s));
-  const QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBoundary, batch->total_seq_rows);
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, device_sms(), s));
+  DLLM_CUDA_TRY(launch_rmsnorm(x_full, rms_gain, ws, batch->total_seq_rows, desc->d_model, desc->rms_eps, qa.counters,
+                               plan.n_counters, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, plan, s));
   const AttnArgs aa = attn_args(desc, batch, cache);
   DLLM_CUDA_TRY(launch_state_build(aa, s));
   return DLLM_OK;
@@ -218,10 +237,13 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
   if (!aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  DLLM_CUDA_TRY(launch_rmsnorm(x_block, rms_gain, ws, batch->total_block_rows, desc->d_model, desc->rms_eps, s));
+  const QkvPlan plan = qkv_plan(batch->total_block_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms());
   QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBlock, batch->total_block_rows);
   qa.q_block = q_block;
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, device_sms(), s));
+  bind_workspace(&qa, plan, ws);
+  DLLM_CUDA_TRY(launch_rmsnorm(x_block, rms_gain, ws, batch->total_block_rows, desc->d_model, desc->rms_eps,
+                               qa.counters, plan.n_counters, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, plan, s));
   return DLLM_OK;
 }
 

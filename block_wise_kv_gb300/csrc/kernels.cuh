@@ -43,7 +43,23 @@ struct QkvArgs {
   int32_t d_model;
   int32_t n_tok;               // rows of the x^ operand
   int32_t mode;                // kModeBlock or kModeBoundary
+  // stream-K schedule (n_tok <= 64): fp32 partial tiles and per-tile arrival
+  // counters in the workspace; the counters are zeroed by the RMSNorm kernel
+  float* partials;             // null: one CTA per (weight tile, token tile)
+  int32_t* counters;
+  int32_t max_contrib;         // partial slots per weight tile
 };
+
+// Workspace layout and schedule of the fused projection for n_tok rows.
+struct QkvPlan {
+  int bn;            // token tile (32, 64 or 128)
+  bool streamk;      // stream-K over (weight tile, k-block) units, else one CTA per tile
+  int grid;          // CTAs of the stream-K schedule
+  int max_contrib;   // stream-K: most CTAs sharing one weight tile
+  int n_counters;    // arrival counters (one per weight tile) to zero before the projection
+  size_t xhat_bytes, part_offset, part_bytes, counter_offset, counter_bytes, total_bytes;
+};
+QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms);
 constexpr int kModeBlock = 0;     // tokens are the packed block rows (cu_block)
 constexpr int kModeBoundary = 1;  // tokens are all rows of every sequence (cu_seq)
 
@@ -66,11 +82,11 @@ struct AttnArgs {
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
 // Each launcher encodes the TMA tensor maps it needs from the raw pointers.
 cudaError_t launch_rmsnorm(const void* x, const void* gain, void* out, int rows, int d_model, float eps,
-                           cudaStream_t stream);
+                           int32_t* zero, int zero_count, cudaStream_t stream);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double theta, cudaStream_t stream);
 cudaError_t launch_zero_tails(const BatchArgs& bt, void* k_pool, void* v_pool, void* q_pool, int n_heads,
                               int head_dim, cudaStream_t stream);
-cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, int num_sms,
+cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
                             cudaStream_t stream);
 cudaError_t launch_block_attention(const AttnArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_state_build(const AttnArgs& a, cudaStream_t stream);

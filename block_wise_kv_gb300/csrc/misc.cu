@@ -39,8 +39,15 @@ __device__ __forceinline__ uint16_t bf16_round_pair(float p, float e) {
 // the correctly rounded value of the real x^.  D % 8 == 0.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const __nv_bfloat16* __restrict__ gain,
-                                                               __nv_bfloat16* __restrict__ out, int D, float eps) {
+                                                               __nv_bfloat16* __restrict__ out, int D, float eps,
+                                                               int32_t* __restrict__ zero, int zero_count) {
   __shared__ float red_hi[kNormThreads / 32], red_lo[kNormThreads / 32];
+  // Programmatic dependent launch: x may come from the preceding kernel; once
+  // it is visible, let the projection kernel start streaming its weights.
+  griddep_wait();
+  griddep_launch_dependents();
+  if (blockIdx.x == 0)  // the projection's stream-K arrival counters start at zero
+    for (int i = threadIdx.x; i < zero_count; i += kNormThreads) zero[i] = 0;
   const size_t row = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * D);
   const uint4* gr = reinterpret_cast<const uint4*>(gain);
@@ -72,12 +79,17 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
     red_lo[threadIdx.x >> 5] = lo;
   }
   __syncthreads();
-  double ss = 0.0;
+  if (threadIdx.x == 0) {  // fp64 is slow on this part: one thread forms the scale
+    double ss = 0.0;
 #pragma unroll
-  for (int w = 0; w < kNormThreads / 32; ++w) ss += static_cast<double>(red_hi[w]) + static_cast<double>(red_lo[w]);
-  const double inv = 1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps));
-  const float inv_hi = static_cast<float>(inv);
-  const float inv_lo = static_cast<float>(inv - static_cast<double>(inv_hi));
+    for (int w = 0; w < kNormThreads / 32; ++w) ss += static_cast<double>(red_hi[w]) + static_cast<double>(red_lo[w]);
+    const double inv = 1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps));
+    const float ih = static_cast<float>(inv);
+    red_hi[0] = ih;
+    red_lo[0] = static_cast<float>(inv - static_cast<double>(ih));
+  }
+  __syncthreads();
+  const float inv_hi = red_hi[0], inv_lo = red_lo[0];
   for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
     const uint4 u = __ldg(xr + v);
     const uint4 gu = __ldg(gr + v);
@@ -148,12 +160,25 @@ __global__ void zero_tails_kernel(BatchArgs bt, __nv_bfloat16* k_pool, __nv_bflo
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void* x, const void* gain, void* out, int rows, int d_model, float eps,
-                           cudaStream_t stream) {
+                           int32_t* zero, int zero_count, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<rows, kNormThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
-                                                      static_cast<const __nv_bfloat16*>(gain),
-                                                      static_cast<__nv_bfloat16*>(out), d_model, eps);
-  return cudaGetLastError();
+  // Same shared-memory carveout as the projection kernel that follows: an SM
+  // cannot change its L1/shared split while a CTA of this kernel runs on it.
+  cudaError_t e = cudaFuncSetAttribute(rmsnorm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, static_cast<const __nv_bfloat16*>(x),
+                            static_cast<const __nv_bfloat16*>(gain), static_cast<__nv_bfloat16*>(out), d_model, eps,
+                            zero, zero_count);
 }
 
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double theta, cudaStream_t stream) {

@@ -16,17 +16,19 @@
 // current) and cached; that lookup happens on the first call on each device,
 // so the first call on a device should come before any stream capture.
 //
-// All calls share the array and it keeps the last call's contents.  The call
-// overwrites every scratch byte it reads (the normalised rows), so nothing
-// needs clearing, but two calls whose GPU work overlaps (different streams,
-// no ordering between them) race on the array.
+// All calls share the array and it keeps the last call's contents.  A call
+// writes every scratch byte before it reads it (the normalised rows, the
+// partial tiles), and the arrival counters that must start at zero are
+// zeroed by the call's own first kernel, so nothing needs clearing between
+// calls; but two calls whose GPU work overlaps (different streams, no
+// ordering between them) race on the array.
 #include <mutex>
 
 #include "dllm.h"
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t{4} << 20;  // 4 MiB: M * d_model <= 2M elements of bf16
+constexpr size_t kNoAllocScratchBytes = size_t{8} << 20;  // 8 MiB: the x^ rows plus the stream-K partial tiles
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -11,55 +11,78 @@
 // values written straight into the cache in one HBM write) applied to the
 // token-wise operators of LaCache §3.3.2, Eq. (1).
 //
-// GB300 design.  The contraction is "swap-AB": the 128-row weight tiles are
-// the tcgen05 M operand and the (few) token rows are the N operand, so a
-// 32-token inner step still fills a 128 x 32 UMMA.  A warp issues TMA loads of
-// 128 x 64 weight tiles and BN x 64 token tiles (128-byte swizzle) into a
-// multi-stage mbarrier ring; one thread issues tcgen05.mma into a TMEM
-// accumulator.  When the weight-tile x token-tile grid alone cannot fill the
-// 152 SMs (the inner step is bound by streaming the 100 MB weight matrix),
-// the K dimension is split across the CTAs of a thread-block cluster and the
-// fp32 partial tiles are summed through distributed shared memory before the
-// RoPE epilogue, so nothing but the final bf16 q/k/v leaves the chip.
-#include <cooperative_groups.h>
-
+// GB300 design.
+//  * Swap-AB: the 128-row weight tiles are the tcgen05 M operand and the
+//    (few) token rows are the N operand, so a 32-token inner step still fills
+//    a 128 x 32 UMMA.
+//  * A CTA that allocates TMEM runs alone on its SM, so the kernel is built
+//    around one CTA per SM with a deep (~200 KB) TMA ring: warp 0 streams
+//    128 x 64 weight tiles and BN x 64 token tiles (128-byte swizzle), warp 1
+//    owns TMEM and issues tcgen05.mma, warps 2-5 accumulate and write.
+//  * Inner steps (<= 64 token rows) are bound by streaming the weight matrix,
+//    so they are scheduled stream-K: the (weight tile, k-block) units are
+//    split evenly over one CTA per SM; a weight tile that spans several CTAs
+//    is finished by whichever contributor arrives last (fp32 partials in the
+//    workspace, an atomic arrival counter; no CTA waits on another).  Larger
+//    row counts use one CTA per (weight tile, 128-row token tile).
+//  * fp32 accumulation on the CUDA cores ("promotion"): the tensor core sums
+//    only 128-element partial products (a chain of 8 MMAs) into one of the
+//    TMEM buffers; the accumulator warps drain each finished buffer into fp32
+//    registers.  The tensor core's own long accumulation chains round
+//    noticeably worse than fp32 round-to-nearest, and every bf16 value this
+//    kernel stores is a cache entry that later steps reuse.  All 512 TMEM
+//    columns serve as partial buffers, so the tensor core can run far ahead
+//    while the accumulator warps finish a tile.
+//  * Programmatic dependent launch: the weight tiles (constants) of the first
+//    ring stages are requested before waiting for the preceding kernel (the
+//    RMSNorm that produces x^), so the weight stream overlaps it.
 #include "kernels.cuh"
 #include "sm103.cuh"
 #include "tmap.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace dllm {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kTileM = 128;     // weight rows per tile (UMMA M)
-constexpr int kTileK = 64;      // K elements per stage (one 128-byte swizzle row)
+constexpr int kThreads = 192;
+constexpr int kAccThreads = kThreads - 64;  // warps 2-5
+constexpr int kTileM = 128;                 // weight rows per tile (UMMA M)
+constexpr int kTileK = 64;                  // K elements per unit (one 128-byte swizzle row)
 constexpr int kTileABytes = kTileM * kTileK * 2;
+constexpr int kPromote = 2;                 // units per TMEM partial (K = 128: a chain of 8 MMAs)
+constexpr int kMinUnitsPerCta = 8;
 
 template <int BN>
 struct GemmCfg;
 template <>
 struct GemmCfg<32> {
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 9;
+  static constexpr bool kOwnRecv = true;  // stream-K: tile epilogues run while the ring is busy
 };
 template <>
 struct GemmCfg<64> {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 7;
+  static constexpr bool kOwnRecv = true;
 };
 template <>
 struct GemmCfg<128> {
-  static constexpr int kStages = 4;
-};
-template <>
-struct GemmCfg<256> {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 6;
+  static constexpr bool kOwnRecv = false;  // one tile per CTA: the drained ring holds the tile
 };
 
 template <int BN>
-constexpr int gemm_smem_bytes() {
-  return GemmCfg<BN>::kStages * (kTileABytes + BN * kTileK * 2) + 1024;
+constexpr int tmem_bufs() {
+  return 512 / BN;
 }
+template <int BN>
+constexpr int ring_bytes() {
+  return GemmCfg<BN>::kStages * (kTileABytes + BN * kTileK * 2);
+}
+template <int BN>
+constexpr int gemm_smem_bytes() {
+  return ring_bytes<BN>() + (GemmCfg<BN>::kOwnRecv ? BN * kTileM * 4 : 0) + 1024;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Largest b in [0, batch) with cu[b] <= j.
 __device__ __forceinline__ int find_seq(const int32_t* cu, int batch, int j) {
@@ -74,6 +97,47 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int batch, int j) {
   return lo;
 }
 
+// Stream-K split of U units over G CTAs: CTA c owns [c*U/G, (c+1)*U/G).
+__host__ __device__ __forceinline__ long long sk_begin(long long c, long long U, long long G) { return c * U / G; }
+__host__ __device__ __forceinline__ int sk_cta_of(long long u, long long U, long long G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+// Walk of a CTA's units: weight tile, k-block, and where segments (runs of one
+// tile) and promotion periods begin and end.  The producer, the MMA issuer and
+// the accumulator warps all follow the same walk, advanced incrementally (no
+// integer division inside the loops).
+struct UnitWalk {
+  int tile, kb, ps;  // weight tile, k-block, position inside the segment
+  int nkb, left;     // k-blocks per tile, units left after this one
+  bool seg_end, period_first, period_last;
+  __device__ __forceinline__ void init(long long u0, long long u1, int nkb_) {
+    nkb = nkb_;
+    tile = static_cast<int>(u0 / nkb);
+    kb = static_cast<int>(u0 % nkb);
+    ps = 0;
+    left = static_cast<int>(u1 - u0) - 1;
+    flags();
+  }
+  __device__ __forceinline__ void flags() {
+    seg_end = left == 0 || kb == nkb - 1;
+    period_first = (ps % kPromote) == 0;
+    period_last = (ps % kPromote) == kPromote - 1 || seg_end;
+  }
+  __device__ __forceinline__ int seg_kb0() const { return kb - ps; }
+  __device__ __forceinline__ void next() {
+    --left;
+    if (++kb == nkb) {
+      kb = 0;
+      ++tile;
+      ps = 0;
+    } else {
+      ++ps;
+    }
+    flags();
+  }
+};
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -81,24 +145,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = GemmCfg<BN>::kStages;
   constexpr int kTileBBytes = BN * kTileK * 2;
   constexpr int kStageBytes = kTileABytes + kTileBBytes;
-  constexpr uint32_t kTmemCols = BN;  // power of two >= 32
+  constexpr int kTmemBufs = tmem_bufs<BN>();
+  constexpr uint32_t kTmemCols = kTmemBufs * BN;  // 512: the CTA is alone on its SM
+  constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  float* recv = reinterpret_cast<float*>(smem + (GemmCfg<BN>::kOwnRecv ? ring_bytes<BN>() : 0));  // [BN][128]
 
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tmem_full_bar;
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[kTmemBufs], tempty_bar[kTmemBufs];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ long long tok_kv[BN];   // element offset of (page, head 0, slot) in the pools, -1: no write
-  __shared__ long long tok_q[BN];    // element offset of the q destination for head 0, -1: no write
-  __shared__ int tok_pos[BN];        // absolute position (RoPE)
+  __shared__ int last_sh;
+  __shared__ long long tok_kv[BN];  // element offset of (page, head 0, slot) in the pools, -1: no write
+  __shared__ long long tok_q[BN];   // element offset of the q destination for head 0, -1: no write
+  __shared__ int tok_pos[BN];       // absolute position (RoPE)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = gridDim.x, rank = blockIdx.x;
-  const int mt = blockIdx.y, nt = blockIdx.z;
-  const int nkb_total = a.d_model / kTileK;
-  const int kb0 = rank * nkb_total / S, kb1 = (rank + 1) * nkb_total / S;
-  const int nkb = kb1 - kb0;
+  const int nkb = a.d_model / kTileK;
+  const int n_wt = 3 * a.n_heads * a.head_dim / kTileM;
+  const bool streamk = a.partials != nullptr;
+  const int nt = streamk ? 0 : static_cast<int>(blockIdx.z);
+  const long long U = static_cast<long long>(n_wt) * nkb, G = gridDim.x;
+  long long u0, u1;  // unit range of this CTA
+  if (streamk) {
+    u0 = sk_begin(blockIdx.x, U, G);
+    u1 = sk_begin(blockIdx.x + 1, U, G);
+  } else {
+    u0 = static_cast<long long>(blockIdx.y) * nkb;
+    u1 = u0 + nkb;
+  }
+  const int n_units = static_cast<int>(u1 - u0);
   const BatchArgs& bt = a.bt;
 
   if (threadIdx.x == 0) {
@@ -106,12 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&tmem_full_bar, 1);
+    for (int b = 0; b < kTmemBufs; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], kAccThreads / 32);
+    }
     fence_barrier_init();
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
   }
-  if (warp == 2) tmem_alloc(&tmem_base_sh, kTmemCols);
+  if (warp == 1) tmem_alloc(&tmem_base_sh, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -119,50 +199,95 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---- TMA producer
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (i >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1)) {
+      // ---- TMA producer.  Weight tiles of the first stages go out before the
+      // dependency wait (weights are constants); x^ tiles only after it.
+      const int npre = n_units < kStages ? n_units : kStages;
+      UnitWalk w;
+      w.init(u0, u1, nkb);
+      for (int i = 0; i < npre; ++i, w.next()) {
+        mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
+        tma_load_2d(smem + i * kStageBytes, &tm_w, &full_bar[i], w.kb * kTileK, w.tile * kTileM);
+      }
+      griddep_wait();
+      {
+        UnitWalk wb;
+        wb.init(u0, u1, nkb);
+        for (int i = 0; i < npre; ++i, wb.next())
+          tma_load_2d(smem + i * kStageBytes + kTileABytes, &tm_x, &full_bar[i], wb.kb * kTileK, nt * BN);
+      }
+      int issued = npre;
+      int s = npre % kStages;
+      uint32_t ph = (npre / kStages) & 1;
+      for (int i = npre; i < n_units; ++i, w.next()) {
+        if (!mbar_wait(&empty_bar[s], ph ^ 1)) {
           report_error(bt.err, kErrTimeout);
           break;
         }
         uint8_t* sa = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-        tma_load_2d(sa, &tm_w, &full_bar[s], (kb0 + i) * kTileK, mt * kTileM);
-        tma_load_2d(sa + kTileABytes, &tm_x, &full_bar[s], (kb0 + i) * kTileK, nt * BN);
+        tma_load_2d(sa, &tm_w, &full_bar[s], w.kb * kTileK, w.tile * kTileM);
+        tma_load_2d(sa + kTileABytes, &tm_x, &full_bar[s], w.kb * kTileK, nt * BN);
         ++issued;
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       // Drain: every issued load has landed before the CTA can retire.
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
         if (!mbar_wait(&full_bar[i % kStages], (i / kStages) & 1)) report_error(bt.err, kErrTimeout);
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer
-      constexpr uint32_t idesc = umma_idesc_bf16(kTileM, BN);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
+      // ---- MMA issuer: period p = round * kTmemBufs + buf goes to TMEM buffer buf.
+      bool ok = true;
+      int buf = kTmemBufs - 1, round = -1;
+      int s = 0;
+      uint32_t ph = 0;
+      UnitWalk w;
+      w.init(u0, u1, nkb);
+      for (int i = 0; i < n_units && ok; ++i, w.next()) {
+        if (w.period_first) {
+          if (++buf == kTmemBufs) {
+            buf = 0;
+            ++round;
+          }
+          if (round >= 1 && !mbar_wait(&tempty_bar[buf], (round + 1) & 1)) {
+            report_error(bt.err, kErrTimeout);
+            ok = false;
+            break;
+          }
+        }
         if (!mbar_wait(&full_bar[s], ph)) {
           report_error(bt.err, kErrTimeout);
+          ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kTileABytes;
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
 #pragma unroll
         for (int k = 0; k < kTileK / 16; ++k)
-          umma_bf16(tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc, (i | k) != 0);
+          umma_bf16(d, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), kIdesc,
+                    (w.period_first && k == 0) ? 0u : 1u);
         umma_commit(&empty_bar[s]);
+        if (w.period_last) umma_commit(&tfull_bar[buf]);
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      umma_commit(&tmem_full_bar);
+      if (!ok)  // let the accumulator warps finish (their waits see the phases they expect)
+        for (int b = 0; b < kTmemBufs; ++b) umma_commit(&tfull_bar[b]);
     }
+    __syncwarp();
   } else {
-    // ---- warps 2-3: resolve each token column to its destinations while the
-    // main loop runs.
-    const int H = a.n_heads, d = a.head_dim;
-    for (int c = threadIdx.x - 64; c < BN; c += 64) {
+    // ---- accumulator warps (TMEM lane quarter = warp % 4)
+    griddep_wait();
+    const int H = a.n_heads, d = a.head_dim, half = d >> 1;
+    const int HD = H * d;
+    for (int c = threadIdx.x - 64; c < BN; c += kAccThreads) {  // resolve token columns
       long long kv = -1, qd = -1;
       int pos = 0;
       const int j = nt * BN + c;
@@ -194,84 +319,163 @@ __global__ void __launch_bounds__(kThreads, 1)
       tok_q[c] = qd;
       tok_pos[c] = pos;
     }
-  }
-  __syncwarp();
+    named_barrier(1, kAccThreads);
 
-  // ---- accumulator: TMEM -> shared (token-major partial tile [BN][128])
-  if (!mbar_wait(&tmem_full_bar, 0)) report_error(bt.err, kErrTimeout);
-  tc_fence_after();
-  float* part = reinterpret_cast<float*>(smem);  // reuses the drained pipeline buffers
-  {
-    const int row = warp * 32 + lane;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) part[(c0 + jj) * kTileM + row] = v[jj];
-    }
-  }
-  tc_fence_before();
-  cg::cluster_group cluster = cg::this_cluster();
-  if (S > 1)
-    cluster.sync();
-  else
-    __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
-
-  // ---- epilogue: sum the split-K partials of this rank's token columns,
-  // rotate q/k, round to bf16 and write each value once.
-  {
-    const int H = a.n_heads, d = a.head_dim, half = d >> 1;
-    const int HD = H * d;
-    const int grow0 = mt * kTileM;
-    const int which = grow0 / HD;                // 0: q, 1: k, 2: v
-    const int head0 = (grow0 % HD) / d;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const int ncols = min(BN, a.n_tok - nt * BN);
-    const int nmine = ncols > rank ? (ncols - rank + S - 1) / S : 0;
     __nv_bfloat16* kpool = static_cast<__nv_bfloat16*>(a.k_pool);
     __nv_bfloat16* vpool = static_cast<__nv_bfloat16*>(a.v_pool);
     __nv_bfloat16* qdst = static_cast<__nv_bfloat16*>(a.mode == kModeBlock ? a.q_block : a.q_pool);
-    for (int item = threadIdx.x; item < nmine * 64; item += kThreads) {
-      const int c = rank + S * (item >> 6);
-      const int jp = item & 63;
-      const long long kv = tok_kv[c];
-      if (kv < 0) continue;
-      const int hit = jp / half, t = jp % half;
-      const int row_lo = hit * d + t, row_hi = row_lo + half;
-      float lo = 0.f, hi = 0.f;
-      for (int r = 0; r < S; ++r) {
-        const float* p = S > 1 ? cluster.map_shared_rank(part, r) : part;
-        lo += p[c * kTileM + row_lo];
-        hi += p[c * kTileM + row_hi];
+    const int chunks_per_half = half / 8;  // 8 (d = 128) or 4 (d = 64)
+    float acc[BN];
+#pragma unroll
+    for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+    int buf = kTmemBufs - 1, round = -1;
+    bool ok = true;  // after a timed-out wait the walk continues (same named barriers) without waiting
+    UnitWalk w;
+    w.init(u0, u1, nkb);
+    for (int i = 0; i < n_units; ++i, w.next()) {
+      if (w.period_first && ++buf == kTmemBufs) {
+        buf = 0;
+        ++round;
       }
-      const int head = head0 + hit;
-      __nv_bfloat16* out;
-      if (which == 2) {
-        out = vpool + kv + static_cast<long long>(head) * kPage * d;
-      } else {
-        const float2 cs = *reinterpret_cast<const float2*>(a.rope + (static_cast<size_t>(tok_pos[c]) * half + t) * 2);
-        const float rlo = lo * cs.x - hi * cs.y;
-        const float rhi = hi * cs.x + lo * cs.y;
-        lo = rlo;
-        hi = rhi;
-        if (which == 1) {
-          out = kpool + kv + static_cast<long long>(head) * kPage * d;
-        } else {
-          const long long qd = tok_q[c];
-          if (qd < 0) continue;
-          out = qdst + qd + static_cast<long long>(head) * (a.mode == kModeBlock ? d : kPage * d);
+      if (!w.period_last) continue;
+      if (ok && !mbar_wait(&tfull_bar[buf], round & 1)) {
+        report_error(bt.err, kErrTimeout);
+        ok = false;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) tmem_ld_add_32(lane_base + static_cast<uint32_t>(buf * BN + c0), acc + c0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+      if (!w.seg_end) continue;
+
+      // ---- a segment (one weight tile's k-range of this CTA) is complete
+      const int tile = w.tile;
+      if (!(w.seg_kb0() == 0 && w.kb == nkb - 1)) {
+        // stream-K fixup: publish the partial, count arrivals; the last one finishes the tile
+        const int c_first = sk_cta_of(static_cast<long long>(tile) * nkb, U, G);
+        const int c_last = sk_cta_of(static_cast<long long>(tile) * nkb + nkb - 1, U, G);
+        const int slot = static_cast<int>(blockIdx.x) - c_first;
+        float* slots = a.partials + static_cast<size_t>(tile) * a.max_contrib * kTileM * BN;
+        float* mine = slots + static_cast<size_t>(slot) * kTileM * BN + static_cast<size_t>(row) * BN;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4)
+          *reinterpret_cast<float4*>(mine + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+        named_barrier(1, kAccThreads);  // the CTA's partial rows are written ...
+        if (threadIdx.x == 64) {
+          __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
+          last_sh = atomicAdd(a.counters + tile, 1) == (c_last - c_first);
         }
+        named_barrier(1, kAccThreads);
+        if (!last_sh) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+          continue;
+        }
+        __threadfence();
+        for (int sl = 0; sl <= c_last - c_first; ++sl) {
+          if (sl == slot) continue;
+          const float* other = slots + static_cast<size_t>(sl) * kTileM * BN + static_cast<size_t>(row) * BN;
+#pragma unroll
+          for (int c = 0; c < BN; c += 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(other + c));
+            acc[c] += v.x;
+            acc[c + 1] += v.y;
+            acc[c + 2] += v.z;
+            acc[c + 3] += v.w;
+          }
+        }
+        if (threadIdx.x == 64) a.counters[tile] = 0;  // ready for the next call
       }
-      out[t] = __float2bfloat16_rn(lo);
-      out[t + half] = __float2bfloat16_rn(hi);
+
+      // ---- epilogue of one weight tile: rotate q/k, round to bf16, write 16-byte runs
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        recv[c * kTileM + row] = acc[c];
+        acc[c] = 0.f;
+      }
+      named_barrier(1, kAccThreads);
+      const int grow0 = tile * kTileM;
+      const int which = grow0 / HD;  // 0: q, 1: k, 2: v
+      const int head0 = (grow0 % HD) / d;
+      for (int item = threadIdx.x - 64; item < ncols * 8; item += kAccThreads) {
+        const int c = item >> 3, jc = item & 7;
+        const long long kv = tok_kv[c];
+        if (kv < 0) continue;
+        const int hit = jc / chunks_per_half, t0 = (jc % chunks_per_half) * 8;
+        const int row_lo = hit * d + t0, row_hi = row_lo + half;
+        float lo[8], hi[8];
+        const float* r = recv + c * kTileM;
+#pragma unroll
+        for (int e = 0; e < 8; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(r + row_lo + e);
+          const float4 h4 = *reinterpret_cast<const float4*>(r + row_hi + e);
+          lo[e] = l4.x;
+          lo[e + 1] = l4.y;
+          lo[e + 2] = l4.z;
+          lo[e + 3] = l4.w;
+          hi[e] = h4.x;
+          hi[e + 1] = h4.y;
+          hi[e + 2] = h4.z;
+          hi[e + 3] = h4.w;
+        }
+        const int head = head0 + hit;
+        __nv_bfloat16* out;
+        if (which == 2) {
+          out = vpool + kv + static_cast<long long>(head) * kPage * d;
+        } else {
+          const float4* cs =
+              reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[c]) * half + t0) * 2);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float4 v = __ldg(cs + e / 2);  // (cos, sin) of t0+e and t0+e+1
+            const float l0 = lo[e] * v.x - hi[e] * v.y, h0 = hi[e] * v.x + lo[e] * v.y;
+            const float l1 = lo[e + 1] * v.z - hi[e + 1] * v.w, h1 = hi[e + 1] * v.z + lo[e + 1] * v.w;
+            lo[e] = l0;
+            hi[e] = h0;
+            lo[e + 1] = l1;
+            hi[e + 1] = h1;
+          }
+          if (which == 1) {
+            out = kpool + kv + static_cast<long long>(head) * kPage * d;
+          } else {
+            const long long qd = tok_q[c];
+            if (qd < 0) continue;
+            out = qdst + qd + static_cast<long long>(head) * (a.mode == kModeBlock ? d : kPage * d);
+          }
+        }
+        uint4 wl, wh;
+        wl.x = pack_bf16x2(lo[0], lo[1]);
+        wl.y = pack_bf16x2(lo[2], lo[3]);
+        wl.z = pack_bf16x2(lo[4], lo[5]);
+        wl.w = pack_bf16x2(lo[6], lo[7]);
+        wh.x = pack_bf16x2(hi[0], hi[1]);
+        wh.y = pack_bf16x2(hi[2], hi[3]);
+        wh.z = pack_bf16x2(hi[4], hi[5]);
+        wh.w = pack_bf16x2(hi[6], hi[7]);
+        *reinterpret_cast<uint4*>(out + t0) = wl;
+        *reinterpret_cast<uint4*>(out + t0 + half) = wh;
+      }
+      named_barrier(1, kAccThreads);  // recv is free for the next tile
     }
   }
-  if (S > 1) cluster.sync();  // peers may still read this CTA's partial tile
+
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 template <int BN>
-cudaError_t launch_bn(const void* w_qkv, const void* xhat, const QkvArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_bn(const void* w_qkv, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
+                      cudaStream_t stream) {
   const int HD = a.n_heads * a.head_dim;
   CUtensorMap tm_w, tm_x;
   cudaError_t e = encode_2d_sw128(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_qkv, a.d_model, 3ull * HD, kTileK,
@@ -279,35 +483,21 @@ cudaError_t launch_bn(const void* w_qkv, const void* xhat, const QkvArgs& a, int
   if (e != cudaSuccess) return e;
   e = encode_2d_sw128(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xhat, a.d_model, a.n_tok, kTileK, BN);
   if (e != cudaSuccess) return e;
-
-  const int n_wt = 3 * HD / kTileM;
-  const int n_tt = (a.n_tok + BN - 1) / BN;
-  const int nkb = a.d_model / kTileK;
-  const int smem = gemm_smem_bytes<BN>();
-  const int per_sm = (228 * 1024) / (smem + 2048);
-  const long long tiles = static_cast<long long>(n_wt) * n_tt;
-  const long long slots = static_cast<long long>(num_sms) * (per_sm > 0 ? per_sm : 1);
-  int split = 1;
-  if (tiles < slots) {
-    split = static_cast<int>(slots / tiles);
-    if (split > 8) split = 8;
-    if (split > nkb / 2) split = nkb / 2;
-    if (split < 1) split = 1;
-  }
-
   auto kern = qkv_gemm_kernel<BN>;
+  constexpr int smem = gemm_smem_bytes<BN>();
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(split, n_wt, n_tt);
+  const int n_wt = 3 * HD / kTileM;
+  cfg.gridDim = plan.streamk ? dim3(plan.grid, 1, 1) : dim3(1, n_wt, (a.n_tok + BN - 1) / BN);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, a);
@@ -315,13 +505,41 @@ cudaError_t launch_bn(const void* w_qkv, const void* xhat, const QkvArgs& a, int
 
 }  // namespace
 
-cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, int num_sms,
+QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms) {
+  QkvPlan p = {};
+  const long long n_wt = 3LL * n_heads * head_dim / kTileM;
+  const long long nkb = d_model / kTileK;
+  p.bn = n_tok <= 32 ? 32 : (n_tok <= 64 ? 64 : 128);
+  p.xhat_bytes = align256(static_cast<size_t>(n_tok) * d_model * 2);
+  p.streamk = p.bn <= 64;
+  p.part_offset = p.counter_offset = p.xhat_bytes;
+  if (p.streamk) {
+    const long long U = n_wt * nkb;
+    long long G = U / kMinUnitsPerCta;
+    if (G > num_sms) G = num_sms;
+    if (G < 1) G = 1;
+    p.grid = static_cast<int>(G);
+    int maxc = 1;
+    for (long long t = 0; t < n_wt; ++t) {
+      const int c = sk_cta_of(t * nkb + nkb - 1, U, G) - sk_cta_of(t * nkb, U, G) + 1;
+      if (c > maxc) maxc = c;
+    }
+    p.max_contrib = maxc;
+    p.n_counters = static_cast<int>(n_wt);
+    p.part_bytes = align256(static_cast<size_t>(n_wt) * maxc * kTileM * p.bn * 4);
+    p.counter_offset = p.part_offset + p.part_bytes;
+    p.counter_bytes = align256(static_cast<size_t>(n_wt) * 4);
+  }
+  p.total_bytes = p.counter_offset + p.counter_bytes;
+  return p;
+}
+
+cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
                             cudaStream_t stream) {
   if (a.n_tok <= 0) return cudaSuccess;
-  if (a.n_tok <= 32) return launch_bn<32>(w_qkv, xhat, a, num_sms, stream);
-  if (a.n_tok <= 64) return launch_bn<64>(w_qkv, xhat, a, num_sms, stream);
-  if (a.n_tok <= 128) return launch_bn<128>(w_qkv, xhat, a, num_sms, stream);
-  return launch_bn<256>(w_qkv, xhat, a, num_sms, stream);
+  if (plan.bn == 32) return launch_bn<32>(w_qkv, xhat, a, plan, stream);
+  if (plan.bn == 64) return launch_bn<64>(w_qkv, xhat, a, plan, stream);
+  return launch_bn<128>(w_qkv, xhat, a, plan, stream);
 }
 
 }  // namespace dllm

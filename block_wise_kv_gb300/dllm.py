@@ -167,7 +167,7 @@ def dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_qkv, rope_table,
 def dllm_block_qkv_rope_write_noalloc(desc, batch, x_block, rms_gain, w_qkv, rope_table, rope_max_pos, cache,
                                       q_block, stream=None):
     """dllm_block_qkv_rope_write without a workspace: for callers that cannot
-    allocate device memory (the library's fixed 4 MiB scratch is used)."""
+    allocate device memory (the library's fixed 8 MiB scratch is used)."""
     _check("dllm_block_qkv_rope_write_noalloc", load().dllm_block_qkv_rope_write_noalloc(
         ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
         int(rope_max_pos), ctypes.byref(cache), _ptr(q_block), _stream(stream)))

@@ -180,9 +180,10 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
  * that passes only inputs and outputs, a server with a fixed memory budget
  * reserved at start-up that forbids allocation on the serving path, or code
  * running where cudaMalloc is not allowed.  This variant allocates nothing and
- * takes no workspace: its scratch is a fixed 4 MiB array in the library's own
- * device memory (held by every GPU that loads the library until exit), so
- * total_block_rows * d_model * 2 bytes must not exceed 4 MiB; a larger batch
+ * takes no workspace: its scratch is a fixed 8 MiB array in the library's own
+ * device memory (held by every GPU that loads the library until exit), so the
+ * call's dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) must not exceed
+ * 8 MiB (about 4.8 MiB for 32 block rows of d_model 4096); a larger batch
  * returns DLLM_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call
  * on each device looks up the array's device address with that device
  * current (make that first call before any stream capture).  All calls share

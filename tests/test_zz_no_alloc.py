@@ -51,9 +51,9 @@ def test_noalloc_matches_workspace_call_twice():
 def test_noalloc_rejects_batches_beyond_its_scratch():
     build.build()
     dllm.load()
-    # 640 block rows of d_model 4096 need 5 MiB of scratch: more than the fixed 4 MiB
-    cfg = make_config("tiny").with_(d_model=4096, n_heads=32, head_dim=128, t_prefix=[64] * 10, gen_len=[64] * 10,
-                                    block=[64] * 10, block_index=[0] * 10)
+    # 1280 block rows of d_model 4096 need 10 MiB of scratch: more than the fixed 8 MiB
+    cfg = make_config("tiny").with_(d_model=4096, n_heads=32, head_dim=128, t_prefix=[64] * 20, gen_len=[64] * 20,
+                                    block=[64] * 20, block_index=[0] * 20)
     st = LayerStep(cfg)
     xb = torch.zeros(st.batch.total_block_rows, cfg.d_model, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dllm.DllmError) as e:
