@@ -14,9 +14,10 @@ Workload: the LLaDA-8B-shaped single layer (batch 1, d_model 4096, 32 heads
 x 128, RoPE theta 5e5, prompt 512, gen 256, block 32), synthetic seeded
 bf16 inputs and N(0, 0.02) weights.  Steps rotate over several independent
 layer instances (about 140 MB each), so no step finds its inputs in the
-129 MB L2.  Each step is three CUDA-graph launches (one per C-ABI call) with
-CUDA events between them on the launching stream; the projection call's
-events give its live duration for the roofline.
+129 MB L2.  The steps replay CUDA graphs (the block attention and the merge
+forked onto two streams); a sample of the steps carries CUDA events around
+the projection call on its stream, which give its live duration for the
+roofline.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (sequences are independent units: weak scaling, no collective on the data
@@ -189,49 +190,85 @@ def run_ours(args, rank, ws, local):
         assert st.batch.error_bits() == 0, "device-side error during setup"
     M = inst[0][0].batch.total_block_rows
 
-    # one graph per C-ABI call of each instance
-    stream = torch.cuda.Stream()
-    graphs = []
+    # CUDA graphs.  A round is one step of every instance (L steps, each
+    # forked: attention on the main stream, merge on the side stream), so
+    # consecutive kernels keep their programmatic-dependent-launch overlap.
+    # Every `sample_every`-th round replays per-instance pieces instead, with
+    # CUDA events around the projection call on its stream: those give the
+    # projection's live duration for the roofline, inside the timed region.
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for st, xb in inst:
-            st.step(xb)
+            st.step(xb, stream=stream, side_stream=side)
         stream.synchronize()
+        g_round = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_round, stream=stream):
+            for st, xb in inst:
+                st.step(xb, stream=stream, side_stream=side)
+        g_step, g_qkv, g_rest = [], [], []
         for st, xb in inst:
-            gs = []
-            for fn in (lambda: st.qkv(xb), lambda: st.attention(), lambda: st.merge()):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    fn()
-                gs.append(g)
-            graphs.append(gs)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.step(xb, stream=stream, side_stream=side)
+            g_step.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.qkv(xb, stream=stream)
+            g_qkv.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fork, join = torch.cuda.Event(), torch.cuda.Event()
+                fork.record(stream)
+                side.wait_event(fork)
+                st.attention(stream)
+                st.merge(side)
+                join.record(side)
+                stream.wait_event(join)
+            g_rest.append(g)
     torch.cuda.synchronize()
 
     K, W = args.steps, args.warmup
+    sample_every = max(1, args.sample_every)
     for i in range(W):
-        for g in graphs[i % L]:
-            g.replay()
+        g_step[i % L].replay()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    n_rounds, tail = divmod(K, L)
+    qkv_ev = []
     _barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks, torch.cuda.stream(stream):
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
-        for i in range(K):
-            e = ev[i]
-            gq, ga, gm = graphs[i % L]
-            e[0].record(stream)
-            gq.replay()
-            e[1].record(stream)
-            ga.replay()
-            e[2].record(stream)
-            gm.replay()
-            e[3].record(stream)
+        t_start.record(stream)
+        for r in range(n_rounds):
+            if r % sample_every == sample_every - 1:
+                for j in range(L):
+                    e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    e[0].record(stream)
+                    g_qkv[j].replay()
+                    e[1].record(stream)
+                    g_rest[j].replay()
+                    qkv_ev.append(e)
+            else:
+                g_round.replay()
+        for j in range(tail):
+            g_step[j].replay()
+        t_end.record(stream)
         stream.synchronize()
         t1 = time.perf_counter()
     torch.cuda.synchronize()
     _barrier(ws)
-    total_ms = ev[0][0].elapsed_time(ev[-1][3])
-    part_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / K for j in range(3)]
+    total_ms = t_start.elapsed_time(t_end)
+    if not qkv_ev:  # too few rounds to sample: time the projection alone after the region
+        with torch.cuda.stream(stream):
+            for j in range(L):
+                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e[0].record(stream)
+                g_qkv[j].replay()
+                e[1].record(stream)
+                qkv_ev.append(e)
+        torch.cuda.synchronize()
+    qkv_ms = sum(a.elapsed_time(b) for a, b in qkv_ev) / len(qkv_ev)
     total_ms = _max_over_ranks(total_ms, ws)
     for st, _ in inst:
         assert st.batch.error_bits() == 0, "device-side error during the timed steps"
@@ -244,7 +281,7 @@ def run_ours(args, rank, ws, local):
     for i in range(min(W, 8)):
         st, _ = inst[i % L]
         x_dev[i % L].copy_(x_host[i % L], non_blocking=True)
-        st.step(x_dev[i % L])
+        st.step(x_dev[i % L], side_stream=side)
         o_host[i % L].copy_(st.o_full, non_blocking=True)
     torch.cuda.synchronize()
     _barrier(ws)
@@ -254,7 +291,7 @@ def run_ours(args, rank, ws, local):
         j = i % L
         st, _ = inst[j]
         x_dev[j].copy_(x_host[j], non_blocking=True)
-        st.step(x_dev[j])
+        st.step(x_dev[j], side_stream=side)
         o_host[j].copy_(st.o_full, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -267,7 +304,7 @@ def run_ours(args, rank, ws, local):
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     bf = step_bytes_flops(cfg, inst[0][0])
     qkv_bytes, qkv_flops = bf["qkv"]
-    t_qkv = part_ms[0] * 1e-3
+    t_qkv = qkv_ms * 1e-3
     achieved = qkv_bytes / t_qkv / 1e9
     value = K * M * ws / (total_ms * 1e-3)
     line = {
@@ -286,9 +323,10 @@ def run_ours(args, rank, ws, local):
         "config": {"workload": f"{WORKLOAD}: 1 layer, batch 1, d_model 4096, 32x128 heads, prompt 512, gen 256, "
                                "block 32 (M=32, N=768)",
                    "l2": f"inputs larger than L2: {L} rotating layer instances (~140 MB each)",
+                   "graphs": f"one CUDA graph per round of {L} steps; every {sample_every}th round replayed "
+                             "per call with events around the projection",
                    "parallelism": f"replicas x{ws} (sequences are independent units)"},
-        "parts_us": {"qkv_rope_write": part_ms[0] * 1e3, "block_attention": part_ms[1] * 1e3,
-                     "state_merge": part_ms[2] * 1e3},
+        "qkv_rope_write_us": round(qkv_ms * 1e3, 2),
         "roofline": {"kernel": "dllm_block_qkv_rope_write (RMSNorm + tcgen05 QKV GEMM with RoPE/paged-write "
                                "epilogue)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
@@ -390,6 +428,8 @@ def main(argv=None):
     ap.add_argument("--config", default=WORKLOAD)
     ap.add_argument("--layers", type=int, default=4, help="rotating layer instances (inputs larger than L2)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--sample-every", type=int, default=8,
+                    help="every n-th round of steps carries events around the projection call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -24,14 +24,17 @@
 // Block attention splits the pages of a (sequence, head) across the CTAs of
 // a thread-block cluster; the partial states are combined exactly (the same
 // Eq. (2)-(6) merge) through distributed shared memory, so no partial ever
-// reaches HBM.
-#include <cooperative_groups.h>
-
+// reaches HBM.  Each CTA pushes its combined partial of row i into the
+// shared memory of the CTA that owns row i (i mod cluster size) with remote
+// 16-byte stores, so the exchange costs one store per element and two
+// cluster barriers; the owners then finish their rows from local memory.
+//
+// All three kernels are launched with programmatic dependent launch: barrier
+// setup overlaps the tail of the preceding kernel, and every read of data a
+// preceding kernel may write comes after griddepcontrol.wait.
 #include "kernels.cuh"
 #include "sm103.cuh"
 #include "tmap.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace dllm {
 namespace {
@@ -200,7 +203,14 @@ template <int D>
 struct BlockAttnCfg {
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kSmem = tile_bytes<D>() * (1 + 2 * kStages) + 1024;
-  static constexpr int kOStride = D + 8;  // padded fp32 row of the combine buffer
+  static constexpr int kOStride = D + 8;  // padded fp32 row of the per-warp partials
+  static constexpr int kCombBytes = 64 * kOStride * 4;
+  // Receive slots of the owner CTA: D accumulator floats, then (m, l) and
+  // padding; rows i = rank + S*il, slot il*S + r for peer r (< 72 slots).
+  static constexpr int kRecvStride = D + 4;
+  static constexpr int kRecvSlots = 72;
+  static_assert(kCombBytes + kRecvSlots * kRecvStride * 4 <= tile_bytes<D>() * (1 + 2 * kStages),
+                "combine buffers must fit in the q tile and the drained ring");
 };
 
 template <int D>
@@ -213,9 +223,12 @@ __global__ void __launch_bounds__(160) block_attention_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  constexpr int RS = BlockAttnCfg<D>::kRecvStride;
   uint8_t* q_tile = smem;
   uint8_t* kv = smem + TB;
-  float* comb_o = reinterpret_cast<float*>(kv);  // [64][OS], reused after the page loop
+  // After the page loop the q tile and the ring hold the combine buffers.
+  float* comb_o = reinterpret_cast<float*>(smem);  // [64][OS] per-warp partials of this CTA
+  float* recv = reinterpret_cast<float*>(smem + BlockAttnCfg<D>::kCombBytes);  // [72][RS] pushed partials
   __shared__ uint64_t full_bar[NST], empty_bar[NST];
   __shared__ float comb_m[64], comb_l[64];
 
@@ -223,6 +236,7 @@ __global__ void __launch_bounds__(160) block_attention_kernel(const __grid_const
   const int b = blockIdx.z, h = blockIdx.y, rank = blockIdx.x, S = gridDim.x;
   const BatchArgs& bt = a.bt;
   const int H = a.n_heads;
+  griddep_wait();  // q_block, the pools (and any metadata) may come from the preceding kernel
   SeqMeta sm = load_meta(bt, b);
   if (!sm.ok) {
     if (threadIdx.x == 0 && rank == 0 && h == 0) report_error(bt.err, kErrBadShape);
@@ -311,6 +325,9 @@ __global__ void __launch_bounds__(160) block_attention_kernel(const __grid_const
     }
   }
   __syncthreads();  // every page consumed and every load landed: the ring becomes the combine buffer
+  // Peers may push into this CTA's receive slots once every CTA of the
+  // cluster is past its page loop.
+  cluster_arrive_release();
 
   if (active) {
     st.reduce_l();
@@ -328,40 +345,63 @@ __global__ void __launch_bounds__(160) block_attention_kernel(const __grid_const
       *reinterpret_cast<float2*>(comb_o + slot1 * OS + 8 * n + 2 * t) = make_float2(st.o[n][2], st.o[n][3]);
     }
   }
-  cg::cluster_group cluster = cg::this_cluster();
-  cluster.sync();
+  __syncthreads();
+  cluster_wait_acquire();
 
-  // ---- exact combine of the S x KS partial states of each block row
-  // (Eq. (2)-(6) applied to states), rows i with i % S == rank.
+  // ---- combine the KS key-slice partials of each block row (Eq. (2)-(6)
+  // applied to states) and push the result to the row's owner i % S
+  constexpr int C4 = D / 4;
+  const uint32_t recv_addr = smem_u32(recv);
+  for (int item = threadIdx.x; item < sm.bb * C4; item += 160) {
+    const int i = item / C4, c = (item % C4) * 4;
+    float M = neg_inf();
+    for (int q = 0; q < KS; ++q) M = fmaxf(M, comb_m[q * RG * 16 + i]);
+    const float Mu = M == neg_inf() ? 0.f : M;
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < KS; ++q) {
+      const int slot = q * RG * 16 + i;
+      const float w = fast_exp2(comb_m[slot] - Mu);
+      L += w * comb_l[slot];
+      const float4 ov = *reinterpret_cast<const float4*>(comb_o + slot * OS + c);
+      acc.x += w * ov.x;
+      acc.y += w * ov.y;
+      acc.z += w * ov.z;
+      acc.w += w * ov.w;
+    }
+    const int owner = i % S, rslot = (i / S) * S + rank;
+    const uint32_t dst = mapa_shared(recv_addr + static_cast<uint32_t>((rslot * RS + c) * 4), owner);
+    st_shared_cluster_v4(dst, acc);
+    if (c == 0)
+      st_shared_cluster_v4(mapa_shared(recv_addr + static_cast<uint32_t>((rslot * RS + D) * 4), owner),
+                           make_float4(M, L, 0.f, 0.f));
+  }
+  cluster_arrive_release();  // pushes are visible to their owners after the wait
+  cluster_wait_acquire();
+  griddep_launch_dependents();
+
+  // ---- the owner merges the S pushed partials of its rows i = rank + S*il
   {
     const int nmine = sm.bb > rank ? (sm.bb - rank + S - 1) / S : 0;
-    constexpr int C4 = D / 4;
     __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
     for (int item = threadIdx.x; item < nmine * C4; item += 160) {
-      const int i = rank + S * (item / C4);
-      const int c = (item % C4) * 4;
+      const int il = item / C4, c = (item % C4) * 4;
+      const int i = rank + S * il;
+      const float* base = recv + il * S * RS;
       float M = neg_inf();
-      for (int r = 0; r < S; ++r) {
-        const float* pm = cluster.map_shared_rank(comb_m, r);
-        for (int q = 0; q < KS; ++q) M = fmaxf(M, pm[q * RG * 16 + i]);
-      }
+      for (int r = 0; r < S; ++r) M = fmaxf(M, base[r * RS + D]);
       const float Mu = M == neg_inf() ? 0.f : M;
       float L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int r = 0; r < S; ++r) {
-        const float* pm = cluster.map_shared_rank(comb_m, r);
-        const float* pl = cluster.map_shared_rank(comb_l, r);
-        const float* po = cluster.map_shared_rank(comb_o, r);
-        for (int q = 0; q < KS; ++q) {
-          const int slot = q * RG * 16 + i;
-          const float w = fast_exp2(pm[slot] - Mu);
-          L += w * pl[slot];
-          const float4 ov = *reinterpret_cast<const float4*>(po + slot * OS + c);
-          acc.x += w * ov.x;
-          acc.y += w * ov.y;
-          acc.z += w * ov.z;
-          acc.w += w * ov.w;
-        }
+        const float* pr = base + r * RS;
+        const float w = fast_exp2(pr[D] - Mu);
+        L += w * pr[D + 1];
+        const float4 ov = *reinterpret_cast<const float4*>(pr + c);
+        acc.x += w * ov.x;
+        acc.y += w * ov.y;
+        acc.z += w * ov.z;
+        acc.w += w * ov.w;
       }
       const float inv = 1.f / L;
       const size_t orow = static_cast<size_t>(sm.cus + sm.sb + i) * H + h;
@@ -372,7 +412,6 @@ __global__ void __launch_bounds__(160) block_attention_kernel(const __grid_const
       if (a.lse != nullptr && c == 0) a.lse[orow] = (M + log2f(L)) * kLn2;
     }
   }
-  cluster.sync();  // peers may still read this CTA's partial states
 }
 
 // ============================================================= state build
@@ -400,6 +439,8 @@ __global__ void __launch_bounds__(160) state_build_kernel(const __grid_constant_
   const int qp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const BatchArgs& bt = a.bt;
   const int H = a.n_heads;
+  griddep_wait();  // the pools (and any metadata) may come from the preceding kernel
+  griddep_launch_dependents();
   const SeqMeta sm = load_meta(bt, b);
   if (!sm.ok) {
     if (threadIdx.x == 0 && qp == 0 && h == 0) report_error(bt.err, kErrBadShape);
@@ -523,6 +564,8 @@ __global__ void __launch_bounds__(128) state_merge_kernel(const __grid_constant_
   const int qp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const BatchArgs& bt = a.bt;
   const int H = a.n_heads;
+  griddep_wait();  // the fresh block keys (and any metadata) may come from the preceding kernel
+  griddep_launch_dependents();
   const SeqMeta sm = load_meta(bt, b);
   if (!sm.ok) {
     if (threadIdx.x == 0 && qp == 0 && h == 0) report_error(bt.err, kErrBadShape);
@@ -634,7 +677,35 @@ __global__ void __launch_bounds__(128) state_merge_kernel(const __grid_constant_
 // ================================================================ launchers
 template <class K>
 cudaError_t set_smem(K kern, int bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)  // all of the unified L1/shared storage as shared memory: more resident CTAs
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+// Launch with programmatic stream serialization (and an optional cluster shape).
+template <class K, class... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, int threads, int smem, int cluster_x, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 struct PoolMaps {
@@ -671,19 +742,7 @@ cudaError_t launch_block_attention_d(const AttnArgs& a, int num_sms, cudaStream_
   if (split > 8) split = 8;
   if (split > max_pages) split = max_pages;
   if (split < 1) split = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(split, a.n_heads, a.bt.batch);
-  cfg.blockDim = dim3(160);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m.k, m.v, a);
+  return launch_pdl(kern, dim3(split, a.n_heads, a.bt.batch), 160, smem, split, stream, m.k, m.v, a);
 }
 
 template <int D>
@@ -696,8 +755,7 @@ cudaError_t launch_state_build_d(const AttnArgs& a, cudaStream_t stream) {
   e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int max_pages = (a.bt.max_seq_len + kPage - 1) / kPage;
-  kern<<<dim3(max_pages, a.n_heads, a.bt.batch), 160, smem, stream>>>(m.q, m.k, m.v, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(max_pages, a.n_heads, a.bt.batch), 160, smem, 0, stream, m.q, m.k, m.v, a);
 }
 
 template <int D>
@@ -710,8 +768,7 @@ cudaError_t launch_state_merge_d(const AttnArgs& a, cudaStream_t stream) {
   e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int max_pages = (a.bt.max_seq_len + kPage - 1) / kPage;
-  kern<<<dim3(max_pages, a.n_heads, a.bt.batch), 128, smem, stream>>>(m.q, m.o, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(max_pages, a.n_heads, a.bt.batch), 128, smem, 0, stream, m.q, m.o, a);
 }
 
 }  // namespace

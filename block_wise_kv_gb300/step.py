@@ -61,12 +61,27 @@ class LayerStep:
         dllm.dllm_state_merge(self.desc, self.batch.c, self.cache.c, self.o_full, self.lse if lse else None, None,
                               stream)
 
-    def step(self, x_block: torch.Tensor, stream=None, lse: bool = True) -> None:
+    def step(self, x_block: torch.Tensor, stream=None, lse: bool = True, side_stream=None) -> None:
         """One inner denoising step of this layer: fused projection, block
-        attention, and the FACache merge for the invariant rows."""
+        attention, and the FACache merge for the invariant rows.
+
+        The block attention and the merge read the same cache and write
+        disjoint rows of o_full / lse, so with `side_stream` the merge runs on
+        it concurrently with the attention (fork after the projection, join
+        before returning); both streams may be under graph capture."""
         self.qkv(x_block, stream)
-        self.attention(stream, lse)
-        self.merge(stream, lse)
+        if side_stream is None:
+            self.attention(stream, lse)
+            self.merge(stream, lse)
+            return
+        main = stream if stream is not None else torch.cuda.current_stream()
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(main)
+        side_stream.wait_event(fork)
+        self.attention(main, lse)
+        self.merge(side_stream, lse)
+        join.record(side_stream)
+        main.wait_event(join)
 
     # ---------------------------------------------------------- inspection
     def seq_slice(self, b: int) -> slice:
