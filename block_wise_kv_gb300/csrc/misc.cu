@@ -10,7 +10,8 @@
 namespace dllm {
 namespace {
 
-constexpr int kNormThreads = 128;
+constexpr int kNormThreads = 256;
+constexpr int kNormVecs = 4;  // 16-byte vectors of the row kept in registers per thread (D <= 8192)
 
 // s + e == a + b exactly (Knuth's TwoSum), with the additions pinned to
 // round-to-nearest so that the compiler cannot contract or reorder them.
@@ -32,11 +33,37 @@ __device__ __forceinline__ uint16_t bf16_round_pair(float p, float e) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(p));
 }
 
+// 1 / sqrt(ss / D + eps) as an unevaluated pair (hi, lo) of floats, from the
+// exact sum of squares (ss_hi, ss_lo), in fp32 arithmetic only (fp64 is slow
+// on this part).  The quotient and the sum are carried as float pairs
+// (the division remainder by FMA is exact); the reciprocal square root is
+// one Newton-Raphson step y1 = y0 - y0 (s y0^2 - 1) / 2 from the hardware
+// estimate y0 (relative error e0 < 2^-21), with the residual s y0^2 - 1
+// formed from an exact product y0^2 and FMAs.  Newton's error (3/2) e0^2 and
+// the rounding of the residual leave |y1 / y - 1| below about 2^-40, far
+// inside the 2^-9 spacing that the bf16 rounding of x^ must resolve.
+__device__ __forceinline__ void rsqrt_pair(float ss_hi, float ss_lo, int D, float eps, float& y_hi, float& y_lo) {
+  const float fd = static_cast<float>(D);
+  const float q_hi = __fdiv_rn(ss_hi, fd);
+  const float rem = __fmaf_rn(-q_hi, fd, ss_hi);  // exact: ss_hi - q_hi * D
+  const float q_lo = __fdiv_rn(__fadd_rn(rem, ss_lo), fd);
+  float s_hi, e;
+  two_sum(q_hi, eps, s_hi, e);
+  const float s_lo = __fadd_rn(e, q_lo);
+  const float y0 = rsqrtf(s_hi);
+  const float p = __fmul_rn(y0, y0);
+  const float pe = __fmaf_rn(y0, y0, -p);  // y0^2 = p + pe exactly
+  const float u = __fmaf_rn(s_hi, p, -1.f);
+  const float t = __fadd_rn(u, __fmaf_rn(s_hi, pe, __fmul_rn(s_lo, p)));  // s y0^2 - 1
+  const float corr = __fmul_rn(__fmul_rn(-0.5f, y0), t);
+  two_sum(y0, corr, y_hi, y_lo);
+}
+
 // One CTA per row: x^ = x / sqrt(mean(x^2) + eps) * g rounded once to bf16.
 // Because x is bf16, each x*x is exact in fp32 and the sum of squares is
-// carried as an exact (hi, lo) pair; the scale is formed in fp64 and the
-// final product is evaluated error-free (FMA) so that the bf16 rounding is
-// the correctly rounded value of the real x^.  D % 8 == 0.
+// carried as an exact (hi, lo) pair; the scale is formed as a float pair and
+// the final product is evaluated error-free (FMA) so that the bf16 rounding
+// is the correctly rounded value of the real x^.  D % 8 == 0.
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
                                                                const __nv_bfloat16* __restrict__ gain,
                                                                __nv_bfloat16* __restrict__ out, int D, float eps,
@@ -53,9 +80,15 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
   const uint4* gr = reinterpret_cast<const uint4*>(gain);
   uint4* orow = reinterpret_cast<uint4*>(out + row * D);
   const int nvec = D / 8;
+  const bool in_regs = nvec <= kNormVecs * kNormThreads;
+  uint4 xv[kNormVecs];
+#pragma unroll
+  for (int j = 0; j < kNormVecs; ++j) {
+    const int v = threadIdx.x + j * kNormThreads;
+    xv[j] = (in_regs && v < nvec) ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+  }
   float hi = 0.f, lo = 0.f;
-  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
-    const uint4 u = __ldg(xr + v);
+  auto accumulate = [&](const uint4& u) {
     const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -66,6 +99,12 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
       two_sum(hi, __fmul_rn(f.y, f.y), hi, e);
       lo = __fadd_rn(lo, e);
     }
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < kNormVecs; ++j) accumulate(xv[j]);
+  } else {
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) accumulate(__ldg(xr + v));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -79,35 +118,44 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
     red_lo[threadIdx.x >> 5] = lo;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {  // fp64 is slow on this part: one thread forms the scale
-    double ss = 0.0;
+  // every thread forms the same scale from the per-warp pairs (fixed order)
+  hi = red_hi[0];
+  lo = red_lo[0];
 #pragma unroll
-    for (int w = 0; w < kNormThreads / 32; ++w) ss += static_cast<double>(red_hi[w]) + static_cast<double>(red_lo[w]);
-    const double inv = 1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps));
-    const float ih = static_cast<float>(inv);
-    red_hi[0] = ih;
-    red_lo[0] = static_cast<float>(inv - static_cast<double>(ih));
+  for (int w = 1; w < kNormThreads / 32; ++w) {
+    float e;
+    two_sum(hi, red_hi[w], hi, e);
+    lo = __fadd_rn(lo, __fadd_rn(e, red_lo[w]));
   }
-  __syncthreads();
-  const float inv_hi = red_hi[0], inv_lo = red_lo[0];
-  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
-    const uint4 u = __ldg(xr + v);
-    const uint4 gu = __ldg(gr + v);
+  float ss_hi, ss_lo;
+  two_sum(hi, lo, ss_hi, ss_lo);
+  float inv_hi, inv_lo;
+  rsqrt_pair(ss_hi, ss_lo, D, eps, inv_hi, inv_lo);
+  auto normalise = [&](const uint4& u, const uint4& gu) {
     const __nv_bfloat16* xp = reinterpret_cast<const __nv_bfloat16*>(&u);
     const __nv_bfloat16* gp = reinterpret_cast<const __nv_bfloat16*>(&gu);
     uint4 r;
     uint16_t* rp = reinterpret_cast<uint16_t*>(&r);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float xv = __bfloat162float(xp[i]), gv = __bfloat162float(gp[i]);
+      const float xf = __bfloat162float(xp[i]), gv = __bfloat162float(gp[i]);
       // c = inv * g as an unevaluated pair, then x * c with its exact error
       const float c_hi = __fmul_rn(inv_hi, gv);
       const float c_lo = __fadd_rn(__fmaf_rn(inv_hi, gv, -c_hi), __fmul_rn(inv_lo, gv));
-      const float p = __fmul_rn(xv, c_hi);
-      const float e = __fadd_rn(__fmaf_rn(xv, c_hi, -p), __fmul_rn(xv, c_lo));
+      const float p = __fmul_rn(xf, c_hi);
+      const float e = __fadd_rn(__fmaf_rn(xf, c_hi, -p), __fmul_rn(xf, c_lo));
       rp[i] = bf16_round_pair(p, e);
     }
-    orow[v] = r;
+    return r;
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < kNormVecs; ++j) {
+      const int v = threadIdx.x + j * kNormThreads;
+      if (v < nvec) orow[v] = normalise(xv[j], __ldg(gr + v));
+    }
+  } else {
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) orow[v] = normalise(__ldg(xr + v), __ldg(gr + v));
   }
 }
 
