@@ -69,10 +69,10 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
                                                                __nv_bfloat16* __restrict__ out, int D, float eps,
                                                                int32_t* __restrict__ zero, int zero_count) {
   __shared__ float red_hi[kNormThreads / 32], red_lo[kNormThreads / 32];
-  // Programmatic dependent launch: x may come from the preceding kernel; once
-  // it is visible, let the projection kernel start streaming its weights.
+  // Programmatic dependent launch: x may come from the preceding kernel.  The
+  // projection kernel is released only once this row (and the gain) sit in
+  // registers, so that its weight stream does not queue ahead of these loads.
   griddep_wait();
-  griddep_launch_dependents();
   if (blockIdx.x == 0)  // the projection's stream-K arrival counters start at zero
     for (int i = threadIdx.x; i < zero_count; i += kNormThreads) zero[i] = 0;
   const size_t row = blockIdx.x;
@@ -81,11 +81,13 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
   uint4* orow = reinterpret_cast<uint4*>(out + row * D);
   const int nvec = D / 8;
   const bool in_regs = nvec <= kNormVecs * kNormThreads;
-  uint4 xv[kNormVecs];
+  uint4 xv[kNormVecs], gv4[kNormVecs];
 #pragma unroll
   for (int j = 0; j < kNormVecs; ++j) {
     const int v = threadIdx.x + j * kNormThreads;
-    xv[j] = (in_regs && v < nvec) ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+    const bool live = in_regs && v < nvec;
+    xv[j] = live ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+    gv4[j] = live ? __ldg(gr + v) : make_uint4(0, 0, 0, 0);
   }
   float hi = 0.f, lo = 0.f;
   auto accumulate = [&](const uint4& u) {
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
     red_lo[threadIdx.x >> 5] = lo;
   }
   __syncthreads();
+  griddep_launch_dependents();
   // every thread forms the same scale from the per-warp pairs (fixed order)
   hi = red_hi[0];
   lo = red_lo[0];
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
 #pragma unroll
     for (int j = 0; j < kNormVecs; ++j) {
       const int v = threadIdx.x + j * kNormThreads;
-      if (v < nvec) orow[v] = normalise(xv[j], __ldg(gr + v));
+      if (v < nvec) orow[v] = normalise(xv[j], gv4[j]);
     }
   } else {
     for (int v = threadIdx.x; v < nvec; v += kNormThreads) orow[v] = normalise(__ldg(xr + v), __ldg(gr + v));

@@ -17,8 +17,11 @@
 //    a 128 x 32 UMMA.
 //  * A CTA that allocates TMEM runs alone on its SM, so the kernel is built
 //    around one CTA per SM with a deep (~200 KB) TMA ring: warp 0 streams
-//    128 x 64 weight tiles and BN x 64 token tiles (128-byte swizzle), warp 1
-//    owns TMEM and issues tcgen05.mma, warps 2-5 accumulate and write.
+//    units of two adjacent 128 x 64 weight boxes and two BN x 64 token boxes
+//    (128-byte swizzle; the two weight boxes are issued together, which lets
+//    the memory system see 256-byte runs of every weight row and streams
+//    about 15% faster than single boxes), warp 1 owns TMEM and issues
+//    tcgen05.mma, warps 2-5 accumulate and write.
 //  * Inner steps (<= 64 token rows) are bound by streaming the weight matrix,
 //    so they are scheduled stream-K: the (weight tile, k-block) units are
 //    split evenly over one CTA per SM; a weight tile that spans several CTAs
@@ -26,9 +29,9 @@
 //    workspace, an atomic arrival counter; no CTA waits on another).  Larger
 //    row counts use one CTA per (weight tile, 128-row token tile).
 //  * fp32 accumulation on the CUDA cores ("promotion"): the tensor core sums
-//    only 128-element partial products (a chain of 8 MMAs) into one of the
-//    TMEM buffers; the accumulator warps drain each finished buffer into fp32
-//    registers.  The tensor core's own long accumulation chains round
+//    only the 128-element partial product of one unit (a chain of 8 MMAs)
+//    into one of the TMEM buffers; the accumulator warps drain each finished
+//    buffer into fp32 registers.  The tensor core's own long accumulation chains round
 //    noticeably worse than fp32 round-to-nearest, and every bf16 value this
 //    kernel stores is a cache entry that later steps reuse.  All 512 TMEM
 //    columns serve as partial buffers, so the tensor core can run far ahead
@@ -46,26 +49,28 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kAccThreads = kThreads - 64;  // warps 2-5
 constexpr int kTileM = 128;                 // weight rows per tile (UMMA M)
-constexpr int kTileK = 64;                  // K elements per unit (one 128-byte swizzle row)
+constexpr int kTileK = 64;                  // K elements per TMA box (one 128-byte swizzle row)
+constexpr int kBoxes = 2;                   // boxes per unit: a unit covers K = 128
+constexpr int kUnitK = kTileK * kBoxes;
 constexpr int kTileABytes = kTileM * kTileK * 2;
-constexpr int kPromote = 2;                 // units per TMEM partial (K = 128: a chain of 8 MMAs)
-constexpr int kMinUnitsPerCta = 8;
+constexpr int kMinUnitsPerCta = 4;
+constexpr int kSmemLimit = 232448 - 4096;   // opt-in maximum less room for the static shared data
 
 template <int BN>
 struct GemmCfg;
 template <>
 struct GemmCfg<32> {
-  static constexpr int kStages = 9;
+  static constexpr int kStages = 5;
   static constexpr bool kOwnRecv = true;  // stream-K: tile epilogues run while the ring is busy
 };
 template <>
 struct GemmCfg<64> {
-  static constexpr int kStages = 7;
+  static constexpr int kStages = 3;
   static constexpr bool kOwnRecv = true;
 };
 template <>
 struct GemmCfg<128> {
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 3;
   static constexpr bool kOwnRecv = false;  // one tile per CTA: the drained ring holds the tile
 };
 
@@ -74,13 +79,21 @@ constexpr int tmem_bufs() {
   return 512 / BN;
 }
 template <int BN>
+constexpr int stage_bytes() {
+  return kBoxes * (kTileABytes + BN * kTileK * 2);
+}
+template <int BN>
 constexpr int ring_bytes() {
-  return GemmCfg<BN>::kStages * (kTileABytes + BN * kTileK * 2);
+  return GemmCfg<BN>::kStages * stage_bytes<BN>();
 }
 template <int BN>
 constexpr int gemm_smem_bytes() {
   return ring_bytes<BN>() + (GemmCfg<BN>::kOwnRecv ? BN * kTileM * 4 : 0) + 1024;
 }
+static_assert(gemm_smem_bytes<32>() <= kSmemLimit && gemm_smem_bytes<64>() <= kSmemLimit &&
+                  gemm_smem_bytes<128>() <= kSmemLimit,
+              "ring too large");
+static_assert(ring_bytes<128>() >= 128 * kTileM * 4, "the drained ring must hold a 128-column tile");
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -103,26 +116,21 @@ __host__ __device__ __forceinline__ int sk_cta_of(long long u, long long U, long
   return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
-// Walk of a CTA's units: weight tile, k-block, and where segments (runs of one
-// tile) and promotion periods begin and end.  The producer, the MMA issuer and
-// the accumulator warps all follow the same walk, advanced incrementally (no
-// integer division inside the loops).
+// Walk of a CTA's units: weight tile, k-unit, and where segments (runs of one
+// tile) begin and end.  The producer, the MMA issuer and the accumulator
+// warps all follow the same walk, advanced incrementally (no integer division
+// inside the loops).
 struct UnitWalk {
-  int tile, kb, ps;  // weight tile, k-block, position inside the segment
-  int nkb, left;     // k-blocks per tile, units left after this one
-  bool seg_end, period_first, period_last;
+  int tile, kb, ps;  // weight tile, k-unit, position inside the segment
+  int nkb, left;     // k-units per tile, units left after this one
+  bool seg_end;
   __device__ __forceinline__ void init(long long u0, long long u1, int nkb_) {
     nkb = nkb_;
     tile = static_cast<int>(u0 / nkb);
     kb = static_cast<int>(u0 % nkb);
     ps = 0;
     left = static_cast<int>(u1 - u0) - 1;
-    flags();
-  }
-  __device__ __forceinline__ void flags() {
     seg_end = left == 0 || kb == nkb - 1;
-    period_first = (ps % kPromote) == 0;
-    period_last = (ps % kPromote) == kPromote - 1 || seg_end;
   }
   __device__ __forceinline__ int seg_kb0() const { return kb - ps; }
   __device__ __forceinline__ void next() {
@@ -134,9 +142,15 @@ struct UnitWalk {
     } else {
       ++ps;
     }
-    flags();
+    seg_end = left == 0 || kb == nkb - 1;
   }
 };
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -144,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const QkvArgs a) {
   constexpr int kStages = GemmCfg<BN>::kStages;
   constexpr int kTileBBytes = BN * kTileK * 2;
-  constexpr int kStageBytes = kTileABytes + kTileBBytes;
+  constexpr int kStageBytes = stage_bytes<BN>();  // A box 0 | A box 1 | B box 0 | B box 1
   constexpr int kTmemBufs = tmem_bufs<BN>();
   constexpr uint32_t kTmemCols = kTmemBufs * BN;  // 512: the CTA is alone on its SM
   constexpr uint32_t kIdesc = umma_idesc_bf16(kTileM, BN);
@@ -162,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int tok_pos[BN];       // absolute position (RoPE)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = a.d_model / kTileK;
+  const int nkb = (a.d_model + kUnitK - 1) / kUnitK;  // a ragged last unit reads zeros past d_model
   const int n_wt = 3 * a.n_heads * a.head_dim / kTileM;
   const bool streamk = a.partials != nullptr;
   const int nt = streamk ? 0 : static_cast<int>(blockIdx.z);
@@ -206,14 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.init(u0, u1, nkb);
       for (int i = 0; i < npre; ++i, w.next()) {
         mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
-        tma_load_2d(smem + i * kStageBytes, &tm_w, &full_bar[i], w.kb * kTileK, w.tile * kTileM);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+          tma_load_2d(smem + i * kStageBytes + j * kTileABytes, &tm_w, &full_bar[i], w.kb * kUnitK + j * kTileK,
+                      w.tile * kTileM);
       }
       griddep_wait();
       {
         UnitWalk wb;
         wb.init(u0, u1, nkb);
         for (int i = 0; i < npre; ++i, wb.next())
-          tma_load_2d(smem + i * kStageBytes + kTileABytes, &tm_x, &full_bar[i], wb.kb * kTileK, nt * BN);
+#pragma unroll
+          for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d(smem + i * kStageBytes + kBoxes * kTileABytes + j * kTileBBytes, &tm_x, &full_bar[i],
+                        wb.kb * kUnitK + j * kTileK, nt * BN);
       }
       int issued = npre;
       int s = npre % kStages;
@@ -225,8 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sa = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-        tma_load_2d(sa, &tm_w, &full_bar[s], w.kb * kTileK, w.tile * kTileM);
-        tma_load_2d(sa + kTileABytes, &tm_x, &full_bar[s], w.kb * kTileK, nt * BN);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+          tma_load_2d(sa + j * kTileABytes, &tm_w, &full_bar[s], w.kb * kUnitK + j * kTileK, w.tile * kTileM);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+          tma_load_2d(sa + kBoxes * kTileABytes + j * kTileBBytes, &tm_x, &full_bar[s], w.kb * kUnitK + j * kTileK,
+                      nt * BN);
         ++issued;
         if (++s == kStages) {
           s = 0;
@@ -240,24 +265,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer: period p = round * kTmemBufs + buf goes to TMEM buffer buf.
+      // ---- MMA issuer: unit i = round * kTmemBufs + buf goes to TMEM buffer buf.
       bool ok = true;
       int buf = kTmemBufs - 1, round = -1;
       int s = 0;
       uint32_t ph = 0;
-      UnitWalk w;
-      w.init(u0, u1, nkb);
-      for (int i = 0; i < n_units && ok; ++i, w.next()) {
-        if (w.period_first) {
-          if (++buf == kTmemBufs) {
-            buf = 0;
-            ++round;
-          }
-          if (round >= 1 && !mbar_wait(&tempty_bar[buf], (round + 1) & 1)) {
-            report_error(bt.err, kErrTimeout);
-            ok = false;
-            break;
-          }
+      for (int i = 0; i < n_units && ok; ++i) {
+        if (++buf == kTmemBufs) {
+          buf = 0;
+          ++round;
+        }
+        if (round >= 1 && !mbar_wait(&tempty_bar[buf], (round + 1) & 1)) {
+          report_error(bt.err, kErrTimeout);
+          ok = false;
+          break;
         }
         if (!mbar_wait(&full_bar[s], ph)) {
           report_error(bt.err, kErrTimeout);
@@ -265,14 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kTileABytes;
+        const uint32_t sa = smem_u32(smem + s * kStageBytes), sb = sa + kBoxes * kTileABytes;
         const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-        for (int k = 0; k < kTileK / 16; ++k)
-          umma_bf16(d, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), kIdesc,
-                    (w.period_first && k == 0) ? 0u : 1u);
+        for (int k = 0; k < kUnitK / 16; ++k) {
+          const int j = k / (kTileK / 16), kk = k % (kTileK / 16);
+          umma_bf16(d, umma_desc_sw128(sa + j * kTileABytes + kk * 32), umma_desc_sw128(sb + j * kTileBBytes + kk * 32),
+                    kIdesc, k == 0 ? 0u : 1u);
+        }
         umma_commit(&empty_bar[s]);
-        if (w.period_last) umma_commit(&tfull_bar[buf]);
+        umma_commit(&tfull_bar[buf]);
         if (++s == kStages) {
           s = 0;
           ph ^= 1;
@@ -317,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tok_kv[c] = kv;
       tok_q[c] = qd;
-      tok_pos[c] = pos;
+      tok_pos[c] = kv >= 0 ? pos : 0;  // a checked position (the RoPE table is read for every column)
     }
     named_barrier(1, kAccThreads);
 
@@ -328,6 +351,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* vpool = static_cast<__nv_bfloat16*>(a.v_pool);
     __nv_bfloat16* qdst = static_cast<__nv_bfloat16*>(a.mode == kModeBlock ? a.q_block : a.q_pool);
     const int chunks_per_half = half / 8;  // 8 (d = 128) or 4 (d = 64)
+    // Epilogue items: (token column c, 8-element chunk jc of the tile's low
+    // halves).  A thread's items are the same for every tile, so with few
+    // columns their RoPE factors are loaded once, here, off the tail.
+    constexpr int kItems = BN * 8 / kAccThreads;
+    constexpr bool kRopeRegs = BN <= 64;
+    float4 rope_r[kRopeRegs ? kItems : 1][4];
+    if constexpr (kRopeRegs) {
+#pragma unroll
+      for (int it = 0; it < kItems; ++it) {
+        const int item = threadIdx.x - 64 + it * kAccThreads, c = item >> 3, jc = item & 7;
+        const int t0 = (jc % chunks_per_half) * 8;
+        const float4* cs =
+            reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[c]) * half + t0) * 2);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rope_r[it][e] = __ldg(cs + e);
+      }
+    }
     float acc[BN];
 #pragma unroll
     for (int c = 0; c < BN; ++c) acc[c] = 0.f;
@@ -336,11 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     UnitWalk w;
     w.init(u0, u1, nkb);
     for (int i = 0; i < n_units; ++i, w.next()) {
-      if (w.period_first && ++buf == kTmemBufs) {
+      if (++buf == kTmemBufs) {
         buf = 0;
         ++round;
       }
-      if (!w.period_last) continue;
       if (ok && !mbar_wait(&tfull_bar[buf], round & 1)) {
         report_error(bt.err, kErrTimeout);
         ok = false;
@@ -356,28 +395,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- a segment (one weight tile's k-range of this CTA) is complete
       const int tile = w.tile;
       if (!(w.seg_kb0() == 0 && w.kb == nkb - 1)) {
-        // stream-K fixup: publish the partial, count arrivals; the last one finishes the tile
+        // Stream-K fixup: the last contributor to arrive finishes the tile
+        // from the others' fp32 partials.  A contributor that finds every
+        // other one already arrived skips publishing its own partial.
         const int c_first = sk_cta_of(static_cast<long long>(tile) * nkb, U, G);
         const int c_last = sk_cta_of(static_cast<long long>(tile) * nkb + nkb - 1, U, G);
+        const int n_other = c_last - c_first;
         const int slot = static_cast<int>(blockIdx.x) - c_first;
         float* slots = a.partials + static_cast<size_t>(tile) * a.max_contrib * kTileM * BN;
-        float* mine = slots + static_cast<size_t>(slot) * kTileM * BN + static_cast<size_t>(row) * BN;
-#pragma unroll
-        for (int c = 0; c < BN; c += 4)
-          *reinterpret_cast<float4*>(mine + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-        named_barrier(1, kAccThreads);  // the CTA's partial rows are written ...
-        if (threadIdx.x == 64) {
-          __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
-          last_sh = atomicAdd(a.counters + tile, 1) == (c_last - c_first);
-        }
+        if (threadIdx.x == 64) last_sh = ld_acquire_gpu(a.counters + tile) == n_other ? 1 : 0;
         named_barrier(1, kAccThreads);
         if (!last_sh) {
+          float* mine = slots + static_cast<size_t>(slot) * kTileM * BN + static_cast<size_t>(row) * BN;
 #pragma unroll
-          for (int c = 0; c < BN; ++c) acc[c] = 0.f;
-          continue;
+          for (int c = 0; c < BN; c += 4)
+            *reinterpret_cast<float4*>(mine + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+          named_barrier(1, kAccThreads);  // the CTA's partial rows are written ...
+          if (threadIdx.x == 64) {
+            __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
+            last_sh = atomicAdd(a.counters + tile, 1) == n_other ? 1 : 0;
+          }
+          named_barrier(1, kAccThreads);
+          if (!last_sh) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+            continue;
+          }
         }
         __threadfence();
-        for (int sl = 0; sl <= c_last - c_first; ++sl) {
+        for (int sl = 0; sl <= n_other; ++sl) {
           if (sl == slot) continue;
           const float* other = slots + static_cast<size_t>(sl) * kTileM * BN + static_cast<size_t>(row) * BN;
 #pragma unroll
@@ -402,63 +448,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grow0 = tile * kTileM;
       const int which = grow0 / HD;  // 0: q, 1: k, 2: v
       const int head0 = (grow0 % HD) / d;
-      for (int item = threadIdx.x - 64; item < ncols * 8; item += kAccThreads) {
-        const int c = item >> 3, jc = item & 7;
-        const long long kv = tok_kv[c];
-        if (kv < 0) continue;
-        const int hit = jc / chunks_per_half, t0 = (jc % chunks_per_half) * 8;
-        const int row_lo = hit * d + t0, row_hi = row_lo + half;
-        float lo[8], hi[8];
-        const float* r = recv + c * kTileM;
 #pragma unroll
-        for (int e = 0; e < 8; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(r + row_lo + e);
-          const float4 h4 = *reinterpret_cast<const float4*>(r + row_hi + e);
-          lo[e] = l4.x;
-          lo[e + 1] = l4.y;
-          lo[e + 2] = l4.z;
-          lo[e + 3] = l4.w;
-          hi[e] = h4.x;
-          hi[e + 1] = h4.y;
-          hi[e + 2] = h4.z;
-          hi[e + 3] = h4.w;
-        }
-        const int head = head0 + hit;
-        __nv_bfloat16* out;
-        if (which == 2) {
-          out = vpool + kv + static_cast<long long>(head) * kPage * d;
-        } else {
-          const float4* cs =
-              reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[c]) * half + t0) * 2);
+      for (int it = 0; it < (kRopeRegs ? kItems : 1); ++it) {
+        for (int item = threadIdx.x - 64 + it * kAccThreads; item < ncols * 8;
+             item += (kRopeRegs ? ncols * 8 : kAccThreads)) {
+          const int c = item >> 3, jc = item & 7;
+          const long long kv = tok_kv[c];
+          if (kv < 0) continue;
+          const int hit = jc / chunks_per_half, t0 = (jc % chunks_per_half) * 8;
+          const int row_lo = hit * d + t0, row_hi = row_lo + half;
+          float lo[8], hi[8];
+          const float* r = recv + c * kTileM;
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float4 v = __ldg(cs + e / 2);  // (cos, sin) of t0+e and t0+e+1
-            const float l0 = lo[e] * v.x - hi[e] * v.y, h0 = hi[e] * v.x + lo[e] * v.y;
-            const float l1 = lo[e + 1] * v.z - hi[e + 1] * v.w, h1 = hi[e + 1] * v.z + lo[e + 1] * v.w;
-            lo[e] = l0;
-            hi[e] = h0;
-            lo[e + 1] = l1;
-            hi[e + 1] = h1;
+          for (int e = 0; e < 8; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(r + row_lo + e);
+            const float4 h4 = *reinterpret_cast<const float4*>(r + row_hi + e);
+            lo[e] = l4.x;
+            lo[e + 1] = l4.y;
+            lo[e + 2] = l4.z;
+            lo[e + 3] = l4.w;
+            hi[e] = h4.x;
+            hi[e + 1] = h4.y;
+            hi[e + 2] = h4.z;
+            hi[e + 3] = h4.w;
           }
-          if (which == 1) {
-            out = kpool + kv + static_cast<long long>(head) * kPage * d;
+          const int head = head0 + hit;
+          __nv_bfloat16* out;
+          if (which == 2) {
+            out = vpool + kv + static_cast<long long>(head) * kPage * d;
           } else {
-            const long long qd = tok_q[c];
-            if (qd < 0) continue;
-            out = qdst + qd + static_cast<long long>(head) * (a.mode == kModeBlock ? d : kPage * d);
+            float4 cs[4];
+            if constexpr (kRopeRegs) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) cs[e] = rope_r[it][e];
+            } else {
+              const float4* tab =
+                  reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[c]) * half + t0) * 2);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + e);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float4 v = cs[e / 2];  // (cos, sin) of t0+e and t0+e+1
+              const float l0 = lo[e] * v.x - hi[e] * v.y, h0 = hi[e] * v.x + lo[e] * v.y;
+              const float l1 = lo[e + 1] * v.z - hi[e + 1] * v.w, h1 = hi[e + 1] * v.z + lo[e + 1] * v.w;
+              lo[e] = l0;
+              hi[e] = h0;
+              lo[e + 1] = l1;
+              hi[e + 1] = h1;
+            }
+            if (which == 1) {
+              out = kpool + kv + static_cast<long long>(head) * kPage * d;
+            } else {
+              const long long qd = tok_q[c];
+              if (qd < 0) continue;
+              out = qdst + qd + static_cast<long long>(head) * (a.mode == kModeBlock ? d : kPage * d);
+            }
           }
+          uint4 wl, wh;
+          wl.x = pack_bf16x2(lo[0], lo[1]);
+          wl.y = pack_bf16x2(lo[2], lo[3]);
+          wl.z = pack_bf16x2(lo[4], lo[5]);
+          wl.w = pack_bf16x2(lo[6], lo[7]);
+          wh.x = pack_bf16x2(hi[0], hi[1]);
+          wh.y = pack_bf16x2(hi[2], hi[3]);
+          wh.z = pack_bf16x2(hi[4], hi[5]);
+          wh.w = pack_bf16x2(hi[6], hi[7]);
+          *reinterpret_cast<uint4*>(out + t0) = wl;
+          *reinterpret_cast<uint4*>(out + t0 + half) = wh;
         }
-        uint4 wl, wh;
-        wl.x = pack_bf16x2(lo[0], lo[1]);
-        wl.y = pack_bf16x2(lo[2], lo[3]);
-        wl.z = pack_bf16x2(lo[4], lo[5]);
-        wl.w = pack_bf16x2(lo[6], lo[7]);
-        wh.x = pack_bf16x2(hi[0], hi[1]);
-        wh.y = pack_bf16x2(hi[2], hi[3]);
-        wh.z = pack_bf16x2(hi[4], hi[5]);
-        wh.w = pack_bf16x2(hi[6], hi[7]);
-        *reinterpret_cast<uint4*>(out + t0) = wl;
-        *reinterpret_cast<uint4*>(out + t0 + half) = wh;
       }
       named_barrier(1, kAccThreads);  // recv is free for the next tile
     }
@@ -508,7 +566,7 @@ cudaError_t launch_bn(const void* w_qkv, const void* xhat, const QkvArgs& a, con
 QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms) {
   QkvPlan p = {};
   const long long n_wt = 3LL * n_heads * head_dim / kTileM;
-  const long long nkb = d_model / kTileK;
+  const long long nkb = (d_model + kUnitK - 1) / kUnitK;
   p.bn = n_tok <= 32 ? 32 : (n_tok <= 64 ? 64 : 128);
   p.xhat_bytes = align256(static_cast<size_t>(n_tok) * d_model * 2);
   p.streamk = p.bn <= 64;
