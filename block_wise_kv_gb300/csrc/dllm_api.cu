@@ -183,6 +183,26 @@ dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* b
   }
 }
 
+dllm_status dllm_qkv_weight_packed_bytes(const dllm_layer_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return DLLM_ERR_INVALID_ARGUMENT;
+  DLLM_TRY(check_desc(desc));
+  *bytes = qkv_packed_bytes(desc->d_model, desc->n_heads, desc->head_dim);
+  return DLLM_OK;
+}
+
+dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv, void* w_packed, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  if (!aligned(w_qkv, 16) || !aligned(w_packed, 16))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  const size_t in_bytes = static_cast<size_t>(3) * desc->n_heads * desc->head_dim * desc->d_model * 2;
+  const size_t out_bytes = qkv_packed_bytes(desc->d_model, desc->n_heads, desc->head_dim);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w_qkv), b = reinterpret_cast<uintptr_t>(w_packed);
+  if (a < b + out_bytes && b < a + in_bytes) return DLLM_ERR_INVALID_ARGUMENT;  // overlapping
+  DLLM_CUDA_TRY(launch_qkv_pack(w_qkv, w_packed, 3 * desc->n_heads * desc->head_dim, desc->d_model,
+                                static_cast<cudaStream_t>(stream)));
+  return DLLM_OK;
+}
+
 dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, float* rope_table, void* stream) {
   DLLM_TRY(check_desc(desc));
   if (max_pos < 1 || !aligned(rope_table, 8)) return DLLM_ERR_INVALID_ARGUMENT;
@@ -191,13 +211,13 @@ dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, 
 }
 
 dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_full,
-                             const void* rms_gain, const void* w_qkv, const float* rope_table, int32_t rope_max_pos,
+                             const void* rms_gain, const void* w_packed, const float* rope_table, int32_t rope_max_pos,
                              const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream) {
   DLLM_TRY(check_desc(desc));
   DLLM_TRY(check_batch(batch));
   if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
   DLLM_TRY(check_cache(cache, desc, true, true));
-  if (!aligned(x_full, 16) || !aligned(rms_gain, 16) || !aligned(w_qkv, 16) || !aligned(rope_table, 8))
+  if (!aligned(x_full, 16) || !aligned(rms_gain, 16) || !aligned(w_packed, 16) || !aligned(rope_table, 8))
     return DLLM_ERR_INVALID_ARGUMENT;
   if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
   size_t need = 0;
@@ -213,21 +233,21 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
   DLLM_CUDA_TRY(launch_rmsnorm(x_full, rms_gain, ws, batch->total_seq_rows, desc->d_model, desc->rms_eps, qa.counters,
                                plan.n_counters, s));
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, plan, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, ws, qa, plan, s));
   const AttnArgs aa = attn_args(desc, batch, cache);
   DLLM_CUDA_TRY(launch_state_build(aa, s));
   return DLLM_OK;
 }
 
 dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_block,
-                                      const void* rms_gain, const void* w_qkv, const float* rope_table,
+                                      const void* rms_gain, const void* w_packed, const float* rope_table,
                                       int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
                                       size_t ws_bytes, void* stream) {
   DLLM_TRY(check_desc(desc));
   DLLM_TRY(check_batch(batch));
   if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
   DLLM_TRY(check_cache(cache, desc, false, false));
-  if (!aligned(x_block, 16) || !aligned(rms_gain, 16) || !aligned(w_qkv, 16) || !aligned(rope_table, 8) ||
+  if (!aligned(x_block, 16) || !aligned(rms_gain, 16) || !aligned(w_packed, 16) || !aligned(rope_table, 8) ||
       !aligned(q_block, 16))
     return DLLM_ERR_INVALID_ARGUMENT;
   if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
@@ -243,7 +263,7 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
   bind_workspace(&qa, plan, ws);
   DLLM_CUDA_TRY(launch_rmsnorm(x_block, rms_gain, ws, batch->total_block_rows, desc->d_model, desc->rms_eps,
                                qa.counters, plan.n_counters, s));
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_qkv, ws, qa, plan, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, ws, qa, plan, s));
   return DLLM_OK;
 }
 

@@ -50,10 +50,21 @@ struct QkvArgs {
   int32_t max_contrib;         // partial slots per weight tile
 };
 
+// Tile-packed projection weight.  Box (t, kb) = rows [128t, 128t + 128) x
+// columns [64kb, 64kb + 64) of W_qkv is 16 KB contiguous at element
+// ((t * boxes_per_tile + kb) * 128 + r) * 64 + c; boxes_per_tile =
+// 2 * ceil(d_model / 128), columns past d_model are zero.  A CTA streaming one
+// tile's K range then reads one contiguous run of memory.
+inline int qkv_boxes_per_tile(int d_model) { return 2 * ((d_model + 127) / 128); }
+inline size_t qkv_packed_bytes(int d_model, int n_heads, int head_dim) {
+  return static_cast<size_t>(3) * n_heads * head_dim * qkv_boxes_per_tile(d_model) * 64 * 2;
+}
+cudaError_t launch_qkv_pack(const void* w, void* packed, int rows, int d_model, cudaStream_t stream);
+
 // Workspace layout and schedule of the fused projection for n_tok rows.
 struct QkvPlan {
   int bn;            // token tile (32, 64 or 128)
-  bool streamk;      // stream-K over (weight tile, k-block) units, else one CTA per tile
+  bool streamk;      // stream-K over (weight tile, k-unit) units, else one CTA per (weight tile, token tile)
   int grid;          // CTAs of the stream-K schedule
   int max_contrib;   // stream-K: most CTAs sharing one weight tile
   int n_counters;    // arrival counters (one per weight tile) to zero before the projection
@@ -86,7 +97,7 @@ cudaError_t launch_rmsnorm(const void* x, const void* gain, void* out, int rows,
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double theta, cudaStream_t stream);
 cudaError_t launch_zero_tails(const BatchArgs& bt, void* k_pool, void* v_pool, void* q_pool, int n_heads,
                               int head_dim, cudaStream_t stream);
-cudaError_t launch_qkv_gemm(const void* w_qkv, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
+cudaError_t launch_qkv_gemm(const void* w_packed, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
                             cudaStream_t stream);
 cudaError_t launch_block_attention(const AttnArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_state_build(const AttnArgs& a, cudaStream_t stream);

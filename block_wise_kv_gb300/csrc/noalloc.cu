@@ -54,7 +54,7 @@ dllm_status scratch_address(void** out) {
 
 extern "C" dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* desc, const dllm_batch* batch,
                                                          const void* x_block, const void* rms_gain,
-                                                         const void* w_qkv, const float* rope_table,
+                                                         const void* w_packed, const float* rope_table,
                                                          int32_t rope_max_pos, const dllm_cache* cache,
                                                          void* q_block, void* stream) {
   size_t need = 0;
@@ -64,6 +64,6 @@ extern "C" dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* 
   void* scratch = nullptr;
   const dllm_status ss = scratch_address(&scratch);
   if (ss != DLLM_OK) return ss;
-  return dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_qkv, rope_table, rope_max_pos, cache, q_block,
+  return dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_packed, rope_table, rope_max_pos, cache, q_block,
                                    scratch, kNoAllocScratchBytes, stream);
 }

@@ -41,8 +41,9 @@ DLLM_OP_STATE_MERGE = 3
 PAGE = 64
 
 # Every symbol include/dllm.h declares.
-EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_cache_build", "dllm_block_qkv_rope_write",
-           "dllm_block_qkv_rope_write_noalloc", "dllm_block_attention", "dllm_state_merge", "dllm_status_string")
+EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_qkv_weight_packed_bytes", "dllm_qkv_weight_pack",
+           "dllm_cache_build", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
+           "dllm_block_attention", "dllm_state_merge", "dllm_status_string")
 
 
 class DllmError(RuntimeError):
@@ -91,6 +92,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
             sig = {
                 "dllm_workspace_size": [P(LayerDescC), P(BatchC), i32, P(sz)],
                 "dllm_rope_table_build": [P(LayerDescC), i32, vp, vp],
+                "dllm_qkv_weight_packed_bytes": [P(LayerDescC), P(sz)],
+                "dllm_qkv_weight_pack": [P(LayerDescC), vp, vp, vp],
                 "dllm_cache_build": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, sz, vp],
                 "dllm_block_qkv_rope_write": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, vp, sz,
                                               vp],
@@ -151,25 +154,45 @@ def dllm_rope_table_build(desc: LayerDescC, max_pos: int, rope_table: torch.Tens
                                                                  _stream(stream)))
 
 
-def dllm_cache_build(desc, batch, x_full, rms_gain, w_qkv, rope_table, rope_max_pos, cache, ws, stream=None):
+def dllm_qkv_weight_packed_bytes(desc: LayerDescC) -> int:
+    out = ctypes.c_size_t(0)
+    _check("dllm_qkv_weight_packed_bytes", load().dllm_qkv_weight_packed_bytes(ctypes.byref(desc), ctypes.byref(out)))
+    return out.value
+
+
+def dllm_qkv_weight_pack(desc: LayerDescC, w_qkv: torch.Tensor, w_packed: torch.Tensor, stream=None) -> None:
+    _check("dllm_qkv_weight_pack", load().dllm_qkv_weight_pack(ctypes.byref(desc), _ptr(w_qkv), _ptr(w_packed),
+                                                               _stream(stream)))
+
+
+def pack_qkv_weight(desc: LayerDescC, w_qkv: torch.Tensor, stream=None) -> torch.Tensor:
+    """The tile-packed copy of a device bf16 [3*H*d][d_model] weight that the
+    projection calls take (allocated here, filled by dllm_qkv_weight_pack)."""
+    n = dllm_qkv_weight_packed_bytes(desc)
+    out = torch.empty(n // 2, dtype=torch.bfloat16, device=w_qkv.device)
+    dllm_qkv_weight_pack(desc, w_qkv.contiguous(), out, stream)
+    return out
+
+
+def dllm_cache_build(desc, batch, x_full, rms_gain, w_packed, rope_table, rope_max_pos, cache, ws, stream=None):
     _check("dllm_cache_build", load().dllm_cache_build(
-        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_full), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
+        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_full), _ptr(rms_gain), _ptr(w_packed), _ptr(rope_table),
         int(rope_max_pos), ctypes.byref(cache), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
-def dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_qkv, rope_table, rope_max_pos, cache, q_block, ws,
-                              stream=None):
+def dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_packed, rope_table, rope_max_pos, cache, q_block,
+                              ws, stream=None):
     _check("dllm_block_qkv_rope_write", load().dllm_block_qkv_rope_write(
-        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
+        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_packed), _ptr(rope_table),
         int(rope_max_pos), ctypes.byref(cache), _ptr(q_block), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
-def dllm_block_qkv_rope_write_noalloc(desc, batch, x_block, rms_gain, w_qkv, rope_table, rope_max_pos, cache,
+def dllm_block_qkv_rope_write_noalloc(desc, batch, x_block, rms_gain, w_packed, rope_table, rope_max_pos, cache,
                                       q_block, stream=None):
     """dllm_block_qkv_rope_write without a workspace: for callers that cannot
     allocate device memory (the library's fixed 8 MiB scratch is used)."""
     _check("dllm_block_qkv_rope_write_noalloc", load().dllm_block_qkv_rope_write_noalloc(
-        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_qkv), _ptr(rope_table),
+        ctypes.byref(desc), ctypes.byref(batch), _ptr(x_block), _ptr(rms_gain), _ptr(w_packed), _ptr(rope_table),
         int(rope_max_pos), ctypes.byref(cache), _ptr(q_block), _stream(stream)))
 
 

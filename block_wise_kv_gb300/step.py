@@ -24,13 +24,14 @@ class LayerStep:
         self.device = device
         wl = Workload(cfg)
         W, g = weights if weights is not None else wl.weights(layer)
-        self.w_qkv = W.to(device).contiguous()
         self.gain = g.to(device).contiguous()
         lay = layout(cfg, blocks)
         self.host_layout = lay
         self.batch = dllm.BatchLayout(lay["block_table"], lay["seq_len"], lay["block_start"], lay["block_len"],
                                       device=device)
         self.desc = dllm.layer_desc(cfg.d_model, cfg.n_heads, cfg.head_dim, cfg.rope_theta, cfg.rms_eps)
+        # the projection calls read the weight in its tile-packed form
+        self.w_qkv = dllm.pack_qkv_weight(self.desc, W.to(device))
         self.rope_max_pos = int(rope_max_pos or self.batch.max_seq_len)
         self.rope = torch.empty(self.rope_max_pos, cfg.head_dim // 2, 2, dtype=torch.float32, device=device)
         dllm.dllm_rope_table_build(self.desc, self.rope_max_pos, self.rope)

@@ -52,7 +52,14 @@
  *   token at position p of sequence b lives at page block_table[b][p / 64],
  *   slot p % 64.
  *   w_qkv:   bf16 [3 * n_heads * head_dim][d_model]; rows are Q heads, then K
- *            heads, then V heads, head-major, head_dim rows per head.
+ *            heads, then V heads, head-major, head_dim rows per head.  The
+ *            projection calls read it in the tile-packed form w_packed
+ *            written once per layer by dllm_qkv_weight_pack:
+ *   w_packed: bf16; box (t, kb) = rows [128t, 128t+128) x columns
+ *            [64kb, 64kb+64) of w_qkv is stored contiguously (row-major
+ *            128 x 64) at element ((t * KB + kb) * 128) * 64, with
+ *            KB = 2 * ceil(d_model / 128) boxes per 128-row tile and zeros in
+ *            the columns past d_model.
  *   rms_gain: bf16 [d_model].
  *   rope_table: fp32 [rope_max_pos][head_dim / 2][2] = (cos, sin) of
  *            p * rope_theta^(-2i/head_dim); filled by dllm_rope_table_build.
@@ -142,6 +149,18 @@ dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* b
  * and rounded to fp32.  RoPE: LaCache Eq. (1); rotate-half pairs (i, i+d/2). */
 dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, float* rope_table, void* stream);
 
+/* Bytes of the tile-packed projection weight of this layer shape:
+ * 3 * n_heads * head_dim * 2 * ceil(d_model / 128) * 64 * 2. */
+dllm_status dllm_qkv_weight_packed_bytes(const dllm_layer_desc* desc, size_t* bytes);
+
+/* Write the tile-packed copy of w_qkv (layout above) that dllm_cache_build and
+ * dllm_block_qkv_rope_write read.  A pure reordering (bit-exact), done once
+ * per layer when the weights are loaded, so that every projection streams
+ * whole 16 KB runs of weight memory (no counterpart in the pages: a layout
+ * choice of this library).  w_qkv and w_packed: device, 16-byte aligned,
+ * not overlapping; w_packed holds dllm_qkv_weight_packed_bytes bytes. */
+dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv, void* w_packed, void* stream);
+
 /* Block boundary (LaCache Algorithm 1 with GenStep = True; Fast-dLLM
  * compute_block_dual_cache).  For every row of every sequence:
  *   x^ = RMSNorm(x) (fp32, rounded to bf16), [q k v] = x^ W_qkv^T (fp32
@@ -155,11 +174,11 @@ dllm_status dllm_rope_table_build(const dllm_layer_desc* desc, int32_t max_pos, 
  * written to m_pool, l_pool, o_pool at row r's slot.  If U_b is empty for a
  * row's keys, m = -inf, l = 0, O~ = 0.
  *   x_full: device bf16 [R][d_model]; rms_gain: device bf16 [d_model];
- *   w_qkv: device bf16 [3*H*d][d_model]; rope_table: device fp32, rope_max_pos
+ *   w_packed: device, from dllm_qkv_weight_pack; rope_table: device fp32, rope_max_pos
  *   >= max_seq_len positions; ws: device scratch of
  *   dllm_workspace_size(DLLM_OP_CACHE_BUILD) bytes. */
 dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_full,
-                             const void* rms_gain, const void* w_qkv, const float* rope_table, int32_t rope_max_pos,
+                             const void* rms_gain, const void* w_packed, const float* rope_table, int32_t rope_max_pos,
                              const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream);
 
 /* Inner step, part 1 (LaCache §3.3.2 Eq. (1); Flash-dLLM Flash-Cache): for
@@ -168,9 +187,10 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
  * position p = s_b + i, then one write: k, v as bf16 into k_pool / v_pool at
  * (block_table[b][p/64], h, p%64) and q as bf16 into q_block [M][H][d].
  *   x_block: device bf16 [M][d_model]; q_block: device bf16 [M][H][d];
+ *   w_packed: device, from dllm_qkv_weight_pack;
  *   ws: dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) bytes. */
 dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_block,
-                                      const void* rms_gain, const void* w_qkv, const float* rope_table,
+                                      const void* rms_gain, const void* w_packed, const float* rope_table,
                                       int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
                                       size_t ws_bytes, void* stream);
 
@@ -191,7 +211,7 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
  * ordering) race on it.  Arguments, layouts and results are otherwise those
  * of dllm_block_qkv_rope_write. */
 dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* desc, const dllm_batch* batch,
-                                              const void* x_block, const void* rms_gain, const void* w_qkv,
+                                              const void* x_block, const void* rms_gain, const void* w_packed,
                                               const float* rope_table, int32_t rope_max_pos,
                                               const dllm_cache* cache, void* q_block, void* stream);
 

@@ -43,14 +43,26 @@ def _batch(batch=2, max_pages=12, M=64, R=1536, max_block=32, max_seq=768):
 
 def test_workspace_sizes(lib):
     d, b = _desc(), _batch()
-    # x^ rows, then (few rows: stream-K) fp32 partial tiles and arrival counters
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) >= 64 * 4096 * 2 + 96 * 4
+    # x^ rows (then, for small models with few weight tiles, stream-K partial tiles and counters)
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) >= 64 * 4096 * 2
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1536 * 4096 * 2
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == 0
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STATE_MERGE) == 0
     with pytest.raises(dllm.DllmError) as e:
         dllm.dllm_workspace_size(d, b, 17)
     assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+
+
+def test_packed_weight_size_and_host_checks(lib):
+    # 2 * ceil(D / 128) boxes of 128 x 64 per 128-row tile of the 3*H*d rows
+    assert dllm.dllm_qkv_weight_packed_bytes(_desc()) == 3 * 32 * 128 * 4096 * 2
+    assert dllm.dllm_qkv_weight_packed_bytes(_desc(d_model=4032)) == 3 * 32 * 128 * 4096 * 2
+    assert dllm.dllm_qkv_weight_packed_bytes(_desc(d_model=192, n_heads=2, head_dim=64)) == 384 * 4 * 64 * 2
+    fn = dllm.load().dllm_qkv_weight_pack
+    d = _desc()
+    n = dllm.dllm_qkv_weight_packed_bytes(d)
+    for w, p in ((0x10000, 0x10000 + n // 2), (0x10008, 0x10000000000), (None, 0x10000000000)):
+        assert fn(ctypes.byref(d), w, p, None) == dllm.DLLM_ERR_INVALID_ARGUMENT  # overlap, misaligned, NULL
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -96,6 +96,22 @@ def test_rmsnorm_operand_is_correctly_rounded():
     assert np.array_equal(got, want), f"{int((got != want).sum())} elements differ"
 
 
+def test_weight_pack_is_the_documented_permutation():
+    """Tile-packed weight: box (t, kb) of 128 rows x 64 columns stored
+    contiguously, 2*ceil(D/128) boxes per tile, zeros past d_model; checked
+    bit for bit against a host reordering (d_model % 128 == 64 included)."""
+    for D, H, d in ((192, 2, 64), (256, 4, 64), (512, 2, 128)):
+        desc = dllm.layer_desc(D, H, d, 1e4)
+        g = torch.Generator().manual_seed(D)
+        W = torch.randn(3 * H * d, D, generator=g).to(torch.bfloat16)
+        got = dllm.pack_qkv_weight(desc, W.cuda()).cpu().view(torch.int16).numpy()
+        kbp = 2 * ((D + 127) // 128)
+        Wp = np.zeros((3 * H * d, kbp * 64), dtype=np.int16)
+        Wp[:, :D] = W.view(torch.int16).numpy()
+        want = Wp.reshape(3 * H * d // 128, 128, kbp, 64).transpose(0, 2, 1, 3).reshape(-1)
+        assert np.array_equal(got, want), (D, H, d)
+
+
 def test_llada_single_blocks():
     cfg = make_config("llada_single")
     for k in (0, 3, cfg.num_blocks(0) - 1):
