@@ -14,10 +14,10 @@ Workload: the LLaDA-8B-shaped single layer (batch 1, d_model 4096, 32 heads
 x 128, RoPE theta 5e5, prompt 512, gen 256, block 32), synthetic seeded
 bf16 inputs and N(0, 0.02) weights.  Steps rotate over several independent
 layer instances (about 140 MB each), so no step finds its inputs in the
-129 MB L2.  The steps replay CUDA graphs (the block attention and the merge
-forked onto two streams); a sample of the steps carries CUDA events around
-the projection call on its stream, which give its live duration for the
-roofline.
+129 MB L2.  The steps replay CUDA graphs (three kernels a step: RMSNorm, the
+projection, and the block attention + FACache merge launch); a sample of the
+steps carries CUDA events around the projection call on its stream, which
+give its live duration for the roofline.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (sequences are independent units: weak scaling, no collective on the data
@@ -190,26 +190,27 @@ def run_ours(args, rank, ws, local):
         assert st.batch.error_bits() == 0, "device-side error during setup"
     M = inst[0][0].batch.total_block_rows
 
-    # CUDA graphs.  A round is one step of every instance (L steps, each
-    # forked: attention on the main stream, merge on the side stream), so
-    # consecutive kernels keep their programmatic-dependent-launch overlap.
+    # CUDA graphs.  A round is one step of every instance (L steps: the
+    # projection call, then the block attention and the FACache merge in one
+    # launch), so consecutive kernels keep their programmatic-dependent-launch
+    # overlap.
     # Every `sample_every`-th round replays per-instance pieces instead, with
     # CUDA events around the projection call on its stream: those give the
     # projection's live duration for the roofline, inside the timed region.
-    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for st, xb in inst:
-            st.step(xb, stream=stream, side_stream=side)
+            st.step(xb, stream=stream)
         stream.synchronize()
         g_round = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_round, stream=stream):
             for st, xb in inst:
-                st.step(xb, stream=stream, side_stream=side)
+                st.step(xb, stream=stream)
         g_step, g_qkv, g_rest = [], [], []
         for st, xb in inst:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                st.step(xb, stream=stream, side_stream=side)
+                st.step(xb, stream=stream)
             g_step.append(g)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -217,13 +218,7 @@ def run_ours(args, rank, ws, local):
             g_qkv.append(g)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                fork, join = torch.cuda.Event(), torch.cuda.Event()
-                fork.record(stream)
-                side.wait_event(fork)
-                st.attention(stream)
-                st.merge(side)
-                join.record(side)
-                stream.wait_event(join)
+                st.step_attention(stream)
             g_rest.append(g)
     torch.cuda.synchronize()
 
@@ -281,7 +276,7 @@ def run_ours(args, rank, ws, local):
     for i in range(min(W, 8)):
         st, _ = inst[i % L]
         x_dev[i % L].copy_(x_host[i % L], non_blocking=True)
-        st.step(x_dev[i % L], side_stream=side)
+        st.step(x_dev[i % L])
         o_host[i % L].copy_(st.o_full, non_blocking=True)
     torch.cuda.synchronize()
     _barrier(ws)
@@ -291,7 +286,7 @@ def run_ours(args, rank, ws, local):
         j = i % L
         st, _ = inst[j]
         x_dev[j].copy_(x_host[j], non_blocking=True)
-        st.step(x_dev[j], side_stream=side)
+        st.step(x_dev[j])
         o_host[j].copy_(st.o_full, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -334,7 +329,7 @@ def run_ours(args, rank, ws, local):
                      "algorithmic_bytes": qkv_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(Ke * M * ws / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 3 * K,
         "host_wall_s": t1 - t0,
     }
     cl = clocks.summary()

@@ -105,7 +105,25 @@ AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cac
   a.n_heads = d->n_heads;
   a.head_dim = d->head_dim;
   a.scale_log2 = softmax_scale(d) * 1.4426950408889634f;
+  a.part = nullptr;
+  a.counters = nullptr;
+  a.chunk_pages = 1;
+  a.n_chunks = 1;
   return a;
+}
+
+AttnPlan plan_of(const dllm_layer_desc* d, const dllm_batch* b, bool block, bool merge) {
+  return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, block, merge);
+}
+
+// Point the attention launch at its workspace (chunk partials, arrival counters).
+void bind_workspace(AttnArgs* a, const AttnPlan& plan, void* ws) {
+  a->chunk_pages = plan.chunk_pages;
+  a->n_chunks = plan.n_chunks;
+  if (plan.total_bytes == 0) return;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a->part = reinterpret_cast<float*>(base);
+  a->counters = reinterpret_cast<int32_t*>(base + plan.counter_offset);
 }
 
 QkvArgs qkv_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache* c, const float* rope,
@@ -175,6 +193,11 @@ dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* b
                    : 0;
       return DLLM_OK;
     case DLLM_OP_BLOCK_ATTENTION:
+      *bytes = batch->batch > 0 && batch->total_block_rows > 0 ? plan_of(desc, batch, true, false).total_bytes : 0;
+      return DLLM_OK;
+    case DLLM_OP_STEP_ATTENTION:
+      *bytes = batch->batch > 0 && batch->total_block_rows > 0 ? plan_of(desc, batch, true, true).total_bytes : 0;
+      return DLLM_OK;
     case DLLM_OP_STATE_MERGE:
       *bytes = 0;
       return DLLM_OK;
@@ -267,40 +290,48 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
   return DLLM_OK;
 }
 
-dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
-                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
-                                 void* stream) {
-  (void)ws;
-  (void)ws_bytes;
+namespace {
+// The common part of the three attention calls: validate, bind the workspace, launch.
+dllm_status attention_call(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                           const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes, void* stream,
+                           bool block, bool merge) {
   DLLM_TRY(check_desc(desc));
   DLLM_TRY(check_batch(batch));
-  if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
-  DLLM_TRY(check_cache(cache, desc, false, false));
-  if (!aligned(q_block, 16) || !aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
+  if (block && batch->total_block_rows == 0) block = false;
+  if (!block && !merge) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, merge, merge));
+  if (block && !aligned(q_block, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
   if (lse != nullptr && !aligned(lse, 4)) return DLLM_ERR_INVALID_ARGUMENT;
+  const AttnPlan plan = plan_of(desc, batch, block, merge);
+  if (ws_bytes < plan.total_bytes) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (plan.total_bytes > 0 && !aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
   AttnArgs aa = attn_args(desc, batch, cache);
   aa.q_block = q_block;
   aa.o_full = o_full;
   aa.lse = lse;
-  DLLM_CUDA_TRY(launch_block_attention(aa, device_sms(), static_cast<cudaStream_t>(stream)));
+  bind_workspace(&aa, plan, ws);
+  DLLM_CUDA_TRY(launch_step_attention(aa, plan, static_cast<cudaStream_t>(stream)));
   return DLLM_OK;
+}
+}  // namespace
+
+dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return attention_call(desc, batch, q_block, cache, o_full, lse, ws, ws_bytes, stream, true, false);
 }
 
 dllm_status dllm_state_merge(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_cache* cache,
                              void* o_full, float* lse, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
-  DLLM_TRY(check_desc(desc));
-  DLLM_TRY(check_batch(batch));
-  if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
-  DLLM_TRY(check_cache(cache, desc, true, true));
-  if (!aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
-  if (lse != nullptr && !aligned(lse, 4)) return DLLM_ERR_INVALID_ARGUMENT;
-  AttnArgs aa = attn_args(desc, batch, cache);
-  aa.o_full = o_full;
-  aa.lse = lse;
-  DLLM_CUDA_TRY(launch_state_merge(aa, static_cast<cudaStream_t>(stream)));
-  return DLLM_OK;
+  return attention_call(desc, batch, nullptr, cache, o_full, lse, ws, ws_bytes, stream, false, true);
+}
+
+dllm_status dllm_step_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                                const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
+                                void* stream) {
+  return attention_call(desc, batch, q_block, cache, o_full, lse, ws, ws_bytes, stream, true, true);
 }
 
 const char* dllm_status_string(dllm_status status) {

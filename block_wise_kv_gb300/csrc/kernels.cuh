@@ -88,7 +88,22 @@ struct AttnArgs {
   int32_t n_heads;
   int32_t head_dim;
   float scale_log2;     // softmax_scale * log2(e)
+  // block attention split into chunks of pages (workspace, see AttnPlan)
+  float* part;          // fp32 partial states [batch][H][n_chunks][64][head_dim + 4]
+  int32_t* counters;    // [batch][H] chunk arrivals; zero between calls
+  int32_t chunk_pages;
+  int32_t n_chunks;
 };
+
+// Work of one attention launch: n_block_items block-attention chunks
+// (sequence, head, chunk of chunk_pages pages) followed by n_merge_items
+// FACache merges (sequence, head, query page).
+struct AttnPlan {
+  int chunk_pages, n_chunks;
+  long long n_block_items, n_merge_items;
+  size_t part_bytes, counter_offset, total_bytes;  // workspace (0 when no chunk split is needed)
+};
+AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, bool block, bool merge);
 
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
 // Each launcher encodes the TMA tensor maps it needs from the raw pointers.
@@ -99,8 +114,9 @@ cudaError_t launch_zero_tails(const BatchArgs& bt, void* k_pool, void* v_pool, v
                               int head_dim, cudaStream_t stream);
 cudaError_t launch_qkv_gemm(const void* w_packed, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
                             cudaStream_t stream);
-cudaError_t launch_block_attention(const AttnArgs& a, int num_sms, cudaStream_t stream);
+// The block attention (LaCache Eq. (2)-(6) over all keys of each block row)
+// and/or the FACache merge of every invariant row, as planned by attn_plan.
+cudaError_t launch_step_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_state_build(const AttnArgs& a, cudaStream_t stream);
-cudaError_t launch_state_merge(const AttnArgs& a, cudaStream_t stream);
 
 }  // namespace dllm

@@ -37,13 +37,14 @@ DLLM_OP_CACHE_BUILD = 0
 DLLM_OP_BLOCK_QKV_ROPE_WRITE = 1
 DLLM_OP_BLOCK_ATTENTION = 2
 DLLM_OP_STATE_MERGE = 3
+DLLM_OP_STEP_ATTENTION = 4
 
 PAGE = 64
 
 # Every symbol include/dllm.h declares.
 EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_qkv_weight_packed_bytes", "dllm_qkv_weight_pack",
            "dllm_cache_build", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
-           "dllm_block_attention", "dllm_state_merge", "dllm_status_string")
+           "dllm_block_attention", "dllm_state_merge", "dllm_step_attention", "dllm_status_string")
 
 
 class DllmError(RuntimeError):
@@ -101,6 +102,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                       vp],
                 "dllm_block_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
                 "dllm_state_merge": [P(LayerDescC), P(BatchC), P(CacheC), vp, vp, vp, sz, vp],
+                "dllm_step_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
             }
             for name, argt in sig.items():
                 fn = getattr(lib, name)
@@ -208,6 +210,12 @@ def dllm_state_merge(desc, batch, cache, o_full, lse=None, ws=None, stream=None)
         _nbytes(ws), _stream(stream)))
 
 
+def dllm_step_attention(desc, batch, q_block, cache, o_full, lse=None, ws=None, stream=None):
+    _check("dllm_step_attention", load().dllm_step_attention(
+        ctypes.byref(desc), ctypes.byref(batch), _ptr(q_block), ctypes.byref(cache), _ptr(o_full), _ptr(lse),
+        _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
 # ---------------------------------------------------- memory / structs ----
 def layer_desc(d_model: int, n_heads: int, head_dim: int, rope_theta: float, rms_eps: float = 1e-5,
                softmax_scale: float = 0.0) -> LayerDescC:
@@ -267,8 +275,9 @@ class PagedCache:
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """Caller-owned scratch of at least nbytes (256-byte aligned by torch's allocator)."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """Caller-owned scratch of at least nbytes (256-byte aligned by torch's
+    allocator), zero-filled as the attention calls' arrival counters require."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def gather_rows(pool: torch.Tensor, block_table: np.ndarray, b: int, n: int) -> torch.Tensor:

@@ -40,6 +40,10 @@ class LayerStep:
                                        device)
         self.ws_step = dllm.workspace(
             dllm.dllm_workspace_size(self.desc, self.batch.c, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE), device)
+        # the attention calls of a step run in order, so one workspace serves all three
+        self.ws_attn = dllm.workspace(max(
+            dllm.dllm_workspace_size(self.desc, self.batch.c, op)
+            for op in (dllm.DLLM_OP_BLOCK_ATTENTION, dllm.DLLM_OP_STATE_MERGE, dllm.DLLM_OP_STEP_ATTENTION)), device)
         H, d = cfg.n_heads, cfg.head_dim
         self.q_block = torch.zeros(self.batch.total_block_rows, H, d, dtype=torch.bfloat16, device=device)
         self.o_full = torch.zeros(self.batch.total_seq_rows, H, d, dtype=torch.bfloat16, device=device)
@@ -56,33 +60,26 @@ class LayerStep:
 
     def attention(self, stream=None, lse: bool = True) -> None:
         dllm.dllm_block_attention(self.desc, self.batch.c, self.q_block, self.cache.c, self.o_full,
-                                  self.lse if lse else None, None, stream)
+                                  self.lse if lse else None, self.ws_attn, stream)
 
     def merge(self, stream=None, lse: bool = True) -> None:
-        dllm.dllm_state_merge(self.desc, self.batch.c, self.cache.c, self.o_full, self.lse if lse else None, None,
-                              stream)
+        dllm.dllm_state_merge(self.desc, self.batch.c, self.cache.c, self.o_full, self.lse if lse else None,
+                              self.ws_attn, stream)
 
-    def step(self, x_block: torch.Tensor, stream=None, lse: bool = True, side_stream=None) -> None:
-        """One inner denoising step of this layer: fused projection, block
-        attention, and the FACache merge for the invariant rows.
+    def step_attention(self, stream=None, lse: bool = True) -> None:
+        dllm.dllm_step_attention(self.desc, self.batch.c, self.q_block, self.cache.c, self.o_full,
+                                 self.lse if lse else None, self.ws_attn, stream)
 
-        The block attention and the merge read the same cache and write
-        disjoint rows of o_full / lse, so with `side_stream` the merge runs on
-        it concurrently with the attention (fork after the projection, join
-        before returning); both streams may be under graph capture."""
+    def step(self, x_block: torch.Tensor, stream=None, lse: bool = True, split: bool = False) -> None:
+        """One inner denoising step of this layer: fused projection, then the
+        block attention and the FACache merge for the invariant rows in one
+        launch (`split`: as the two separate calls instead)."""
         self.qkv(x_block, stream)
-        if side_stream is None:
+        if split:
             self.attention(stream, lse)
             self.merge(stream, lse)
-            return
-        main = stream if stream is not None else torch.cuda.current_stream()
-        fork, join = torch.cuda.Event(), torch.cuda.Event()
-        fork.record(main)
-        side_stream.wait_event(fork)
-        self.attention(main, lse)
-        self.merge(side_stream, lse)
-        join.record(side_stream)
-        main.wait_event(join)
+        else:
+            self.step_attention(stream, lse)
 
     # ---------------------------------------------------------- inspection
     def seq_slice(self, b: int) -> slice:

@@ -12,6 +12,7 @@
  *   dllm_state_merge           output rows of the invariant set U (prefix and
  *                              suffix): cached online-softmax state (m, l, O~)
  *                              merged exactly with the fresh block keys.
+ *   dllm_step_attention        both of the previous two in one launch.
  *
  * and, once per block boundary, dllm_cache_build, which fills the paged cache
  * for all rows and the per-row state (m, l, O~) of every row of U over the
@@ -138,10 +139,15 @@ typedef struct dllm_batch {
 #define DLLM_OP_BLOCK_QKV_ROPE_WRITE 1
 #define DLLM_OP_BLOCK_ATTENTION 2
 #define DLLM_OP_STATE_MERGE 3
+#define DLLM_OP_STEP_ATTENTION 4
 
 /* Bytes of device workspace `op` needs for this layer and batch (0 if none).
  * The workspace is scratch owned by the caller, 256-byte aligned, and may be
- * reused once the call's work on its stream has completed. */
+ * reused once the call's work on its stream has completed.  The workspace of
+ * DLLM_OP_BLOCK_ATTENTION and DLLM_OP_STEP_ATTENTION holds arrival counters:
+ * it must be zero-filled before its first use, and every call leaves it
+ * zero-filled (after a call that reported DLLM_DEVERR_TIMEOUT, fill it with
+ * zeros again). */
 dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t op, size_t* bytes);
 
 /* Fill the RoPE table (device fp32 [max_pos][head_dim/2][2]) with
@@ -222,7 +228,11 @@ dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* desc, const
  * o_full row cu_seq[b] + s_b + i, and L = m + ln l to lse (nullable) at the
  * same row.  q_block as written by dllm_block_qkv_rope_write; the pools as
  * written by dllm_cache_build and this step's dllm_block_qkv_rope_write.
- *   ws: dllm_workspace_size(DLLM_OP_BLOCK_ATTENTION) bytes (currently 0). */
+ * The keys of a (sequence, head) are split into chunks of pages whose
+ * partial states (m, l, O~) meet in ws and are merged exactly (the
+ * Eq. (2)-(6) merge applied to states) by the chunk that finishes last.
+ *   ws: dllm_workspace_size(DLLM_OP_BLOCK_ATTENTION) bytes (zero-filled before
+ *   first use, see dllm_workspace_size). */
 dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
                                  const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
                                  void* stream);
@@ -239,6 +249,17 @@ dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* 
  *   ws: dllm_workspace_size(DLLM_OP_STATE_MERGE) bytes (currently 0). */
 dllm_status dllm_state_merge(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_cache* cache,
                              void* o_full, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Inner step, parts 2 and 3 in one launch: the results of
+ * dllm_block_attention followed by dllm_state_merge (both write disjoint rows
+ * of o_full and lse), with the merge work filling the GPU while the block
+ * attention finishes (no counterpart in the pages: a scheduling choice of
+ * this library).
+ *   ws: dllm_workspace_size(DLLM_OP_STEP_ATTENTION) bytes (zero-filled before
+ *   first use, see dllm_workspace_size). */
+dllm_status dllm_step_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
+                                const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* dllm_status_string(dllm_status status);

@@ -46,8 +46,13 @@ def test_workspace_sizes(lib):
     # x^ rows (then, for small models with few weight tiles, stream-K partial tiles and counters)
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) >= 64 * 4096 * 2
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1536 * 4096 * 2
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == 0
+    # block attention: 12 pages per sequence in 4 chunks of 3; fp32 partial states [2][32][4][64][128 + 4]
+    part = 2 * 32 * 4 * 64 * 132 * 4
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == part + 256
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STEP_ATTENTION) == part + 256
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STATE_MERGE) == 0
+    # two pages per sequence: a single chunk, no workspace
+    assert dllm.dllm_workspace_size(d, _batch(max_seq=128, R=256), dllm.DLLM_OP_STEP_ATTENTION) == 0
     with pytest.raises(dllm.DllmError) as e:
         dllm.dllm_workspace_size(d, b, 17)
     assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
