@@ -107,19 +107,15 @@ AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cac
   a.scale_log2 = softmax_scale(d) * 1.4426950408889634f;
   a.part = nullptr;
   a.counters = nullptr;
-  a.chunk_pages = 1;
-  a.n_chunks = 1;
   return a;
 }
 
 AttnPlan plan_of(const dllm_layer_desc* d, const dllm_batch* b, bool block, bool merge) {
-  return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, block, merge);
+  return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, b->max_block_len, device_sms(), block, merge);
 }
 
-// Point the attention launch at its workspace (chunk partials, arrival counters).
+// Point the attention launch at its workspace (partial states, arrival counters).
 void bind_workspace(AttnArgs* a, const AttnPlan& plan, void* ws) {
-  a->chunk_pages = plan.chunk_pages;
-  a->n_chunks = plan.n_chunks;
   if (plan.total_bytes == 0) return;
   uint8_t* base = static_cast<uint8_t*>(ws);
   a->part = reinterpret_cast<float*>(base);
@@ -300,6 +296,7 @@ dllm_status attention_call(const dllm_layer_desc* desc, const dllm_batch* batch,
   if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
   if (block && batch->total_block_rows == 0) block = false;
   if (!block && !merge) return DLLM_OK;
+  if (!attn_batch_supported(batch->batch)) return DLLM_ERR_UNSUPPORTED;
   DLLM_TRY(check_cache(cache, desc, merge, merge));
   if (block && !aligned(q_block, 16)) return DLLM_ERR_INVALID_ARGUMENT;
   if (!aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;

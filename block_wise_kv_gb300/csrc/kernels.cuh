@@ -88,22 +88,22 @@ struct AttnArgs {
   int32_t n_heads;
   int32_t head_dim;
   float scale_log2;     // softmax_scale * log2(e)
-  // block attention split into chunks of pages (workspace, see AttnPlan)
-  float* part;          // fp32 partial states [batch][H][n_chunks][64][head_dim + 4]
-  int32_t* counters;    // [batch][H] chunk arrivals; zero between calls
-  int32_t chunk_pages;
-  int32_t n_chunks;
+  // block part of (b, h) split over CTAs: partial states and arrival counters in the workspace
+  float* part;          // fp32 [grid][2][part_rows][head_dim + 4]
+  int32_t* counters;    // [batch][H]; zero between calls
 };
 
-// Work of one attention launch: n_block_items block-attention chunks
-// (sequence, head, chunk of chunk_pages pages) followed by n_merge_items
-// FACache merges (sequence, head, query page).
+// One attention launch: a persistent grid of `grid` CTAs walking the
+// (sequence, head, page) units; block part and/or merge part per unit.
 struct AttnPlan {
-  int chunk_pages, n_chunks;
-  long long n_block_items, n_merge_items;
-  size_t part_bytes, counter_offset, total_bytes;  // workspace (0 when no chunk split is needed)
+  int grid;                           // CTAs (one per SM)
+  int part_rows;                      // rows of a partial-state slot (max_block_len)
+  long long n_block_items, n_merge_items;  // unit bounds (0: that part is off)
+  size_t part_bytes, counter_offset, total_bytes;  // workspace (0 without the block part)
 };
-AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, bool block, bool merge);
+AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int num_sms, bool block,
+                   bool merge);
+bool attn_batch_supported(int batch);
 
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
 // Each launcher encodes the TMA tensor maps it needs from the raw pointers.

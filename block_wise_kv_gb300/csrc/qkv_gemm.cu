@@ -151,11 +151,7 @@ struct UnitWalk {
   }
 };
 
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
+
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -396,40 +392,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- a segment (one weight tile's k-range of this CTA) is complete
       const int tile = w.tile;
       if (!(w.seg_kb0() == 0 && w.kb == nkb - 1)) {
-        // Stream-K fixup: the last contributor to arrive finishes the tile
-        // from the others' fp32 partials.  A contributor that finds every
-        // other one already arrived skips publishing its own partial.
+        // Stream-K fixup: every contributor publishes its fp32 partial; the
+        // last to arrive sums all of them in slot order (its own too, as
+        // written), so the rounding does not depend on the arrival order.
         const int c_first = sk_cta_of(static_cast<long long>(tile) * nkb, U, G);
         const int c_last = sk_cta_of(static_cast<long long>(tile) * nkb + nkb - 1, U, G);
         const int n_other = c_last - c_first;
         const int slot = static_cast<int>(blockIdx.x) - c_first;
         float* slots = a.partials + static_cast<size_t>(tile) * a.max_contrib * kTileM * BN;
-        if (threadIdx.x == 64) last_sh = ld_acquire_gpu(a.counters + tile) == n_other ? 1 : 0;
-        named_barrier(1, kAccThreads);
-        if (!last_sh) {
-          float* mine = slots + static_cast<size_t>(slot) * kTileM * BN + static_cast<size_t>(row) * BN;
+        float* mine = slots + static_cast<size_t>(slot) * kTileM * BN + static_cast<size_t>(row) * BN;
 #pragma unroll
-          for (int c = 0; c < BN; c += 4)
-            *reinterpret_cast<float4*>(mine + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-          named_barrier(1, kAccThreads);  // the CTA's partial rows are written ...
-          if (threadIdx.x == 64) {
-            __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
-            last_sh = atomicAdd(a.counters + tile, 1) == n_other ? 1 : 0;
-          }
-          named_barrier(1, kAccThreads);
-          if (!last_sh) {
-#pragma unroll
-            for (int c = 0; c < BN; ++c) acc[c] = 0.f;
-            continue;
-          }
+        for (int c = 0; c < BN; c += 4)
+          *reinterpret_cast<float4*>(mine + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+        named_barrier(1, kAccThreads);  // the CTA's partial rows are written ...
+        if (threadIdx.x == 64) {
+          __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
+          last_sh = atomicAdd(a.counters + tile, 1) == n_other ? 1 : 0;
         }
+        named_barrier(1, kAccThreads);
+#pragma unroll
+        for (int c = 0; c < BN; ++c) acc[c] = 0.f;
+        if (!last_sh) continue;
         __threadfence();
         for (int sl = 0; sl <= n_other; ++sl) {
-          if (sl == slot) continue;
-          const float* other = slots + static_cast<size_t>(sl) * kTileM * BN + static_cast<size_t>(row) * BN;
+          const float* part = slots + static_cast<size_t>(sl) * kTileM * BN + static_cast<size_t>(row) * BN;
 #pragma unroll
           for (int c = 0; c < BN; c += 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(other + c));
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(part + c));
             acc[c] += v.x;
             acc[c + 1] += v.y;
             acc[c + 2] += v.z;

@@ -46,13 +46,18 @@ def test_workspace_sizes(lib):
     # x^ rows (then, for small models with few weight tiles, stream-K partial tiles and counters)
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) >= 64 * 4096 * 2
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1536 * 4096 * 2
-    # block attention: 12 pages per sequence in 4 chunks of 3; fp32 partial states [2][32][4][64][128 + 4]
-    part = 2 * 32 * 4 * 64 * 132 * 4
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == part + 256
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STEP_ATTENTION) == part + 256
+    # block part: two fp32 partial-state slots [max_block_len][128 + 4] per CTA (one CTA per SM, at most
+    # one per unit), then one arrival counter per (sequence, head)
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    part = sms * 2 * 32 * 132 * 4
+    want = (part + 255) // 256 * 256 + 256
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == want
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STEP_ATTENTION) == want
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STATE_MERGE) == 0
-    # two pages per sequence: a single chunk, no workspace
-    assert dllm.dllm_workspace_size(d, _batch(max_seq=128, R=256), dllm.DLLM_OP_STEP_ATTENTION) == 0
+    # fewer units than SMs: one CTA per unit (1 sequence x 32 heads x 2 pages = 64 units)
+    small = _batch(batch=1, max_seq=128, R=128, M=32)
+    assert dllm.dllm_workspace_size(d, small, dllm.DLLM_OP_STEP_ATTENTION) == 64 * 2 * 32 * 132 * 4 + 256
     with pytest.raises(dllm.DllmError) as e:
         dllm.dllm_workspace_size(d, b, 17)
     assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
