@@ -164,6 +164,20 @@ def step_bytes_flops(cfg, st):
     return dict(qkv=(qkv_bytes, qkv_flops), attention=(att_bytes, att_flops), merge=(mrg_bytes, mrg_flops))
 
 
+def describe(cfg) -> str:
+    """The workload, named by what it is with its sizes."""
+    N = np.array([cfg.seq_len(b) for b in range(cfg.batch)], dtype=np.int64)
+    M = int(sum(cfg.block))
+    seqs = f"batch {cfg.batch}"
+    if len(set(cfg.t_prefix)) == 1 and len(set(cfg.gen_len)) == 1 and len(set(cfg.block)) == 1:
+        seqs += f", prompt {cfg.t_prefix[0]}, gen {cfg.gen_len[0]}, block {cfg.block[0]}"
+    else:
+        seqs += f", prompt {min(cfg.t_prefix)}..{max(cfg.t_prefix)}, gen {sorted(set(cfg.gen_len))}, " \
+                f"block {sorted(set(cfg.block))}"
+    return (f"{cfg.name}: 1 layer step, d_model {cfg.d_model}, {cfg.n_heads}x{cfg.head_dim} heads, {seqs} "
+            f"(M={M} block rows, N={int(N.sum())} rows)")
+
+
 def run_ours(args, rank, ws, local):
     from block_wise_kv_gb300 import build, dllm
     from block_wise_kv_gb300.inputs import Workload, make_config
@@ -206,7 +220,7 @@ def run_ours(args, rank, ws, local):
         with torch.cuda.graph(g_round, stream=stream):
             for st, xb in inst:
                 st.step(xb, stream=stream)
-        g_step, g_qkv, g_rest = [], [], []
+        g_step, g_qkv, g_rest = [], [], []  # one step; the projection call; the attention call
         for st, xb in inst:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -238,11 +252,12 @@ def run_ours(args, rank, ws, local):
         for r in range(n_rounds):
             if r % sample_every == sample_every - 1:
                 for j in range(L):
-                    e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                     e[0].record(stream)
                     g_qkv[j].replay()
                     e[1].record(stream)
                     g_rest[j].replay()
+                    e[2].record(stream)
                     qkv_ev.append(e)
             else:
                 g_round.replay()
@@ -257,13 +272,16 @@ def run_ours(args, rank, ws, local):
     if not qkv_ev:  # too few rounds to sample: time the projection alone after the region
         with torch.cuda.stream(stream):
             for j in range(L):
-                e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 e[0].record(stream)
                 g_qkv[j].replay()
                 e[1].record(stream)
+                g_rest[j].replay()
+                e[2].record(stream)
                 qkv_ev.append(e)
         torch.cuda.synchronize()
-    qkv_ms = sum(a.elapsed_time(b) for a, b in qkv_ev) / len(qkv_ev)
+    qkv_ms = sum(e[0].elapsed_time(e[1]) for e in qkv_ev) / len(qkv_ev)
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in qkv_ev) / len(qkv_ev)
     total_ms = _max_over_ranks(total_ms, ws)
     for st, _ in inst:
         assert st.batch.error_bits() == 0, "device-side error during the timed steps"
@@ -294,6 +312,21 @@ def run_ours(args, rank, ws, local):
     h2d = x_host[0].numel() * x_host[0].element_size()
     d2h = o_host[0].numel() * o_host[0].element_size()
 
+    # the block boundary (cache build: projection of every row, FACache state
+    # over U x U), timed apart: once per block, amortised over its inner steps
+    x_full = [full_rows_of(wl, layer, 0, blocks).to(dev) for layer in range(L)]
+    for j in range(L):
+        inst[j][0].boundary(x_full[j])
+    torch.cuda.synchronize()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nb = 2 * L
+    b0.record()
+    for i in range(nb):
+        inst[i % L][0].boundary(x_full[i % L])
+    b1.record()
+    torch.cuda.synchronize()
+    build_ms = b0.elapsed_time(b1) / nb
+
     if rank != 0:
         return None
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
@@ -315,13 +348,16 @@ def run_ours(args, rank, ws, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: 1 layer, batch 1, d_model 4096, 32x128 heads, prompt 512, gen 256, "
-                               "block 32 (M=32, N=768)",
+        "config": {"workload": describe(cfg),
                    "l2": f"inputs larger than L2: {L} rotating layer instances (~140 MB each)",
                    "graphs": f"one CUDA graph per round of {L} steps; every {sample_every}th round replayed "
                              "per call with events around the projection",
                    "parallelism": f"replicas x{ws} (sequences are independent units)"},
         "qkv_rope_write_us": round(qkv_ms * 1e3, 2),
+        "step_attention_us": round(attn_ms * 1e3, 2),
+        "step_attention_gbs": round((bf["attention"][0] + bf["merge"][0]) / (attn_ms * 1e-3) / 1e9, 1),
+        "cache_build_us": {"per_boundary": round(build_ms * 1e3, 1),
+                           "per_inner_step": round(build_ms * 1e3 / cfg.steps_per_block, 2)},
         "roofline": {"kernel": "dllm_block_qkv_rope_write (RMSNorm + tcgen05 QKV GEMM with RoPE/paged-write "
                                "epilogue)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
@@ -370,7 +406,7 @@ def cpu_baseline(cfg, seconds: float):
     from block_wise_kv_gb300.inputs import Workload
 
     wl = Workload(cfg)
-    M = sum(cfg.block)
+    M = cfg.block[0]  # the sample is sequence 0: its block rows per step
     _oracle_sample(cfg, wl, [0], 1)  # warm: builds/loads the library, generates the inputs
     n, t = 0, 0.0
     while t < seconds and n < cfg.n_heads:
@@ -380,8 +416,9 @@ def cpu_baseline(cfg, seconds: float):
         n += 1
     per_step = t / n * cfg.n_heads
     return {"value": round(M / per_step, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"full-recompute layer step (fp64) for {n} of {cfg.n_heads} heads of {WORKLOAD}, "
-                      f"{t:.1f} s, scaled to all heads"}
+            "sample": f"full-recompute layer step (fp64) of sequence 0 for {n} of {cfg.n_heads} heads of "
+                      f"{cfg.name}, {t:.1f} s, scaled to all heads" + ("" if cfg.batch == 1 else
+                                                                        " (sequence 0 only)")}
 
 
 def run_reference(args, rank, ws):
@@ -392,7 +429,7 @@ def run_reference(args, rank, ws):
 
     cfg = make_config(args.config)
     wl = Workload(cfg)
-    M = sum(cfg.block)
+    M = cfg.block[0]  # each step samples sequence 0: its block rows per step
     _oracle_inputs(cfg, wl, 1)
     K, W = args.steps_ref, args.warmup_ref
     for i in range(W):
@@ -403,12 +440,12 @@ def run_reference(args, rank, ws):
     t = time.perf_counter() - t0
     per_step = t / K * cfg.n_heads
     value = M / per_step
-    sample = f"each step: full-recompute layer step (fp64) for one head of {cfg.n_heads}, scaled to all heads"
+    sample = (f"each step: full-recompute layer step (fp64) of sequence 0 for one head of {cfg.n_heads}, scaled "
+              "to all heads" + ("" if cfg.batch == 1 else "; rate of one sequence"))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: 1 layer, batch 1, d_model 4096, 32x128 heads, prompt 512, gen "
-                                   "256, block 32 (M=32, N=768)"},
+            "config": {"workload": describe(cfg)},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
