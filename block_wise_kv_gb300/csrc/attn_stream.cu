@@ -136,6 +136,7 @@ struct BlockSplit {
     KS = RG <= 2 ? 4 : 2;
   }
   __device__ __forceinline__ bool active(int warp) const { return warp < RG * KS; }
+  __device__ __forceinline__ int states() const { return KS; }  // per row group
 };
 
 template <int D>
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       ++nk;
       if (!w.seg_end()) continue;
 
-      // ---- (b, h) segment complete on this CTA: combine the key slices in shared memory
+      // ---- (b, h) segment complete on this CTA: combine the KS states of each row in shared memory
       if (active) {
         st.reduce_l();
         const int slot0 = ks * sp.RG * 16 + rg * 16 + g, slot1 = slot0 + 8;
@@ -298,11 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       for (int item = threadIdx.x; item < w.sm.bb * C4; item += 256) {
         const int i = item / C4, col = (item % C4) * 4;
         float M = neg_inf();
-        for (int q = 0; q < sp.KS; ++q) M = fmaxf(M, S.comb_m[q * sp.RG * 16 + i]);
+        for (int q = 0; q < sp.states(); ++q) M = fmaxf(M, S.comb_m[q * sp.RG * 16 + i]);
         const float Mu = M == neg_inf() ? 0.f : M;
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < sp.KS; ++q) {
+        for (int q = 0; q < sp.states(); ++q) {
           const int slot = q * sp.RG * 16 + i;
           const float wgt = fast_exp2(S.comb_m[slot] - Mu);
           L += wgt * S.comb_l[slot];
@@ -570,8 +571,11 @@ AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int ma
   const int g = static_cast<int>(units < num_sms ? (units < 1 ? 1 : units) : num_sms);
   p.part_rows = max_block_len < 1 ? 1 : max_block_len;
   if (block && merge) {
-    // half the CTAs each: a merge CTA runs two pages at a time, a block CTA one
-    p.n_block_ctas = g / 2 < 1 ? 1 : g / 2;
+    // one block-role CTA per (b, h) (so that no (b, h) needs a cross-CTA merge)
+    // while that is at most half of the CTAs; the rest take the merge role
+    const long long bh = static_cast<long long>(batch) * n_heads;
+    const int half = g / 2 < 1 ? 1 : g / 2;
+    p.n_block_ctas = bh < half ? static_cast<int>(bh) : half;
     p.n_merge_ctas = g - p.n_block_ctas < 1 ? 1 : g - p.n_block_ctas;
   } else {
     p.n_block_ctas = block ? g : 0;
