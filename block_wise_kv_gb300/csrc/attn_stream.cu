@@ -45,37 +45,36 @@ template <int D>
 struct StreamCfg {
   static constexpr int TB = tile_bytes<D>();  // bf16 64 x D
   static constexpr int OB = 64 * D * 4;       // fp32 O~ page
-  static constexpr int OS = D + 8;            // padded fp32 row of the per-warp partial states
-  // block role: K/V ring | block queries | per-warp partial states
+  // block role: K/V ring | 128-row query tile | two 128 x 64 score-probability tiles
   static constexpr int kKStages = 4;
   static constexpr int KStage = 2 * TB;
   static constexpr int off_qb = kKStages * KStage;
-  static constexpr int off_comb = off_qb + TB;
-  static constexpr int kCombBytes = 128 * OS * 4;  // 128 (slice, row) states; later the contributors' slots
-  static constexpr int kBlockSmem = off_comb + kCombBytes;
+  static constexpr int QB = 2 * TB;  // 128 rows x D
+  static constexpr int off_p = off_qb + QB;
+  static constexpr int PB = 128 * 128;  // 128 rows x 64 keys bf16
+  static constexpr int kBlockSmem = off_p + 2 * PB;
   // merge role: query page | O~ page | m | l ring, then the gathered block keys / values
-  static constexpr int kMStages = 3;
+  static constexpr int kMStages = 2;
   static constexpr int MStage = TB + OB + 1024;
   static constexpr int off_kc = kMStages * MStage;
   static constexpr int off_vc = off_kc + TB;
   static constexpr int kMergeSmem = off_vc + TB;
   static constexpr int kSmem = (kBlockSmem > kMergeSmem ? kBlockSmem : kMergeSmem) + 1024;  // + alignment slack
-  static constexpr int PS = D + 4;  // workspace partial row: D accumulators, then (m, l)
+  // tensor memory of the block role: O (D columns) then two score buffers of 64 columns
+  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 256;
+  static constexpr uint32_t kTmemS = D;
 };
 
 struct Shared {
-  uint64_t full[4], empty[4], qfull, qempty, cbar;
+  uint64_t full[4], empty[4], qfull, qempty;
+  uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
+  uint32_t tmem_base;
   int abort_flag;
-  int last_flag;
-  float comb_m[8 * 16], comb_l[8 * 16];  // per-warp row states of the block role
-  int n_seq_units[kMaxBatch];            // H * pages of sequence b (0: invalid metadata)
-  int cu[kMaxBatch + 1];                 // unit prefix
+  int n_seq_units[kMaxBatch];  // H * pages of sequence b (0: invalid metadata)
+  int cu[kMaxBatch + 1];       // unit prefix
 };
 
 __device__ __forceinline__ long long split_begin(long long c, long long U, long long G) { return c * U / G; }
-__device__ __forceinline__ int split_of(long long u, long long U, long long G) {
-  return static_cast<int>(((u + 1) * G - 1) / U);
-}
 
 // Walk over the units [u, u1).
 struct UWalk {
@@ -101,8 +100,6 @@ struct UWalk {
   }
   __device__ __forceinline__ bool valid() const { return u < u1; }
   __device__ __forceinline__ bool seg_start() const { return p == first_p; }
-  __device__ __forceinline__ bool seg_end() const { return u + 1 == u1 || p == np - 1; }
-  __device__ __forceinline__ bool seg_whole() const { return first_p == 0 && p == np - 1; }
   __device__ __forceinline__ bool has_u_rows() const {
     const int r_lo = p * kPage, r_hi = min(sm.nb, r_lo + kPage);
     return r_lo < sm.sb || r_hi > sm.sb + sm.bb;
@@ -127,26 +124,285 @@ __device__ __forceinline__ void wait_or_abort(Shared& S, uint64_t* bar, uint32_t
   }
 }
 
-// Block-role split of a (b, h) of bb queries over the 8 compute warps:
-// RG 16-row groups x KS key slices of NK = 64 / KS keys (NK a multiple of 16).
-struct BlockSplit {
-  int RG, KS;
-  __device__ __forceinline__ explicit BlockSplit(int bb) {
-    RG = (bb + 15) / 16;
-    KS = RG <= 2 ? 4 : 2;
+
+// ---------------------------------------------------------------------------
+// Block role on the 5th-generation tensor cores.  For each (b, h) the CTA
+// owns: the block queries (<= 64 rows, padded to the 128-row MMA tile) stay in
+// shared memory; per 64-key page, warp 4 issues S = Q K^T (M = 128, N = 64,
+// into one of two TMEM score buffers) and, once the softmax warps have written
+// P for it, O += P V (M = 128, N = D, V as an MN-major operand) into TMEM, so
+// the scores of page p + 1 are computed while page p's softmax runs.  Warps
+// 0-3 own one query row per thread (TMEM lane): exact row max over the page,
+// P = 2^(S - m_ref) with a reference max m_ref that is raised (and O, l
+// rescaled) only when a page's max exceeds it by more than 2^8 (every P stays
+// <= 2^8; the result is exact for any reference), running sum l in fp32, and
+// at the end of the (b, h) O / l and L = m_ref + log2 l.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CUtensorMap& tm_qb,
+                                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
+                                              long long c, long long G) {
+  using C = StreamCfg<D>;
+  constexpr int TB = C::TB;
+  constexpr float kRescale = 8.f;  // log2 units
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BatchArgs& bt = a.bt;
+  const int H = a.n_heads;
+  const long long BH = static_cast<long long>(bt.batch) * H;
+  const long long bh0 = split_begin(c, BH, G), bh1 = split_begin(c + 1, BH, G);
+  uint8_t* ring = smem;
+  uint8_t* q_tile = smem + C::off_qb;
+  uint8_t* p_tile = smem + C::off_p;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.sfull[i], 1);
+      mbar_init(&S.sempty[i], 4);
+      mbar_init(&S.pfull[i], 4);
+      mbar_init(&S.pvdone[i], 1);
+    }
+    mbar_init(&S.ofinal, 1);
+    mbar_init(&S.oempty, 4);
+    fence_barrier_init();
   }
-  __device__ __forceinline__ bool active(int warp) const { return warp < RG * KS; }
-  __device__ __forceinline__ int states() const { return KS; }  // per row group
-};
+  // Warp roles, each on its own scheduler (warp % 4): warps 0-3 the rows,
+  // warp 5 the MMAs (and TMEM), warp 6 the loads; warps 4, 7 and 8 are idle.
+  if (warp == 5) tmem_alloc(&S.tmem_base, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 6) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int nk = 0, nq = 0;
+      bool waited = false;  // griddepcontrol.wait done
+      for (long long bh = bh0; bh < bh1; ++bh) {
+        const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+        const SeqMeta sm = load_meta(bt, b);
+        if (!sm.ok) continue;
+        const int np = (sm.nb + kPage - 1) / kPage;
+        if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
+        // the queries of (b, h) come from the preceding kernel; before them, the
+        // first (b, h) streams its pages that hold no block rows into the free stages
+        int p = 0;
+        if (!waited) {
+          for (; p < np && nk < C::kKStages; ++p, ++nk) {
+            if (p * kPage < sm.sb + sm.bb && (p + 1) * kPage > sm.sb) break;  // a page with block rows
+            const int y = (page_of(bt, b, p) * H + h) * kPage;
+            uint8_t* kt = ring + nk * C::KStage;
+            mbar_arrive_expect_tx(&S.full[nk], 2 * TB);
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) {
+              tma_load_2d(kt + hf * 8192, &tm_k, &S.full[nk], hf * 64, y);
+              tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.full[nk], hf * 64, y);
+            }
+          }
+          griddep_wait();
+          waited = true;
+        }
+        if (nq >= 1) wait_or_abort(S, &S.qempty, (nq - 1) & 1, bt.err);  // the previous (b, h)'s Q K^T are done
+        mbar_arrive_expect_tx(&S.qfull, C::QB);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(q_tile + hf * 16384, &tm_qb, &S.qfull, hf * 64, h, sm.cub);
+        ++nq;
+        for (; p < np; ++p, ++nk) {
+          const int s = nk % C::kKStages;
+          if (nk >= C::kKStages) wait_or_abort(S, &S.empty[s], (nk / C::kKStages - 1) & 1, bt.err);
+          const int y = (page_of(bt, b, p) * H + h) * kPage;
+          uint8_t* kt = ring + s * C::KStage;
+          mbar_arrive_expect_tx(&S.full[s], 2 * TB);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_2d(kt + hf * 8192, &tm_k, &S.full[s], hf * 64, y);
+            tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.full[s], hf * 64, y);
+          }
+        }
+      }
+      for (int i = (nk > C::kKStages ? nk - C::kKStages : 0); i < nk; ++i)  // every copy has landed
+        if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
+      if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
+      constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
+      int n = 0, nq = 0;  // pages, (b, h) pairs so far
+      for (long long bh = bh0; bh < bh1; ++bh) {
+        const int b = static_cast<int>(bh / H);
+        const SeqMeta sm = load_meta(bt, b);
+        if (!sm.ok) continue;
+        const int np = (sm.nb + kPage - 1) / kPage;
+        wait_or_abort(S, &S.qfull, nq & 1, bt.err);
+        tc_fence_after();
+        const uint32_t qa = smem_u32(q_tile);
+        auto issue_pv = [&](int j, int nn) {  // O += P V for the page j of this (b, h), global page nn
+          const int sb = nn & 1, st = nn % C::kKStages;
+          if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
+          wait_or_abort(S, &S.pfull[sb], (nn >> 1) & 1, bt.err);
+          tc_fence_after();
+          const uint32_t pa = smem_u32(p_tile + sb * C::PB);
+          const uint32_t va = smem_u32(ring + st * C::KStage + TB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&S.empty[st]);   // the K/V stage is free
+          umma_commit(&S.pvdone[sb]);  // P buffer free, O holds page j
+        };
+        for (int j = 0; j < np; ++j, ++n) {
+          const int st = n % C::kKStages, sb = n & 1;
+          wait_or_abort(S, &S.full[st], (n / C::kKStages) & 1, bt.err);
+          if (n >= 2) wait_or_abort(S, &S.sempty[sb], ((n >> 1) - 1) & 1, bt.err);
+          tc_fence_after();
+          const uint32_t ka = smem_u32(ring + st * C::KStage);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16(tmem + C::kTmemS + sb * 64, umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
+                      umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
+          umma_commit(&S.sfull[sb]);
+          if (j == np - 1) umma_commit(&S.qempty);  // this (b, h)'s queries are no longer read
+          if (j >= 1) issue_pv(j - 1, n - 1);
+        }
+        issue_pv(np - 1, n - 1);
+        umma_commit(&S.ofinal);
+        ++nq;
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax warps (one query row per thread)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
+    int n = 0, nq = 0;
+    for (long long bh = bh0; bh < bh1; ++bh) {
+      const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+      const SeqMeta sm = load_meta(bt, b);
+      if (!sm.ok) continue;
+      const int np = (sm.nb + kPage - 1) / kPage;
+      const bool warp_rows = warp * 32 < sm.bb;  // this warp holds block rows (warp-uniform)
+      const bool row_ok = r < sm.bb;
+      float m_ref = neg_inf(), l = 0.f;
+      for (int j = 0; j < np; ++j, ++n) {
+        const int sb = n & 1;
+        wait_or_abort(S, &S.sfull[sb], (n >> 1) & 1, bt.err);
+        tc_fence_after();
+        float sc[64];
+        if (warp_rows) tmem_ld_32x32b_x64(lane_base + C::kTmemS + sb * 64, sc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.sempty[sb]);
+        if (!warp_rows) {  // no block rows in this warp: its rows of P do not matter
+          if (lane == 0) mbar_arrive(&S.pfull[sb]);
+          continue;
+        }
+        // scale, mask keys past the sequence, page max (8 independent chains)
+        const int nvalid = sm.nb - j * kPage;  // keys of this page inside the sequence (>= 1)
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = neg_inf();
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          sc[k] = k < nvalid ? sc[k] * a.scale_log2 : neg_inf();
+          mx8[k & 7] = fmaxf(mx8[k & 7], sc[k]);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // a new reference max (first page, or a rise beyond the threshold) rescales O and l
+        const bool raise = row_ok && (j == 0 || mx > m_ref + kRescale);
+        const float factor = raise && j > 0 ? fast_exp2(m_ref - mx) : 1.f;
+        if (raise) m_ref = mx;
+        if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+          // O holds pages 0 .. j-1 once the previous P V is done
+          wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            tmem_ld_32x32b_x32(lane_base + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] *= factor;
+            tmem_st_32x32b_x32(lane_base + c0, ov);
+          }
+          tmem_st_wait();
+          l *= factor;
+        }
+        // P = 2^(S - m_ref) as bf16 into this row of the P tile (K-major, 128-byte swizzle)
+        if (n >= 2) wait_or_abort(S, &S.pvdone[sb], ((n >> 1) - 1) & 1, bt.err);  // P buffer sb is free
+        const float mu = row_ok ? m_ref : 0.f;
+        uint8_t* prow = p_tile + sb * C::PB;
+        float l8[8];  // 8 independent partial sums
+#pragma unroll
+        for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pv[e] = row_ok ? fast_exp2(sc[ch * 8 + e] - mu) : 0.f;
+            l8[e] += pv[e];
+          }
+          uint4 u;
+          u.x = pack_bf16x2(pv[0], pv[1]);
+          u.y = pack_bf16x2(pv[2], pv[3]);
+          u.z = pack_bf16x2(pv[4], pv[5]);
+          u.w = pack_bf16x2(pv[6], pv[7]);
+          *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch)) = u;
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pfull[sb]);
+      }
+      // ---- the (b, h) is complete: O / l out, then release O for the next (b, h)
+      wait_or_abort(S, &S.ofinal, nq & 1, bt.err);
+      tc_fence_after();
+      if (warp_rows) {
+        const float inv = 1.f / l;
+        const size_t orow = (static_cast<size_t>(sm.cus + sm.sb + r) * H + h);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          tmem_ld_32x32b_x32(lane_base + c0, ov);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(of + orow * D + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              u.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
+              u.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
+              u.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
+              u.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+              dst[q] = u;
+            }
+          }
+        }
+        if (row_ok && a.lse != nullptr) a.lse[orow] = (m_ref + log2f(l)) * kLn2;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.oempty);
+      ++nq;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
-    const __grid_constant__ CUtensorMap tm_o, const AttnArgs a, int n_block_ctas, int n_merge_ctas,
-    int part_rows) {
+    const __grid_constant__ CUtensorMap tm_o, const AttnArgs a, int n_block_ctas, int n_merge_ctas) {
   using C = StreamCfg<D>;
-  constexpr int TB = C::TB, PS = C::PS, OS = C::OS, C4 = D / 4;
+  constexpr int TB = C::TB;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -159,15 +415,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], block_role ? 8 : 4);  // block role: all 8 warps release a page; merge: one group
+      mbar_init(&S.empty[s], block_role ? 1 : 4);  // block role: the MMA completion; merge: one group of 4 warps
     }
     mbar_init(&S.qfull, 1);
-    mbar_init(&S.qempty, 8);
-    mbar_init(&S.cbar, 1);
+    mbar_init(&S.qempty, 1);  // block role: the Q K^T completion of a (b, h)
     S.abort_flag = 0;
     fence_barrier_init();
   }
-  griddep_wait();  // q_block, the pools (and any metadata) may come from the preceding kernel
+  // Programmatic dependent launch.  The preceding kernel (the step's projection)
+  // writes q_block and the current blocks' k/v rows only, so the metadata, the
+  // block table, the cached state and every other page are read before
+  // griddepcontrol.wait (a precondition of the ABI); q_block and the pages that
+  // hold block rows are read after it.
   griddep_launch_dependents();
   for (int b = threadIdx.x; b < bt.batch; b += kThreads) {  // units of every sequence
     const SeqMeta m = load_meta(bt, b);
@@ -192,231 +451,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     if (lane == 0) S.cu[bt.batch] = carry;
   }
   __syncthreads();
-  // This role's split over G = min(role CTAs, U) CTAs, so that every CTA taking
-  // part owns at least one unit (the arrival count of a (b, h) assumes it).
+  // Block role: CTA c owns the (b, h) pairs [c BH / G, (c + 1) BH / G), whole.
+  // Merge role: CTA c owns the units [c U / G, (c + 1) U / G).
   const long long U = S.cu[bt.batch];
   const long long n_role = block_role ? n_block_ctas : n_merge_ctas;
-  const long long G = U < n_role ? U : n_role;
   const long long c = block_role ? blockIdx.x : blockIdx.x - n_block_ctas;
+  if (block_role) {
+    const long long BH = static_cast<long long>(bt.batch) * H;
+    const long long G = BH < n_role ? BH : n_role;
+    if (c >= G) return;  // uniform across the CTA
+    block_role_tc<D>(S, smem, tm_qb, tm_k, tm_v, a, c, G);
+    return;
+  }
+  const long long G = U < n_role ? U : n_role;
   if (c >= G) return;  // uniform across the CTA
   UWalk w;
   w.u = split_begin(c, U, G);
   w.u1 = split_begin(c + 1, U, G);
   w.seek(S, bt, H);
-
-  if (block_role) {
-    uint8_t* ring = smem;
-    uint8_t* qb_tile = smem + C::off_qb;
-    float* comb_o = reinterpret_cast<float*>(smem + C::off_comb);  // [KS * RG * 16 <= 128 (slice, row)][OS]
-    if (warp == 8) {
-      // ---------------------------------------------------- block producer
-      if (lane == 0) {
-        int nk = 0, nq = 0;
-        for (; w.valid(); w.next(S, bt, H)) {
-          if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
-          if (w.seg_start()) {  // the block queries of (b, h)
-            if (nq >= 1) wait_or_abort(S, &S.qempty, (nq - 1) & 1, bt.err);
-            mbar_arrive_expect_tx(&S.qfull, TB);
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf)
-              tma_load_3d(qb_tile + hf * 8192, &tm_qb, &S.qfull, hf * 64, w.h, w.sm.cub);
-            ++nq;
-          }
-          const int s = nk % C::kKStages;
-          if (nk >= C::kKStages) wait_or_abort(S, &S.empty[s], (nk / C::kKStages - 1) & 1, bt.err);
-          const int y = (page_of(bt, w.b, w.p) * H + w.h) * kPage;
-          uint8_t* kt = ring + s * C::KStage;
-          mbar_arrive_expect_tx(&S.full[s], 2 * TB);
-#pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_2d(kt + hf * 8192, &tm_k, &S.full[s], hf * 64, y);
-            tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.full[s], hf * 64, y);
-          }
-          ++nk;
-        }
-        for (int i = (nk > C::kKStages ? nk - C::kKStages : 0); i < nk; ++i)  // every copy has landed
-          if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
-        if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
-      }
-      return;
-    }
-    // ------------------------------------------------ block compute (warps 0-7)
-    const int g = lane >> 2, t = lane & 3;
-    int nk = 0, nq = 0, ncb = 0;  // K/V pages, query tiles, combine passes so far
-    WarpAttn<D> st;
-    uint32_t qf[D / 16][4];
-    __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
-    for (; w.valid(); w.next(S, bt, H)) {
-      const BlockSplit sp(w.sm.bb);
-      const bool active = sp.active(warp);
-      const int rg = warp % sp.RG, ks = warp / sp.RG;
-      if (w.seg_start()) {
-        wait_or_abort(S, &S.qfull, nq & 1, bt.err);
-        if (active) load_q_frags<D>(qf, smem_u32(qb_tile), rg * 16, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.qempty);
-        ++nq;
-        st.init();
-      }
-      const int s = nk % C::kKStages;
-      wait_or_abort(S, &S.full[s], (nk / C::kKStages) & 1, bt.err);
-      if (active) {
-        const uint32_t kt = smem_u32(ring + s * C::KStage), vt = kt + TB;
-        const int base = w.p * kPage, nb = w.sm.nb;
-        auto valid = [base, nb](int key) { return base + key < nb; };
-        if (sp.KS == 4)
-          attend<D, 16>(st, qf, kt, vt, ks * 16, a.scale_log2, valid, lane);
-        else
-          attend<D, 32>(st, qf, kt, vt, ks * 32, a.scale_log2, valid, lane);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[s]);
-      ++nk;
-      if (!w.seg_end()) continue;
-
-      // ---- (b, h) segment complete on this CTA: combine the KS states of each row in shared memory
-      if (active) {
-        st.reduce_l();
-        const int slot0 = ks * sp.RG * 16 + rg * 16 + g, slot1 = slot0 + 8;
-        if (t == 0) {
-          S.comb_m[slot0] = st.m[0];
-          S.comb_l[slot0] = st.l[0];
-          S.comb_m[slot1] = st.m[1];
-          S.comb_l[slot1] = st.l[1];
-        }
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          *reinterpret_cast<float2*>(comb_o + slot0 * OS + 8 * n + 2 * t) = make_float2(st.o[n][0], st.o[n][1]);
-          *reinterpret_cast<float2*>(comb_o + slot1 * OS + 8 * n + 2 * t) = make_float2(st.o[n][2], st.o[n][3]);
-        }
-      }
-      named_barrier(1, 256);
-      const size_t row0 = static_cast<size_t>(w.sm.cus + w.sm.sb) * H + w.h;  // o_full / lse row of block row 0
-      const bool whole = w.seg_whole();
-      const long long s_bh = S.cu[w.b] + static_cast<long long>(w.h) * w.np, e_bh = s_bh + w.np;
-      const int my_slot = (split_begin(c, U, G) >= s_bh) ? 0 : 1;  // first / last segment of this CTA
-      float* mine = a.part + ((static_cast<size_t>(c) * 2 + my_slot) * part_rows) * PS;
-      for (int item = threadIdx.x; item < w.sm.bb * C4; item += 256) {
-        const int i = item / C4, col = (item % C4) * 4;
-        float M = neg_inf();
-        for (int q = 0; q < sp.states(); ++q) M = fmaxf(M, S.comb_m[q * sp.RG * 16 + i]);
-        const float Mu = M == neg_inf() ? 0.f : M;
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < sp.states(); ++q) {
-          const int slot = q * sp.RG * 16 + i;
-          const float wgt = fast_exp2(S.comb_m[slot] - Mu);
-          L += wgt * S.comb_l[slot];
-          const float4 ov = *reinterpret_cast<const float4*>(comb_o + slot * OS + col);
-          acc.x += wgt * ov.x;
-          acc.y += wgt * ov.y;
-          acc.z += wgt * ov.z;
-          acc.w += wgt * ov.w;
-        }
-        if (whole) {  // every page of (b, h) was here: finish the row
-          const float inv = 1.f / L;
-          const size_t orow = row0 + static_cast<size_t>(i) * H;
-          uint2 pk;
-          pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-          pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(of + orow * D + col) = pk;
-          if (a.lse != nullptr && col == 0) a.lse[orow] = (M + log2f(L)) * kLn2;
-        } else {
-          *reinterpret_cast<float4*>(mine + i * PS + col) = acc;
-          if (col == 0) *reinterpret_cast<float2*>(mine + i * PS + D) = make_float2(M, L);
-        }
-      }
-      named_barrier(1, 256);  // comb is free again; the partial rows are written ...
-      if (whole) continue;
-      const int c_first = split_of(s_bh, U, G), c_last = split_of(e_bh - 1, U, G);
-      int32_t* counter = a.counters + static_cast<size_t>(w.b) * H + w.h;
-      if (threadIdx.x == 0) {
-        __threadfence();  // ... and (cumulatively) visible GPU-wide before the arrival is counted
-        S.last_flag = atomicAdd(counter, 1) == c_last - c_first;
-      }
-      named_barrier(1, 256);
-      if (!S.last_flag) continue;
-      __threadfence();
-      // Last arrival: merge every contributor's state (this CTA's too, as
-      // written) in contributor order, so the rounding does not depend on
-      // which CTA arrives last.  The contributors' slots come into the idle
-      // key-slice buffer with bulk copies, as many at once as fit, so each
-      // pass costs one round trip however many rows and contributors it has.
-      const int n_contrib = c_last - c_first + 1;
-      const float* slot_first =
-          a.part + (static_cast<size_t>(c_first) * 2 + (split_begin(c_first, U, G) < s_bh ? 1 : 0)) * part_rows * PS;
-      const size_t cta_stride = static_cast<size_t>(2) * part_rows * PS;
-      auto slot_of = [&](int k) { return k == 0 ? slot_first : a.part + static_cast<size_t>(c_first + k) * cta_stride; };
-      const uint32_t slot_bytes = static_cast<uint32_t>(w.sm.bb) * PS * 4;
-      const int fit = C::kCombBytes / static_cast<int>(slot_bytes);  // slots the buffer holds (>= 2)
-      // one pass if every contributor fits; otherwise the last slot keeps the running state
-      const int per_pass = n_contrib <= fit ? fit : fit - 1;
-      float* stage = comb_o;  // [fit][bb][PS]
-      // Passes of per_pass contributors (one pass in all but the largest
-      // splits); between passes the running (max, sum, accumulators) of each
-      // row wait in the buffer's last slot.
-      float* keep = stage + static_cast<size_t>(fit - 1) * w.sm.bb * PS;
-      for (int k0 = 0; k0 < n_contrib; k0 += per_pass) {
-        const int nk = min(per_pass, n_contrib - k0);
-        const bool first = k0 == 0, last_pass = k0 + nk >= n_contrib;
-        if (threadIdx.x == 0) {
-          // order the other contributors' writes (acquired above) and this CTA's earlier generic
-          // accesses of the buffer before the async-proxy copies
-          asm volatile("fence.proxy.async;" ::: "memory");
-          mbar_arrive_expect_tx(&S.cbar, slot_bytes * nk);
-          for (int k = 0; k < nk; ++k) bulk_load(stage + k * w.sm.bb * PS, slot_of(k0 + k), slot_bytes, &S.cbar);
-        }
-        wait_or_abort(S, &S.cbar, ncb & 1, bt.err);
-        ++ncb;
-        for (int item = threadIdx.x; item < w.sm.bb * C4; item += 256) {
-          const int i = item / C4, col = (item % C4) * 4;
-          float* kr = keep + i * PS;
-          float Mprev = neg_inf(), Lprev = 0.f;
-          float4 Aprev = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!first) {
-            Aprev = *reinterpret_cast<const float4*>(kr + col);
-            const float2 ml = *reinterpret_cast<const float2*>(kr + D);  // the row's, from the previous pass
-            Mprev = ml.x;
-            Lprev = ml.y;
-          }
-          float M = Mprev;
-          for (int k = 0; k < nk; ++k) M = fmaxf(M, stage[(k * w.sm.bb + i) * PS + D]);
-          const float Mu = M == neg_inf() ? 0.f : M;
-          const float r = fast_exp2(Mprev - Mu);  // rescales the earlier passes (0 before the first)
-          float L = r * Lprev;
-          float4 acc = make_float4(r * Aprev.x, r * Aprev.y, r * Aprev.z, r * Aprev.w);
-          for (int k = 0; k < nk; ++k) {
-            const float* pr = stage + (k * w.sm.bb + i) * PS;
-            const float wgt = fast_exp2(pr[D] - Mu);
-            L += wgt * pr[D + 1];
-            const float4 ov = *reinterpret_cast<const float4*>(pr + col);
-            acc.x += wgt * ov.x;
-            acc.y += wgt * ov.y;
-            acc.z += wgt * ov.z;
-            acc.w += wgt * ov.w;
-          }
-          if (last_pass) {
-            const float inv = 1.f / L;
-            const size_t orow = row0 + static_cast<size_t>(i) * H;
-            uint2 pk;
-            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(of + orow * D + col) = pk;
-            if (a.lse != nullptr && col == 0) a.lse[orow] = (M + log2f(L)) * kLn2;
-          } else {
-            // every item of a row computes the same (M, L); the column-0 item keeps it for the
-            // next pass (read there by the row's other items, after the barrier below)
-            *reinterpret_cast<float4*>(kr + col) = acc;
-            if (col == 0) *reinterpret_cast<float2*>(kr + D) = make_float2(M, L);
-          }
-        }
-        named_barrier(1, 256);  // the staged slots are consumed before the next pass overwrites them
-      }
-      if (threadIdx.x == 0) *counter = 0;  // ready for the next call
-      named_barrier(1, 256);  // comb_m is reused by the next segment
-    }
-    return;
-  }
 
   // ===================================================================== merge role
   uint8_t* ring = smem;
@@ -456,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
   for (; w.valid(); w.next(S, bt, H)) {
     if (w.seg_start()) {  // gather the fresh block keys / values of (b, h) through the table
+      griddep_wait();         // they come from the preceding kernel (a no-op after the first time)
       named_barrier(2, 256);  // both groups are done with the previous (b, h)'s
       nkc = w.sm.bb <= 32 ? 32 : 64;  // keys the QK^T below covers; rows past bb are zero
       const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
@@ -548,7 +601,7 @@ cudaError_t launch_d(const AttnArgs& a, const AttnPlan& plan, cudaStream_t strea
   CUtensorMap tm_qb = m.k;
   if (block) {
     e = encode_3d_rows_sw128(&tm_qb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_block, D, a.n_heads,
-                             a.bt.total_block_rows, 64, 64);
+                             a.bt.total_block_rows, 64, 128);
     if (e != cudaSuccess) return e;
   }
   constexpr int smem = StreamCfg<D>::kSmem;
@@ -556,37 +609,32 @@ cudaError_t launch_d(const AttnArgs& a, const AttnPlan& plan, cudaStream_t strea
   e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(plan.n_block_ctas + plan.n_merge_ctas), kThreads, smem, 0, stream, tm_qb, m.k, m.v,
-                    m.q, m.o, a, plan.n_block_ctas, plan.n_merge_ctas, plan.part_rows);
+                    m.q, m.o, a, plan.n_block_ctas, plan.n_merge_ctas);
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
 AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int num_sms, bool block,
                    bool merge) {
+  (void)head_dim;
+  (void)max_block_len;
   AttnPlan p = {};
   const long long max_pages = (max_seq_len + kPage - 1) / kPage;
-  const long long units = static_cast<long long>(batch) * n_heads * max_pages;  // upper bound of either role's units
+  const long long bh = static_cast<long long>(batch) * n_heads;
+  const long long units = bh * max_pages;  // upper bound of the merge role's units
   const int g = static_cast<int>(units < num_sms ? (units < 1 ? 1 : units) : num_sms);
-  p.part_rows = max_block_len < 1 ? 1 : max_block_len;
   if (block && merge) {
-    // one block-role CTA per (b, h) (so that no (b, h) needs a cross-CTA merge)
-    // while that is at most half of the CTAs; the rest take the merge role
-    const long long bh = static_cast<long long>(batch) * n_heads;
+    // one block-role CTA per (b, h) while that is at most half of the CTAs (each
+    // owns whole (b, h) pairs: no cross-CTA merge); the rest take the merge role
     const int half = g / 2 < 1 ? 1 : g / 2;
     p.n_block_ctas = bh < half ? static_cast<int>(bh) : half;
     p.n_merge_ctas = g - p.n_block_ctas < 1 ? 1 : g - p.n_block_ctas;
   } else {
-    p.n_block_ctas = block ? g : 0;
+    p.n_block_ctas = block ? static_cast<int>(bh < num_sms ? bh : num_sms) : 0;
     p.n_merge_ctas = merge ? g : 0;
   }
-  if (block) {  // two partial slots per block CTA (its first and last (b, h)) and one counter per (b, h)
-    p.part_bytes = align256(static_cast<size_t>(p.n_block_ctas) * 2 * p.part_rows * (head_dim + 4) * 4);
-    p.counter_offset = p.part_bytes;
-    p.total_bytes = p.counter_offset + align256(static_cast<size_t>(batch) * n_heads * 4);
-  }
-  return p;
+  return p;  // no workspace
 }
 
 bool attn_batch_supported(int batch) { return batch <= kMaxBatch; }

@@ -105,8 +105,6 @@ AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cac
   a.n_heads = d->n_heads;
   a.head_dim = d->head_dim;
   a.scale_log2 = softmax_scale(d) * 1.4426950408889634f;
-  a.part = nullptr;
-  a.counters = nullptr;
   return a;
 }
 
@@ -114,13 +112,7 @@ AttnPlan plan_of(const dllm_layer_desc* d, const dllm_batch* b, bool block, bool
   return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, b->max_block_len, device_sms(), block, merge);
 }
 
-// Point the attention launch at its workspace (partial states, arrival counters).
-void bind_workspace(AttnArgs* a, const AttnPlan& plan, void* ws) {
-  if (plan.total_bytes == 0) return;
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  a->part = reinterpret_cast<float*>(base);
-  a->counters = reinterpret_cast<int32_t*>(base + plan.counter_offset);
-}
+
 
 QkvArgs qkv_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache* c, const float* rope,
                  int32_t rope_max_pos, int mode, int n_tok) {
@@ -308,7 +300,6 @@ dllm_status attention_call(const dllm_layer_desc* desc, const dllm_batch* batch,
   aa.q_block = q_block;
   aa.o_full = o_full;
   aa.lse = lse;
-  bind_workspace(&aa, plan, ws);
   DLLM_CUDA_TRY(launch_step_attention(aa, plan, static_cast<cudaStream_t>(stream)));
   return DLLM_OK;
 }

@@ -88,17 +88,13 @@ struct AttnArgs {
   int32_t n_heads;
   int32_t head_dim;
   float scale_log2;     // softmax_scale * log2(e)
-  // block part of (b, h) split over CTAs: partial states and arrival counters in the workspace
-  float* part;          // fp32 [block CTAs][2][part_rows][head_dim + 4]
-  int32_t* counters;    // [batch][H]; zero between calls
 };
 
 // One attention launch: a persistent grid of block-role and merge-role CTAs,
 // each role walking the (sequence, head, page) units.
 struct AttnPlan {
-  int n_block_ctas, n_merge_ctas;     // CTAs of each role (one CTA per SM in all)
-  int part_rows;                      // rows of a partial-state slot (max_block_len)
-  size_t part_bytes, counter_offset, total_bytes;  // workspace (0 without the block role)
+  int n_block_ctas, n_merge_ctas;  // CTAs of each role (one CTA per SM in all)
+  size_t total_bytes;              // workspace (none needed: 0)
 };
 AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int num_sms, bool block,
                    bool merge);

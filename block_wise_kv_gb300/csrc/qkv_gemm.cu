@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // Let the next kernel (the step's attention) start on the SMs this grid leaves
+  // free: it streams what this kernel does not write while the weights stream.
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -512,7 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -276,7 +276,7 @@ class PagedCache:
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     """Caller-owned scratch of at least nbytes (256-byte aligned by torch's
-    allocator), zero-filled as the attention calls' arrival counters require."""
+    allocator), zero-filled."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 

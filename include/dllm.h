@@ -44,6 +44,16 @@
  *     when that pointer is non-NULL; outputs are then undefined.
  *   - Thread safety: calls on different streams are safe when their outputs
  *     do not overlap.
+ *   - Overlap with the preceding kernel: the calls are launched with
+ *     programmatic dependent launch.  The attention calls
+ *     (dllm_block_attention, dllm_state_merge, dllm_step_attention) may read
+ *     the batch metadata, the block table, q_pool, m_pool, l_pool, o_pool and
+ *     every k/v page that holds none of the current blocks' rows before the
+ *     kernel that precedes them on the stream has finished; that kernel must
+ *     not write those.  dllm_block_qkv_rope_write writes only q_block and the
+ *     current blocks' k/v rows, so the step's own order (projection, then
+ *     attention) meets this.  q_block and the current blocks' k/v pages are
+ *     read only after the preceding kernel has completed.
  *
  * Layouts (all row-major, little-endian, bf16 = IEEE bfloat16)
  *   page      = 64 consecutive token positions of one sequence.
@@ -143,11 +153,7 @@ typedef struct dllm_batch {
 
 /* Bytes of device workspace `op` needs for this layer and batch (0 if none).
  * The workspace is scratch owned by the caller, 256-byte aligned, and may be
- * reused once the call's work on its stream has completed.  The workspace of
- * DLLM_OP_BLOCK_ATTENTION and DLLM_OP_STEP_ATTENTION holds arrival counters:
- * it must be zero-filled before its first use, and every call leaves it
- * zero-filled (after a call that reported DLLM_DEVERR_TIMEOUT, fill it with
- * zeros again). */
+ * reused once the call's work on its stream has completed. */
 dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t op, size_t* bytes);
 
 /* Fill the RoPE table (device fp32 [max_pos][head_dim/2][2]) with
@@ -228,11 +234,10 @@ dllm_status dllm_block_qkv_rope_write_noalloc(const dllm_layer_desc* desc, const
  * o_full row cu_seq[b] + s_b + i, and L = m + ln l to lse (nullable) at the
  * same row.  q_block as written by dllm_block_qkv_rope_write; the pools as
  * written by dllm_cache_build and this step's dllm_block_qkv_rope_write.
- * The keys of a (sequence, head) are split into chunks of pages whose
- * partial states (m, l, O~) meet in ws and are merged exactly (the
- * Eq. (2)-(6) merge applied to states) by the chunk that finishes last.
- *   ws: dllm_workspace_size(DLLM_OP_BLOCK_ATTENTION) bytes (zero-filled before
- *   first use, see dllm_workspace_size). */
+ * The online-softmax state of a row runs over all pages of its sequence
+ * (Eq. (2)-(6)); its reference maximum is raised only when a page's maximum
+ * exceeds it by more than 2^8 (exact for any reference).
+ *   ws: dllm_workspace_size(DLLM_OP_BLOCK_ATTENTION) bytes (currently 0). */
 dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
                                  const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
                                  void* stream);
@@ -255,8 +260,7 @@ dllm_status dllm_state_merge(const dllm_layer_desc* desc, const dllm_batch* batc
  * of o_full and lse), with the merge work filling the GPU while the block
  * attention finishes (no counterpart in the pages: a scheduling choice of
  * this library).
- *   ws: dllm_workspace_size(DLLM_OP_STEP_ATTENTION) bytes (zero-filled before
- *   first use, see dllm_workspace_size). */
+ *   ws: dllm_workspace_size(DLLM_OP_STEP_ATTENTION) bytes (currently 0). */
 dllm_status dllm_step_attention(const dllm_layer_desc* desc, const dllm_batch* batch, const void* q_block,
                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
                                 void* stream);

@@ -46,24 +46,8 @@ def test_workspace_sizes(lib):
     # x^ rows (then, for small models with few weight tiles, stream-K partial tiles and counters)
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) >= 64 * 4096 * 2
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1536 * 4096 * 2
-    # block role: two fp32 partial-state slots [max_block_len][128 + 4] per block-role CTA (one CTA per
-    # SM, at most one per unit; with the merge in the same launch, one block-role CTA per (sequence, head)
-    # up to half of them), then
-    # one arrival counter per (sequence, head)
-    import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
-    slot = 2 * 32 * 132 * 4
-
-    def want(ctas):
-        return (ctas * slot + 255) // 256 * 256 + 256
-
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_ATTENTION) == want(sms)
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STEP_ATTENTION) == want(min(sms // 2, 2 * 32))
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_STATE_MERGE) == 0
-    # fewer units than SMs: at most one CTA per unit (1 sequence x 32 heads x 2 pages = 64 units)
-    small = _batch(batch=1, max_seq=128, R=128, M=32)
-    assert dllm.dllm_workspace_size(d, small, dllm.DLLM_OP_BLOCK_ATTENTION) == want(64)
-    assert dllm.dllm_workspace_size(d, small, dllm.DLLM_OP_STEP_ATTENTION) == want(64 // 2)
+    for op in (dllm.DLLM_OP_BLOCK_ATTENTION, dllm.DLLM_OP_STATE_MERGE, dllm.DLLM_OP_STEP_ATTENTION):
+        assert dllm.dllm_workspace_size(d, b, op) == 0
     with pytest.raises(dllm.DllmError) as e:
         dllm.dllm_workspace_size(d, b, 17)
     assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
