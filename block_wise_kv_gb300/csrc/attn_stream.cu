@@ -2,43 +2,37 @@
 // persistent, pipelined kernel (sm_103a): the block rows' attention over
 // every key of their sequence and the FACache merge of every invariant row.
 //
-// Work is cut into units (sequence b, head h, page p) over the real pages of
-// every sequence.  The grid's CTAs (one per SM) take one of two roles, each
-// walking a contiguous range of the units:
-//   block role   the block queries of (b, h) (<= 64 rows, loaded once per
-//                (b, h) by TMA through a 3-D tensor map over q_block) against
-//                the 64 keys of page p (Fast-dLLM DualCache: [prefix KV |
-//                fresh block KV | suffix KV] read through the block table).
-//                The 8 compute warps split each page's keys; each keeps its
-//                online-softmax state (LaCache Eq. (2)-(6)) in registers
-//                across the CTA's pages of (b, h), and at the end of the
-//                (b, h) the states meet in shared memory.  A (b, h) whose
-//                pages span several CTAs leaves one partial state per CTA in
-//                the workspace; the last CTA to arrive merges them exactly,
-//                in contributor order (the same merge applied to states).
-//   merge role   the rows of U in page p: the cached state (m, l, O~) merged
-//                with the fresh partial state over the block keys (LaCache
-//                §3.3.3, Algorithm 1 with GenStep = False).  Two groups of 4
-//                warps take alternate pages.
-// Half of the CTAs take the block role (a merge CTA works on two pages at a
-// time, a block CTA on one), so a (b, h) spans few CTAs and its merge is
-// short.  In both
-// roles warp 8 streams tiles with TMA (128-byte swizzle) into an mbarrier
-// ring that runs ahead across pages and (b, h) boundaries; QK^T / PV run on
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate), 16 query rows per warp, row
-// max and sum with quad shuffles.
+// The grid's CTAs (one per SM) take one of two roles:
+//   block role   a contiguous range of (sequence b, head h) pairs, each owned
+//                whole by one CTA: the block queries (<= 64 rows) against all
+//                of the sequence's pages (Fast-dLLM DualCache: [prefix KV |
+//                fresh block KV | suffix KV] read through the block table),
+//                S = Q K^T and O += P V on the 5th-generation tensor cores
+//                with the accumulators in tensor memory, online softmax
+//                (LaCache Eq. (2)-(6)) between the two MMAs.  No state leaves
+//                the CTA before O / l is final.
+//   merge role   a contiguous range of units (b, h, page p) over the real
+//                pages of every sequence: the rows of U in page p, the cached
+//                state (m, l, O~) merged with the fresh partial state over
+//                the block keys (LaCache §3.3.3, Algorithm 1 with GenStep =
+//                False), on mma.sync m16n8k16 (bf16 in, fp32 accumulate); two
+//                groups of 4 warps take alternate pages.
+// At most half of the CTAs (and at most one per (b, h)) take the block role.
+// In both roles one warp streams tiles with TMA (128-byte swizzle) into an
+// mbarrier ring that runs ahead across pages and (b, h) boundaries.
 //
-// Programmatic dependent launch: barrier setup overlaps the tail of the
-// preceding kernel; every read of data it may write comes after
-// griddepcontrol.wait.  Every wait is bounded; after a timeout the CTA stops
-// waiting, flags DLLM_DEVERR_TIMEOUT and drains its own copies.
+// Programmatic dependent launch: barrier setup, the metadata prefix and the
+// loads of data the preceding kernel does not write (pages without block
+// rows) overlap that kernel's tail; every read of data it may write comes
+// after griddepcontrol.wait.  Every wait is bounded; after a timeout the CTA
+// stops waiting, flags DLLM_DEVERR_TIMEOUT and drains its own copies.
 #include "attn_common.cuh"
 
 namespace dllm {
 namespace {
 using namespace attn;
 
-constexpr int kThreads = 288;  // warps 0-7 compute, warp 8 streams tiles
+constexpr int kThreads = 320;  // merge role: warps 0-7 compute, 8 streams; block role: 0-3, 8 MMAs, 9 streams
 constexpr int kMaxBatch = 512;
 
 template <int D>
@@ -69,6 +63,8 @@ struct Shared {
   uint64_t full[4], empty[4], qfull, qempty;
   uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
   uint32_t tmem_base;
+  float xmax[2][4][32];  // block role: [page parity][warp][lane] maxima over the warp's keys
+  float xl[4][32];       // block role: [warp][lane] sums over the warp's keys
   int abort_flag;
   int n_seq_units[kMaxBatch];  // H * pages of sequence b (0: invalid metadata)
   int cu[kMaxBatch + 1];       // unit prefix
@@ -127,20 +123,21 @@ __device__ __forceinline__ void wait_or_abort(Shared& S, uint64_t* bar, uint32_t
 
 // ---------------------------------------------------------------------------
 // Block role on the 5th-generation tensor cores.  For each (b, h) the CTA
-// owns: the block queries (<= 64 rows, padded to the 128-row MMA tile) stay in
-// shared memory; per 64-key page, warp 4 issues S = Q K^T (M = 128, N = 64,
-// into one of two TMEM score buffers) and, once the softmax warps have written
-// P for it, O += P V (M = 128, N = D, V as an MN-major operand) into TMEM, so
-// the scores of page p + 1 are computed while page p's softmax runs.  Warps
-// 0-3 own one query row per thread (TMEM lane): exact row max over the page,
-// P = 2^(S - m_ref) with a reference max m_ref that is raised (and O, l
-// rescaled) only when a page's max exceeds it by more than 2^8 (every P stays
-// <= 2^8; the result is exact for any reference), running sum l in fp32, and
-// at the end of the (b, h) O / l and L = m_ref + log2 l.
+// owns: the block queries stay in shared memory as a 128-row MMA tile; per
+// 64-key page, warp 8 issues S = Q K^T (M = 128, N = 64, into one of two TMEM
+// score buffers) and, once the softmax warps have written P for it, O += P V
+// (M = 128, N = D, V as an MN-major operand) into TMEM, so the scores of page
+// p + 1 are computed while page p's softmax runs.  The softmax (warps 0-3):
+// exact row max over the page, P = 2^(S - m_ref) with a reference max m_ref
+// that is raised (and O, l rescaled) only when a page's max exceeds it by
+// more than 2^8 (every P stays <= 2^8; the result is exact for any
+// reference), running sum l in fp32, and at the end of the (b, h) O / l and
+// L = m_ref + log2 l.
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CUtensorMap& tm_qb,
-                                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
+                                              const CUtensorMap& tm_qb64, const CUtensorMap& tm_k,
+                                              const CUtensorMap& tm_v, const AttnArgs& a,
                                               long long c, long long G) {
   using C = StreamCfg<D>;
   constexpr int TB = C::TB;
@@ -164,15 +161,21 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
     mbar_init(&S.oempty, 4);
     fence_barrier_init();
   }
-  // Warp roles, each on its own scheduler (warp % 4): warps 0-3 the rows,
-  // warp 5 the MMAs (and TMEM), warp 6 the loads; warps 4, 7 and 8 are idle.
-  if (warp == 5) tmem_alloc(&S.tmem_base, C::kTmemCols);
+  // A TMEM lane quadrant q is read only by warps q mod 4, which all issue
+  // from scheduler q, so the block queries (<= 32 or <= 64 rows) are loaded
+  // into every quadrant of the 128-row query tile (4 or 2 copies; the extra
+  // MMA rows cost nothing): warp q (0-3) reads its quadrant's copy and takes
+  // 1/4 or 1/2 of every page's keys, and the four schedulers share each
+  // page's softmax.  Row r's state across the warps is combined through
+  // shared memory (page max every page, the sums at the end).  Warp 8 issues
+  // the MMAs (and owns TMEM), warp 9 streams the tiles, warps 4-7 idle.
+  if (warp == 8) tmem_alloc(&S.tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  if (warp == 6) {
+  if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int nk = 0, nq = 0;
@@ -203,8 +206,15 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         }
         if (nq >= 1) wait_or_abort(S, &S.qempty, (nq - 1) & 1, bt.err);  // the previous (b, h)'s Q K^T are done
         mbar_arrive_expect_tx(&S.qfull, C::QB);
+        {
+          const bool wide = sm.bb > 32;  // copies of 64 rows (2) or 32 rows (4)
+          const int rows = wide ? 64 : 32;
+          for (int cp = 0; cp < 128 / rows; ++cp)
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(q_tile + hf * 16384, &tm_qb, &S.qfull, hf * 64, h, sm.cub);
+            for (int hf = 0; hf < D / 64; ++hf)
+              tma_load_3d(q_tile + hf * 16384 + cp * rows * 128, wide ? &tm_qb64 : &tm_qb, &S.qfull, hf * 64, h,
+                          sm.cub);
+        }
         ++nq;
         for (; p < np; ++p, ++nk) {
           const int s = nk % C::kKStages;
@@ -223,7 +233,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
       if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
-  } else if (warp == 5) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
@@ -272,8 +282,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
     }
     __syncwarp();
   } else if (warp < 4) {
-    // ------------------------------------------------------------ softmax warps (one query row per thread)
-    const int r = warp * 32 + lane;
+    // ------------------------------------------------------------ softmax warps
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
     int n = 0, nq = 0;
@@ -282,86 +291,99 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
       const SeqMeta sm = load_meta(bt, b);
       if (!sm.ok) continue;
       const int np = (sm.nb + kPage - 1) / kPage;
-      const bool warp_rows = warp * 32 < sm.bb;  // this warp holds block rows (warp-uniform)
+      const int RQ = sm.bb > 32 ? 2 : 1;        // quadrants per copy of the queries
+      const int rb = warp % RQ, slice = warp / RQ;  // row block, key slice
+      const int KW = 16 * RQ;                   // keys per warp per page
+      const int r = rb * 32 + lane;             // query row
       const bool row_ok = r < sm.bb;
-      float m_ref = neg_inf(), l = 0.f;
+      float m_ref = neg_inf(), l = 0.f;  // l: over this warp's keys
       for (int j = 0; j < np; ++j, ++n) {
         const int sb = n & 1;
         wait_or_abort(S, &S.sfull[sb], (n >> 1) & 1, bt.err);
         tc_fence_after();
-        float sc[64];
-        if (warp_rows) tmem_ld_32x32b_x64(lane_base + C::kTmemS + sb * 64, sc);
+        float sc[32];
+        const uint32_t scol = lane_base + C::kTmemS + sb * 64 + slice * KW;
+        if (RQ == 1)
+          tmem_ld_32x32b_x16(scol, *reinterpret_cast<float(*)[16]>(sc));
+        else
+          tmem_ld_32x32b_x32(scol, sc);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.sempty[sb]);
-        if (!warp_rows) {  // no block rows in this warp: its rows of P do not matter
-          if (lane == 0) mbar_arrive(&S.pfull[sb]);
-          continue;
-        }
-        // scale, mask keys past the sequence, page max (8 independent chains)
-        const int nvalid = sm.nb - j * kPage;  // keys of this page inside the sequence (>= 1)
-        float mx8[8];
+        // scale, mask keys past the sequence, this warp's max; the row's page max
+        const int nvalid = sm.nb - j * kPage - slice * KW;
+        float mx4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) mx8[q] = neg_inf();
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < 32; ++k) {
+          if (k >= KW) break;
           sc[k] = k < nvalid ? sc[k] * a.scale_log2 : neg_inf();
-          mx8[k & 7] = fmaxf(mx8[k & 7], sc[k]);
+          mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // a new reference max (first page, or a rise beyond the threshold) rescales O and l
+        S.xmax[j & 1][warp][lane] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        named_barrier(4, 128);
+        float mx = neg_inf();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q % RQ == rb) mx = fmaxf(mx, S.xmax[j & 1][q][lane]);
+        // a new reference max (first page, or a rise beyond the threshold) rescales O and l;
+        // every warp of the row takes the same decision from the same values
         const bool raise = row_ok && (j == 0 || mx > m_ref + kRescale);
         const float factor = raise && j > 0 ? fast_exp2(m_ref - mx) : 1.f;
         if (raise) m_ref = mx;
         if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-          // O holds pages 0 .. j-1 once the previous P V is done
-          wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);
-          tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            float ov[32];
-            tmem_ld_32x32b_x32(lane_base + c0, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= factor;
-            tmem_st_32x32b_x32(lane_base + c0, ov);
-          }
-          tmem_st_wait();
           l *= factor;
+          if (slice == 0) {  // O's rows of this row block live in this warp's quadrant
+            wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);  // O holds pages 0 .. j-1
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              float ov[32];
+              tmem_ld_32x32b_x32(lane_base + c0, ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] *= factor;
+              tmem_st_32x32b_x32(lane_base + c0, ov);
+            }
+            tmem_st_wait();
+          }
         }
-        // P = 2^(S - m_ref) as bf16 into this row of the P tile (K-major, 128-byte swizzle)
+        // P = 2^(S - m_ref) as bf16 into this warp's keys of row r of the P tile (K-major, 128-byte swizzle)
         if (n >= 2) wait_or_abort(S, &S.pvdone[sb], ((n >> 1) - 1) & 1, bt.err);  // P buffer sb is free
         const float mu = row_ok ? m_ref : 0.f;
         uint8_t* prow = p_tile + sb * C::PB;
-        float l8[8];  // 8 independent partial sums
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) l8[q] = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int cc = 0; cc < 4; ++cc) {
+          if (cc * 8 >= KW) break;
           float pv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            pv[e] = row_ok ? fast_exp2(sc[ch * 8 + e] - mu) : 0.f;
-            l8[e] += pv[e];
+            pv[e] = row_ok ? fast_exp2(sc[cc * 8 + e] - mu) : 0.f;
+            l4[e & 3] += pv[e];
           }
           uint4 u;
           u.x = pack_bf16x2(pv[0], pv[1]);
           u.y = pack_bf16x2(pv[2], pv[3]);
           u.z = pack_bf16x2(pv[4], pv[5]);
           u.w = pack_bf16x2(pv[6], pv[7]);
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, ch)) = u;
+          *reinterpret_cast<uint4*>(prow + sw128_offset(r, slice * (KW / 8) + cc)) = u;
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.pfull[sb]);
       }
-      // ---- the (b, h) is complete: O / l out, then release O for the next (b, h)
+      // ---- the (b, h) is complete: O / l out (the warps of copy 0), then release O
+      S.xl[warp][lane] = l;
+      named_barrier(4, 128);
       wait_or_abort(S, &S.ofinal, nq & 1, bt.err);
       tc_fence_after();
-      if (warp_rows) {
-        const float inv = 1.f / l;
+      if (slice == 0) {
+        float lt = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q % RQ == rb) lt += S.xl[q][lane];
+        const float inv = 1.f / lt;
         const size_t orow = (static_cast<size_t>(sm.cus + sm.sb + r) * H + h);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -380,8 +402,9 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
             }
           }
         }
-        if (row_ok && a.lse != nullptr) a.lse[orow] = (m_ref + log2f(l)) * kLn2;
+        if (row_ok && a.lse != nullptr) a.lse[orow] = (m_ref + log2f(lt)) * kLn2;
       }
+      named_barrier(4, 128);  // xl is read before the next (b, h) writes it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.oempty);
@@ -390,7 +413,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -398,7 +421,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
-    const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_qb, const __grid_constant__ CUtensorMap tm_qb64,
+    const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q,
     const __grid_constant__ CUtensorMap tm_o, const AttnArgs a, int n_block_ctas, int n_merge_ctas) {
   using C = StreamCfg<D>;
@@ -460,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     const long long BH = static_cast<long long>(bt.batch) * H;
     const long long G = BH < n_role ? BH : n_role;
     if (c >= G) return;  // uniform across the CTA
-    block_role_tc<D>(S, smem, tm_qb, tm_k, tm_v, a, c, G);
+    block_role_tc<D>(S, smem, tm_qb, tm_qb64, tm_k, tm_v, a, c, G);
     return;
   }
   const long long G = U < n_role ? U : n_role;
@@ -499,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     }
     return;
   }
+  if (warp == 9) return;  // not used by the merge role
   // ------------------------------------------------ merge compute (2 groups of 4 warps)
   const int grp = warp >> 2, mw = warp & 3;
   const int g = lane >> 2, t = lane & 3;
@@ -598,18 +623,21 @@ cudaError_t launch_d(const AttnArgs& a, const AttnPlan& plan, cudaStream_t strea
   cudaError_t e = encode_pool_maps(a, merge, merge, &m);
   if (e != cudaSuccess) return e;
   if (!merge) m.q = m.k, m.o = m.k;  // unused without the merge role
-  CUtensorMap tm_qb = m.k;
+  CUtensorMap tm_qb = m.k, tm_qb64 = m.k;  // the block queries in boxes of 32 and of 64 rows
   if (block) {
     e = encode_3d_rows_sw128(&tm_qb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_block, D, a.n_heads,
-                             a.bt.total_block_rows, 64, 128);
+                             a.bt.total_block_rows, 64, 32);
+    if (e == cudaSuccess)
+      e = encode_3d_rows_sw128(&tm_qb64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_block, D, a.n_heads,
+                               a.bt.total_block_rows, 64, 64);
     if (e != cudaSuccess) return e;
   }
   constexpr int smem = StreamCfg<D>::kSmem;
   auto kern = attn_stream_kernel<D>;
   e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(plan.n_block_ctas + plan.n_merge_ctas), kThreads, smem, 0, stream, tm_qb, m.k, m.v,
-                    m.q, m.o, a, plan.n_block_ctas, plan.n_merge_ctas);
+  return launch_pdl(kern, dim3(plan.n_block_ctas + plan.n_merge_ctas), kThreads, smem, 0, stream, tm_qb, tm_qb64,
+                    m.k, m.v, m.q, m.o, a, plan.n_block_ctas, plan.n_merge_ctas);
 }
 
 
