@@ -129,19 +129,29 @@ QkvArgs qkv_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cache
   a.d_model = d->d_model;
   a.n_tok = n_tok;
   a.mode = mode;
+  a.x = nullptr;
+  a.gain = nullptr;
+  a.rms_eps = d->rms_eps;
+  a.xhat = nullptr;
+  a.inv = nullptr;
+  a.norm_ctr = nullptr;
   a.partials = nullptr;
   a.counters = nullptr;
   a.max_contrib = 0;
   return a;
 }
 
-// Point the projection at its workspace: x^ first, then (stream-K) the fp32
-// partial tiles and the arrival counters the RMSNorm kernel zeroes.
+// Point the projection at its workspace: the counters (RMSNorm row claims,
+// then the stream-K tile arrivals), the per-row RMSNorm scales, the x^ rows,
+// and (stream-K) the fp32 partial tiles.
 void bind_workspace(QkvArgs* a, const QkvPlan& plan, void* ws) {
-  if (!plan.streamk) return;
   uint8_t* base = static_cast<uint8_t*>(ws);
+  a->norm_ctr = reinterpret_cast<int32_t*>(base);
+  a->inv = reinterpret_cast<float2*>(base + plan.inv_offset);
+  a->xhat = base + plan.xhat_offset;
+  if (!plan.streamk) return;
+  a->counters = reinterpret_cast<int32_t*>(base) + kQkvNormCounters;
   a->partials = reinterpret_cast<float*>(base + plan.part_offset);
-  a->counters = reinterpret_cast<int32_t*>(base + plan.counter_offset);
   a->max_contrib = plan.max_contrib;
 }
 
@@ -240,11 +250,11 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   const BatchArgs bt = batch_args(batch, cache);
   const QkvPlan plan = qkv_plan(batch->total_seq_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms());
   QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBoundary, batch->total_seq_rows);
+  qa.x = x_full;
+  qa.gain = rms_gain;
   bind_workspace(&qa, plan, ws);
   DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
-  DLLM_CUDA_TRY(launch_rmsnorm(x_full, rms_gain, ws, batch->total_seq_rows, desc->d_model, desc->rms_eps, qa.counters,
-                               plan.n_counters, s));
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, ws, qa, plan, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, qa, plan, s));
   const AttnArgs aa = attn_args(desc, batch, cache);
   DLLM_CUDA_TRY(launch_state_build(aa, s));
   return DLLM_OK;
@@ -271,10 +281,10 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
   const QkvPlan plan = qkv_plan(batch->total_block_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms());
   QkvArgs qa = qkv_args(desc, batch, cache, rope_table, rope_max_pos, kModeBlock, batch->total_block_rows);
   qa.q_block = q_block;
+  qa.x = x_block;
+  qa.gain = rms_gain;
   bind_workspace(&qa, plan, ws);
-  DLLM_CUDA_TRY(launch_rmsnorm(x_block, rms_gain, ws, batch->total_block_rows, desc->d_model, desc->rms_eps,
-                               qa.counters, plan.n_counters, s));
-  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, ws, qa, plan, s));
+  DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, qa, plan, s));
   return DLLM_OK;
 }
 

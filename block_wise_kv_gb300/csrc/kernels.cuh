@@ -41,10 +41,19 @@ struct QkvArgs {
   int32_t n_heads;
   int32_t head_dim;
   int32_t d_model;
-  int32_t n_tok;               // rows of the x^ operand
+  int32_t n_tok;               // rows of x
   int32_t mode;                // kModeBlock or kModeBoundary
+  // RMSNorm: input rows, gain, epsilon; in the workspace the normalised rows
+  // x^, the per-row scale pairs and the counters of the row claims (claimed,
+  // published, CTAs done)
+  const void* x;               // bf16 [n_tok][d_model]
+  const void* gain;            // bf16 [d_model]
+  float rms_eps;
+  void* xhat;                  // bf16 [n_tok][d_model]
+  float2* inv;                 // [n_tok] (hi, lo) of 1 / sqrt(mean(x^2) + eps)
+  int32_t* norm_ctr;           // [3]; zero before the call, zero again after it
   // stream-K schedule (n_tok <= 64): fp32 partial tiles and per-tile arrival
-  // counters in the workspace; the counters are zeroed by the RMSNorm kernel
+  // counters in the workspace; the last contributor of a tile zeroes its counter
   float* partials;             // null: one CTA per (weight tile, token tile)
   int32_t* counters;
   int32_t max_contrib;         // partial slots per weight tile
@@ -61,14 +70,22 @@ inline size_t qkv_packed_bytes(int d_model, int n_heads, int head_dim) {
 }
 cudaError_t launch_qkv_pack(const void* w, void* packed, int rows, int d_model, cudaStream_t stream);
 
-// Workspace layout and schedule of the fused projection for n_tok rows.
+// Workspace layout and schedule of the fused projection for n_tok rows:
+// [counters: 1 KB][row scales: n_tok (hi, lo) pairs][x^: n_tok bf16 rows]
+// [stream-K partials].  The
+// counters (3 for the RMSNorm row claims, then one per weight tile) sit in a
+// region of fixed size at the start, so calls of different shapes sharing a
+// workspace never find another call's partials there; they are zero before
+// and after every call.
+constexpr size_t kQkvCounterBytes = 1024;
+constexpr int kQkvNormCounters = 4;  // 3 used, the 4th keeps the tile counters 16-byte aligned
+constexpr int kQkvMaxTileCounters = static_cast<int>(kQkvCounterBytes / 4) - kQkvNormCounters;
 struct QkvPlan {
   int bn;            // token tile (32, 64 or 128)
   bool streamk;      // stream-K over (weight tile, k-unit) units, else one CTA per (weight tile, token tile)
   int grid;          // CTAs of the stream-K schedule
   int max_contrib;   // stream-K: most CTAs sharing one weight tile
-  int n_counters;    // arrival counters (one per weight tile) to zero before the projection
-  size_t xhat_bytes, part_offset, part_bytes, counter_offset, counter_bytes, total_bytes;
+  size_t inv_offset, inv_bytes, xhat_offset, xhat_bytes, part_offset, part_bytes, total_bytes;
 };
 QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms);
 constexpr int kModeBlock = 0;     // tokens are the packed block rows (cu_block)
@@ -102,13 +119,10 @@ bool attn_batch_supported(int batch);
 
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
 // Each launcher encodes the TMA tensor maps it needs from the raw pointers.
-cudaError_t launch_rmsnorm(const void* x, const void* gain, void* out, int rows, int d_model, float eps,
-                           int32_t* zero, int zero_count, cudaStream_t stream);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double theta, cudaStream_t stream);
 cudaError_t launch_zero_tails(const BatchArgs& bt, void* k_pool, void* v_pool, void* q_pool, int n_heads,
                               int head_dim, cudaStream_t stream);
-cudaError_t launch_qkv_gemm(const void* w_packed, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
-                            cudaStream_t stream);
+cudaError_t launch_qkv_gemm(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream);
 // The block attention (LaCache Eq. (2)-(6) over all keys of each block row)
 // and/or the FACache merge of every invariant row, as planned by attn_plan.
 cudaError_t launch_step_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);

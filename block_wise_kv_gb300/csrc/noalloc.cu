@@ -17,18 +17,18 @@
 // so the first call on a device should come before any stream capture.
 //
 // All calls share the array and it keeps the last call's contents.  A call
-// writes every scratch byte before it reads it (the normalised rows, the
-// partial tiles), and the arrival counters that must start at zero are
-// zeroed by the call's own first kernel, so nothing needs clearing between
-// calls; but two calls whose GPU work overlaps (different streams, no
-// ordering between them) race on the array.
+// writes every scale and partial tile before it reads it, and the counters
+// at the start of the array (zero when the library is loaded) are set back
+// to zero by every call, so nothing needs clearing between calls; but two
+// calls whose GPU work overlaps (different streams, no ordering between
+// them) race on the array.
 #include <mutex>
 
 #include "dllm.h"
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t{8} << 20;  // 8 MiB: the x^ rows plus the stream-K partial tiles
+constexpr size_t kNoAllocScratchBytes = size_t{8} << 20;  // 8 MiB: counters, row scales, stream-K partial tiles
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -1,15 +1,17 @@
-// qkv_gemm.cu — fused QKV projection + RoPE + single cache write (sm_103a).
+// qkv_gemm.cu — fused RMSNorm + QKV projection + RoPE + single cache write
+// (sm_103a), one kernel.
 //
-// Computes, for a set of token rows t with normalised input x^_t (bf16, the
-// output of the RMSNorm kernel), y_t = W_qkv x^_t with fp32 accumulation,
-// rotates the q and k parts (RoPE, rotate-half pairs (i, i + d/2) at the
-// token's absolute position) and writes q, k, v once, as bf16, to their
-// destinations: k, v into the paged pools through the block table, q into
-// q_block (inner step) or q_pool (block boundary).  This is the Flash-Cache
-// fusion of the Flash-dLLM write-up ("Flash-Cache: Fusing Projection, RoPE,
-// and Cache Writes into One Kernel": projection and RoPE on chip, keys and
-// values written straight into the cache in one HBM write) applied to the
-// token-wise operators of LaCache §3.3.2, Eq. (1).
+// Computes, for a set of token rows t (bf16 x_t), the normalised row
+// x^_t = x_t / sqrt(mean(x_t^2) + eps) * g correctly rounded to bf16,
+// y_t = W_qkv x^_t with fp32 accumulation, rotates the q and k parts (RoPE,
+// rotate-half pairs (i, i + d/2) at the token's absolute position) and
+// writes q, k, v once, as bf16, to their destinations: k, v into the paged
+// pools through the block table, q into q_block (inner step) or q_pool
+// (block boundary).  This is the Flash-Cache fusion of the Flash-dLLM
+// write-up ("Flash-Cache: Fusing Projection, RoPE, and Cache Writes into One
+// Kernel": projection and RoPE on chip, keys and values written straight
+// into the cache in one HBM write) applied to the token-wise operators of
+// LaCache §3.3.2, Eq. (1), with the RMSNorm in the same kernel.
 //
 // GB300 design.
 //  * Swap-AB: the 128-row weight tiles are the tcgen05 M operand and the
@@ -41,10 +43,23 @@
 //    kernel stores is a cache entry that later steps reuse.  All 512 TMEM
 //    columns serve as partial buffers, so the tensor core can run far ahead
 //    while the accumulator warps finish a tile.
+//  * RMSNorm inside the kernel.  A row's scale needs the whole row, and every
+//    CTA multiplies all of its token rows, so each row is normalised once
+//    for all CTAs: the accumulator warps claim rows through a counter in the
+//    workspace (one atomic per claim), and a claiming warp reads the row,
+//    forms its exact sum of squares and scale (float pairs), writes the
+//    correctly rounded bf16 x^ row to the workspace and publishes it.  The
+//    TMA producer waits until every row is published before it loads x^
+//    tiles.  It waits only after all rows have been claimed (its own CTA's
+//    warps claim until none is left) and a claimed row belongs to a running
+//    warp that publishes it without waiting on anything, so the wait ends
+//    whatever the number of resident CTAs.  The last CTA done with the
+//    counters sets them back to zero.
 //  * Programmatic dependent launch: the weight tiles (constants) of the first
-//    ring stages are requested before waiting for the preceding kernel (the
-//    RMSNorm that produces x^), so the weight stream overlaps it.
+//    ring stages are requested before waiting for the preceding kernel (which
+//    may produce x), so the weight stream overlaps that kernel's tail.
 #include "kernels.cuh"
+#include "norm.cuh"
 #include "sm103.cuh"
 #include "tmap.cuh"
 
@@ -172,6 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[kTmemBufs], tempty_bar[kTmemBufs];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int last_sh;
+  __shared__ int claim_sh[2];         // RMSNorm: the claimed row (slots alternate between rows)
+  __shared__ float2 red_sh[2][kAccThreads / 32], scale_sh[2];
   __shared__ long long tok_kv[BN];  // element offset of (page, head 0, slot) in the pools, -1: no write
   __shared__ long long tok_q[BN];   // element offset of the q destination for head 0, -1: no write
   __shared__ int tok_pos[BN];       // absolute position (RoPE)
@@ -217,17 +234,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
 
   if (warp == 0) {
+    // ---- TMA producer.  Weight tiles of the first stages go out before the
+    // dependency wait (weights are constants); x^ tiles only once every row
+    // has been normalised and published.
+    const int npre = n_units < kStages ? n_units : kStages;
+    UnitWalk w;
+    w.init(u0, u1, nkb);
     if (lane == 0) {
-      // ---- TMA producer.  Weight tiles of the first stages go out before the
-      // dependency wait (weights are constants); x^ tiles only after it.
-      const int npre = n_units < kStages ? n_units : kStages;
-      UnitWalk w;
-      w.init(u0, u1, nkb);
       for (int i = 0; i < npre; ++i, w.next()) {
         mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
         tma_load_2d(smem + i * kStageBytes, &tm_w, &full_bar[i], 0, (w.tile * kbp + kBoxes * w.kb) * kTileM);
       }
       griddep_wait();
+      const uint64_t t0 = global_timer_ns();  // bounded wait for the x^ rows
+      while (ld_acquire_gpu(a.norm_ctr + 1) < a.n_tok) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          report_error(bt.err, kErrTimeout);
+          break;
+        }
+        __nanosleep(100);
+      }
+      fence_proxy_async_global();  // the rows written by other CTAs' threads, as seen by TMA
+    }
+    __syncwarp();
+    named_barrier_arrive(2, 32 + kAccThreads);  // this CTA no longer reads the claim counters
+    named_barrier(3, 32 + kAccThreads);         // this CTA's RMSNorm staging areas are free for x^ tiles
+    if (lane == 0) {
       {
         UnitWalk wb;
         wb.init(u0, u1, nkb);
@@ -307,9 +339,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---- accumulator warps (TMEM lane quarter = warp % 4)
-    griddep_wait();
     const int H = a.n_heads, d = a.head_dim, half = d >> 1;
     const int HD = H * d;
+    // RMSNorm: the CTA's accumulator warps claim one row at a time until none
+    // is left.  Until the producer loads x^ tiles, the x^ areas of ring
+    // stages 0 and 1 are free: the row and the gain are staged there, each
+    // thread in its own 16-byte slots (vectors at + 128 j), so the code is a
+    // few short loops (this runs once per launch, from a cold instruction
+    // cache).
+    {
+      const int at = threadIdx.x - 64;
+      const uint4* xg = static_cast<const uint4*>(a.x);
+      const uint4* gg = static_cast<const uint4*>(a.gain);
+      uint4* xh = static_cast<uint4*>(a.xhat);
+      const int nvec = a.d_model / 8;
+      constexpr int kCap = kBoxes * kTileBBytes / 16;  // 16-byte vectors in one stage's x^ area
+      uint4* rowbuf = reinterpret_cast<uint4*>(smem + kBoxes * kTileABytes);
+      uint4* gainbuf = reinterpret_cast<uint4*>(smem + kStageBytes + kBoxes * kTileABytes);
+      const bool staged = nvec <= kCap;  // the row fits: one load pass, the gain kept in shared memory
+      if (staged)  // the gain is a layer constant: read before the dependency wait
+        for (int v = at; v < nvec; v += kAccThreads) gainbuf[v] = __ldg(gg + v);
+      // Iteration -1 runs the row code on zeros, with no loads, stores or
+      // atomics, before the dependency wait: it brings the code into the
+      // instruction cache while the preceding kernel finishes (the start
+      // value comes through asm so that the compiler keeps one copy of the
+      // loop body).
+      int it0;
+      asm volatile("mov.b32 %0, -1;" : "=r"(it0));
+      for (int it = it0;; ++it) {
+        const bool warm = it < 0;
+        const int par = it & 1;  // the shared slots alternate between consecutive rows
+        if (at == 0) claim_sh[par] = warm ? 0 : atomicAdd(a.norm_ctr, 1);
+        named_barrier(1, kAccThreads);
+        const int r = claim_sh[par];
+        if (r >= a.n_tok) break;
+        const uint4* xr = xg + static_cast<size_t>(r) * nvec;
+        uint4* hr = xh + static_cast<size_t>(r) * nvec;
+        float hi = 0.f, lo = 0.f;
+        for (int c0 = 0; c0 < nvec; c0 += kCap) {  // exact sum of squares, a staged chunk at a time
+          const int n = min(kCap, nvec - c0);
+#pragma unroll 4
+          for (int v = at; v < n; v += kAccThreads)
+            rowbuf[v] = warm ? make_uint4(0, 0, 0, 0) : __ldg(xr + c0 + v);
+#pragma unroll 1
+          for (int v = at; v < n; v += kAccThreads) sumsq_pair_add(rowbuf[v], hi, lo);
+        }
+#pragma unroll 1
+        for (int o = 16; o > 0; o >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, hi, o), ol = __shfl_xor_sync(0xffffffffu, lo, o);
+          pair_add(hi, lo, oh, ol);
+        }
+        if (lane == 0) red_sh[par][warp - 2] = make_float2(hi, lo);
+        named_barrier(1, kAccThreads);
+        if (at == 0) {  // the four warps' sums in a fixed order, then the scale
+          float ss_hi = red_sh[par][0].x, ss_lo = red_sh[par][0].y;
+#pragma unroll 1
+          for (int q = 1; q < kAccThreads / 32; ++q) pair_add(ss_hi, ss_lo, red_sh[par][q].x, red_sh[par][q].y);
+          two_sum(ss_hi, ss_lo, ss_hi, ss_lo);
+          float y_hi, y_lo;
+          rsqrt_pair(ss_hi, ss_lo, a.d_model, a.rms_eps, y_hi, y_lo);
+          scale_sh[par] = make_float2(y_hi, y_lo);
+          if (!warm) a.inv[r] = make_float2(y_hi, y_lo);
+        }
+        named_barrier(1, kAccThreads);
+        const float2 y = scale_sh[par];
+#pragma unroll 1
+        for (int v = at; v < nvec; v += kAccThreads) {  // x^, correctly rounded
+          const uint4 xv = staged ? rowbuf[v] : (warm ? make_uint4(0, 0, 0, 0) : __ldg(xr + v));
+          const uint4 gvv = staged ? gainbuf[v] : __ldg(gg + v);
+          const uint4 o = normalise8(xv, gvv, y.x, y.y);
+          if (!warm) hr[v] = o;
+        }
+        fence_proxy_async_global();  // the row will be read by TMA
+        named_barrier(1, kAccThreads);
+        if (warm) {
+          griddep_wait();  // from here on x may be read
+          continue;
+        }
+        if (at == 0) {
+          __threadfence();  // the whole row and its scale are visible GPU-wide before they are counted
+          atomicAdd(a.norm_ctr + 1, 1);
+        }
+      }
+      // the staging areas are about to be written by TMA (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      named_barrier_arrive(3, 32 + kAccThreads);
+    }
     for (int c = threadIdx.x - 64; c < BN; c += kAccThreads) {  // resolve token columns
       long long kv = -1, qd = -1;
       int pos = 0;
@@ -341,6 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tok_kv[c] = kv;
       tok_q[c] = qd;
       tok_pos[c] = kv >= 0 ? pos : 0;  // a checked position (the RoPE table is read for every column)
+    }
+    // Once this CTA's producer has seen every row published (and its own
+    // warps have stopped claiming), the CTA is done with the claim counters;
+    // the last CTA to get there zeroes them for the next call.
+    named_barrier(2, 32 + kAccThreads);
+    if (threadIdx.x == 64) {
+      const int n_cta = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+      if (atomicAdd(a.norm_ctr + 2, 1) == n_cta - 1) {
+        a.norm_ctr[0] = 0;
+        a.norm_ctr[1] = 0;
+        a.norm_ctr[2] = 0;
+      }
     }
     named_barrier(1, kAccThreads);
 
@@ -524,8 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN>
-cudaError_t launch_bn(const void* w_packed, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
-                      cudaStream_t stream) {
+cudaError_t launch_bn(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream) {
   const int HD = a.n_heads * a.head_dim;
   CUtensorMap tm_w, tm_x;
   // the packed weight as rows of 64 columns; one load = the two boxes of a unit
@@ -533,7 +659,7 @@ cudaError_t launch_bn(const void* w_packed, const void* xhat, const QkvArgs& a, 
   cudaError_t e = encode_2d_sw128(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_packed, kTileK, w_rows, kTileK,
                                   kBoxes * kTileM);
   if (e != cudaSuccess) return e;
-  e = encode_2d_sw128(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xhat, a.d_model, a.n_tok, kTileK, BN);
+  e = encode_2d_sw128(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.xhat, a.d_model, a.n_tok, kTileK, BN);
   if (e != cudaSuccess) return e;
   auto kern = qkv_gemm_kernel<BN>;
   constexpr int smem = gemm_smem_bytes<BN>();
@@ -562,9 +688,12 @@ QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms)
   const long long n_wt = 3LL * n_heads * head_dim / kTileM;
   const long long nkb = (d_model + kUnitK - 1) / kUnitK;
   p.bn = n_tok <= 32 ? 32 : (n_tok <= 64 ? 64 : 128);
+  p.streamk = p.bn <= 64 && 2 * n_wt <= num_sms && n_wt <= kQkvMaxTileCounters;
+  p.inv_offset = kQkvCounterBytes;
+  p.inv_bytes = align256(static_cast<size_t>(n_tok) * 8);
+  p.xhat_offset = p.inv_offset + p.inv_bytes;
   p.xhat_bytes = align256(static_cast<size_t>(n_tok) * d_model * 2);
-  p.streamk = p.bn <= 64 && 2 * n_wt <= num_sms;
-  p.part_offset = p.counter_offset = p.xhat_bytes;
+  p.part_offset = p.xhat_offset + p.xhat_bytes;
   if (p.streamk) {
     const long long U = n_wt * nkb;
     long long G = U / kMinUnitsPerCta;
@@ -577,21 +706,17 @@ QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms)
       if (c > maxc) maxc = c;
     }
     p.max_contrib = maxc;
-    p.n_counters = static_cast<int>(n_wt);
     p.part_bytes = align256(static_cast<size_t>(n_wt) * maxc * kTileM * p.bn * 4);
-    p.counter_offset = p.part_offset + p.part_bytes;
-    p.counter_bytes = align256(static_cast<size_t>(n_wt) * 4);
   }
-  p.total_bytes = p.counter_offset + p.counter_bytes;
+  p.total_bytes = p.part_offset + p.part_bytes;
   return p;
 }
 
-cudaError_t launch_qkv_gemm(const void* w_packed, const void* xhat, const QkvArgs& a, const QkvPlan& plan,
-                            cudaStream_t stream) {
+cudaError_t launch_qkv_gemm(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream) {
   if (a.n_tok <= 0) return cudaSuccess;
-  if (plan.bn == 32) return launch_bn<32>(w_packed, xhat, a, plan, stream);
-  if (plan.bn == 64) return launch_bn<64>(w_packed, xhat, a, plan, stream);
-  return launch_bn<128>(w_packed, xhat, a, plan, stream);
+  if (plan.bn == 32) return launch_bn<32>(w_packed, a, plan, stream);
+  if (plan.bn == 64) return launch_bn<64>(w_packed, a, plan, stream);
+  return launch_bn<128>(w_packed, a, plan, stream);
 }
 
 namespace {

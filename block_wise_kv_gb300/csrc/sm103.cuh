@@ -322,6 +322,19 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrive at a named barrier without waiting (the waiting side uses named_barrier).
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Order this thread's generic-proxy global writes with async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // ------------------------------------------------------ warp-level MMA -----
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)

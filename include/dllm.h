@@ -53,7 +53,11 @@
  *     not write those.  dllm_block_qkv_rope_write writes only q_block and the
  *     current blocks' k/v rows, so the step's own order (projection, then
  *     attention) meets this.  q_block and the current blocks' k/v pages are
- *     read only after the preceding kernel has completed.
+ *     read only after the preceding kernel has completed.  The projection
+ *     calls (dllm_cache_build, dllm_block_qkv_rope_write) may read w_packed
+ *     and rms_gain before the preceding kernel has finished; that kernel
+ *     must not write them.  Everything else they read or write is touched
+ *     only after the preceding kernel has completed.
  *
  * Layouts (all row-major, little-endian, bf16 = IEEE bfloat16)
  *   page      = 64 consecutive token positions of one sequence.
@@ -175,7 +179,7 @@ dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv,
 
 /* Block boundary (LaCache Algorithm 1 with GenStep = True; Fast-dLLM
  * compute_block_dual_cache).  For every row of every sequence:
- *   x^ = RMSNorm(x) (fp32, rounded to bf16), [q k v] = x^ W_qkv^T (fp32
+ *   x^ = RMSNorm(x) (correctly rounded to bf16), [q k v] = x^ W_qkv^T (fp32
  *   accumulation), RoPE(q, k) at position p, and k, v (and q for rows of U)
  *   written as bf16 into the pools.  Pool positions p >= N_b of each
  *   sequence's last page are set to zero.
@@ -194,13 +198,21 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
                              const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream);
 
 /* Inner step, part 1 (LaCache §3.3.2 Eq. (1); Flash-dLLM Flash-Cache): for
- * the B_b rows of each current block only, x^ = RMSNorm(x_block) rounded to
- * bf16, [q k v] = x^ W_qkv^T with fp32 accumulation, RoPE(q, k) at absolute
- * position p = s_b + i, then one write: k, v as bf16 into k_pool / v_pool at
- * (block_table[b][p/64], h, p%64) and q as bf16 into q_block [M][H][d].
+ * the B_b rows of each current block only, in one kernel: x^ = RMSNorm(x_block)
+ * correctly rounded to bf16, [q k v] = x^ W_qkv^T with fp32 accumulation,
+ * RoPE(q, k) at absolute position p = s_b + i, then one write: k, v as bf16
+ * into k_pool / v_pool at (block_table[b][p/64], h, p%64) and q as bf16 into
+ * q_block [M][H][d].
  *   x_block: device bf16 [M][d_model]; q_block: device bf16 [M][H][d];
  *   w_packed: device, from dllm_qkv_weight_pack;
- *   ws: dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) bytes. */
+ *   ws: dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) bytes, 256-byte
+ *   aligned: 1 KB of counters, one fp32 pair per row (the RMSNorm scale
+ *   1 / sqrt(mean(x^2) + eps) as hi + lo), the bf16 x^ rows [M][d_model]
+ *   (each region 256-byte aligned), then, for small models, the fp32 partial
+ *   tiles of a split schedule.  The counters must be zero before the
+ *   workspace's first use; every call leaves them zero (also after a
+ *   device-side timeout).  The same holds for dllm_cache_build's workspace
+ *   (with R rows). */
 dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_block,
                                       const void* rms_gain, const void* w_packed, const float* rope_table,
                                       int32_t rope_max_pos, const dllm_cache* cache, void* q_block, void* ws,
@@ -215,8 +227,9 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
  * takes no workspace: its scratch is a fixed 8 MiB array in the library's own
  * device memory (held by every GPU that loads the library until exit), so the
  * call's dllm_workspace_size(DLLM_OP_BLOCK_QKV_ROPE_WRITE) must not exceed
- * 8 MiB (about 4.8 MiB for 32 block rows of d_model 4096); a larger batch
- * returns DLLM_ERR_WORKSPACE_TOO_SMALL and launches nothing.  The first call
+ * 8 MiB (about 0.26 MiB for 32 block rows of d_model 4096: mostly the x^
+ * rows); a larger need returns DLLM_ERR_WORKSPACE_TOO_SMALL and launches
+ * nothing.  The first call
  * on each device looks up the array's device address with that device
  * current (make that first call before any stream capture).  All calls share
  * the array: calls whose GPU work may overlap (different streams without

@@ -26,11 +26,15 @@ def _lib():
     torch.cuda.init()
 
 
-def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=True, rows_of=None, seqs=None):
+def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=True, rows_of=None, seqs=None,
+               gain=None):
     """Boundary of the blocks `k_of` (one per sequence) then the given inner
-    steps; every listed sequence is compared with the oracle after each step."""
+    steps; every listed sequence is compared with the oracle after each step.
+    `gain` replaces the workload's RMSNorm gain (all ones)."""
     wl = Workload(cfg)
     W, g = wl.weights(layer)
+    if gain is not None:
+        g = gain
     st = LayerStep(cfg, layer=layer, blocks=k_of, weights=(W, g))
     st.boundary(full_rows_of(wl, layer, 0, k_of).cuda())
     torch.cuda.synchronize()
@@ -79,21 +83,31 @@ def test_tiny_every_block_every_step():
         _run_block(cfg, [k], range(cfg.steps_per_block))
 
 
-def test_rmsnorm_operand_is_correctly_rounded():
-    """The projection's bf16 operand (the step workspace after the call)
-    equals the oracle's x^ rounded to bf16, bit for bit."""
+def test_rmsnorm_rows_and_scales_in_the_workspace():
+    """The fused projection writes, per token row, its RMSNorm scale
+    1 / sqrt(mean(x^2) + eps) as a float pair (hi, lo) and the bf16 operand
+    x^ into its workspace (after the 1 KB of counters): hi + lo equals the
+    fp64 value to ~2^-38, x^ equals the oracle's x^ rounded to bf16 bit for
+    bit, and the claim counters are back at zero."""
     import oracle as orc
 
     cfg = make_config("llada_single")
     wl = Workload(cfg)
     st = LayerStep(cfg)
-    xb = block_rows_of(wl, 0, 3, cfg.block_index)
-    st.qkv(xb.cuda())
-    torch.cuda.synchronize()
-    M, D = xb.shape
-    got = st.ws_step[:M * D * 2].view(torch.bfloat16).view(M, D).double().cpu().numpy()
-    want = orc.bf16_round(orc.rmsnorm(xb.double().numpy(), st.gain.double().cpu().numpy(), cfg.rms_eps))
-    assert np.array_equal(got, want), f"{int((got != want).sum())} elements differ"
+    for step in (3, 4):
+        xb = block_rows_of(wl, 0, step, cfg.block_index)
+        st.qkv(xb.cuda())
+        torch.cuda.synchronize()
+        M, D = xb.shape
+        pairs = st.ws_step[1024:1024 + M * 8].view(torch.float32).view(M, 2).double().cpu().numpy()
+        x = xb.double().numpy()
+        want = 1.0 / np.sqrt((x * x).mean(axis=1) + cfg.rms_eps)
+        assert np.max(np.abs((pairs[:, 0] + pairs[:, 1]) / want - 1.0)) < 2.0 ** -38
+        off = 1024 + 256 * ((M * 8 + 255) // 256)
+        got = st.ws_step[off:off + M * D * 2].view(torch.bfloat16).view(M, D).double().cpu().numpy()
+        xh = orc.bf16_round(orc.rmsnorm(x, st.gain.double().cpu().numpy(), cfg.rms_eps))
+        assert np.array_equal(got, xh), f"{int((got != xh).sum())} elements of x^ differ"
+        assert int(st.ws_step[:1024].view(torch.int32).abs().sum()) == 0, "counters left non-zero"
 
 
 def test_weight_pack_is_the_documented_permutation():
@@ -140,23 +154,49 @@ def test_mini_ragged_head_dim_128():
     _run_block(cfg, cfg.block_index, (1,))
 
 
+def test_rmsnorm_gain_not_one():
+    """A random RMSNorm gain (the workloads use g = 1): the fused projection
+    applies g[k] to the right K position of every swizzled x tile, also in a
+    ragged last K unit (d_model 192 = 1.5 units) and with token tiles of 128,
+    64 and 32 rows."""
+    for name, d_model, H, d, t_prefix, gen_len, block, k_of in (
+            ("gain_ragged_k", 192, 2, 64, [0, 100, 37, 10, 300, 5, 0, 64], [64, 96, 128, 64, 240, 20, 32, 128],
+             [32, 32, 16, 64, 48, 20, 32, 64], [0, 2, 3, 0, 1, 0, 0, 1]),
+            ("gain_bn64", 512, 2, 128, [100, 5], [96, 40], [32, 20], [1, 1]),
+            ("gain_bn32", 1024, 4, 64, [37, 0], [48, 32], [16, 16], [2, 0])):
+        cfg = Config(name, d_model, H, d, 1e4, t_prefix=t_prefix, gen_len=gen_len, block=block, block_index=k_of,
+                     steps_per_block=2)
+        gen = torch.Generator().manual_seed(d_model)
+        gain = (0.5 + torch.rand(d_model, generator=gen)).to(torch.bfloat16)
+        _run_block(cfg, cfg.block_index, (1,), gain=gain)
+
+
 def test_split_stream_k_tiles_and_repeatability():
-    """Few weight tiles (2 heads x 128 -> 6 tiles) with d_model 4096: the
-    projection runs stream-K with every tile split over 8 CTAs, so the fp32
-    partial-tile fixup is exercised; then the same step run again on the same
-    inputs gives bit-identical outputs (fixed summation orders)."""
-    cfg = _mini_ragged(d_model=4096, n_heads=2, head_dim=128, rope_theta=5e5)
-    st = _run_block(cfg, cfg.block_index, (1,))
-    wl = Workload(cfg)
-    xb = block_rows_of(wl, 0, 1, cfg.block_index).cuda()
-    first = (st.o_full.clone(), st.lse.clone(), st.q_block.clone(), st.cache.k.clone(), st.cache.v.clone())
-    for _ in range(3):
-        st.step(xb)
-        torch.cuda.synchronize()
-        again = (st.o_full, st.lse, st.q_block, st.cache.k, st.cache.v)
-        for x, y in zip(first, again):
-            iv = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
-            assert torch.equal(x.view(iv), y.view(iv))
+    """Few weight tiles (2 heads x 128 -> 6 tiles) with d_model 4096 and at
+    most 64 block rows: the projection splits each tile's K range over
+    several CTAs (fp32 partial tiles summed by the last contributor), with
+    token tiles of 64 and of 32 rows; the results
+    match the oracle, and the same step run again on the same inputs gives
+    bit-identical outputs (fixed summation orders)."""
+    for name, t_prefix, gen_len, block, k_of in (("split64", [100, 5], [96, 40], [32, 20], [1, 1]),
+                                                  ("split32", [37, 0], [48, 32], [16, 16], [2, 0])):
+        cfg = Config(name, 4096, 2, 128, 5e5, t_prefix=t_prefix, gen_len=gen_len, block=block, block_index=k_of,
+                     steps_per_block=2)
+        st = _run_block(cfg, cfg.block_index, (1,))
+        M = sum(block)
+        plain = 1024 + 256 * ((M * 8 + 255) // 256) + 256 * ((M * 4096 * 2 + 255) // 256)
+        assert st.ws_step.numel() > plain, "expected the split schedule (partials)"
+        wl = Workload(cfg)
+        xb = block_rows_of(wl, 0, 1, cfg.block_index).cuda()
+        first = (st.o_full.clone(), st.lse.clone(), st.q_block.clone(), st.cache.k.clone(), st.cache.v.clone())
+        for _ in range(3):
+            st.step(xb)
+            torch.cuda.synchronize()
+            again = (st.o_full, st.lse, st.q_block, st.cache.k, st.cache.v)
+            for x, y in zip(first, again):
+                iv = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
+                assert torch.equal(x.view(iv), y.view(iv)), name
+        assert int(st.ws_step[:1024].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
 
 
 def test_placement_is_bit_exact_and_sentinels_survive():
