@@ -48,7 +48,7 @@ struct StreamCfg {
   static constexpr int PB = 128 * 128;  // 128 rows x 64 keys bf16
   static constexpr int kBlockSmem = off_p + 2 * PB;
   // merge role: query page | O~ page | m | l ring, then the gathered block keys / values
-  static constexpr int kMStages = 2;
+  static constexpr int kMStages = 3;
   static constexpr int MStage = TB + OB + 1024;
   static constexpr int off_kc = kMStages * MStage;
   static constexpr int off_vc = off_kc + TB;
