@@ -146,6 +146,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one projection
+# launch, per workload, from one ncu capture of the kernel as it stands
+# (--set full, the launch of an inner step); no entry: not captured.
+QKV_TRAFFIC_BYTES = {"llada_single": 104_140_032}
+
+
 def step_bytes_flops(cfg, st):
     """Algorithmic bytes and flops of one layer-step (what the method must
     move and compute), per part."""
@@ -362,7 +368,7 @@ def run_ours(args, rank, ws, local):
         "roofline": {"kernel": "dllm_block_qkv_rope_write (one kernel: RMSNorm, tcgen05 QKV GEMM, RoPE and the "
                                "paged K/V write)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": QKV_TRAFFIC_BYTES.get(cfg.name),
                      "algorithmic_bytes": qkv_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(Ke * M * ws / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
