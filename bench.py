@@ -14,11 +14,12 @@ Workload: the LLaDA-8B-shaped single layer (batch 1, d_model 4096, 32 heads
 x 128, RoPE theta 5e5, prompt 512, gen 256, block 32), synthetic seeded
 bf16 inputs and N(0, 0.02) weights.  Steps rotate over several independent
 layer instances (about 140 MB each), so no step finds its inputs in the
-129 MB L2.  The steps replay CUDA graphs (two kernels a step: the fused
-RMSNorm + projection + RoPE + K/V write, and the block attention + FACache
-merge launch); a sample of the steps (one round in 32) carries CUDA events
-around the projection call on its stream, which give its live duration for
-the roofline.
+129 MB L2.  The steps replay CUDA graphs of 32 layer-steps (8 rounds of the
+4 instances, as one forward over 32 layers would be; two kernels a step: the
+fused RMSNorm + projection + RoPE + K/V write, and the block attention +
+FACache merge launch); a sample of the steps (one round in 32) carries CUDA
+events around the projection call on its stream, which give its live
+duration for the roofline.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (sequences are independent units: weak scaling, no collective on the data
@@ -213,11 +214,14 @@ def run_ours(args, rank, ws, local):
 
     # CUDA graphs.  A round is one step of every instance (L steps: the
     # projection call, then the block attention and the FACache merge in one
-    # launch), so consecutive kernels keep their programmatic-dependent-launch
-    # overlap.
-    # Every `sample_every`-th round replays per-instance pieces instead, with
-    # CUDA events around the projection call on its stream: those give the
-    # projection's live duration for the roofline, inside the timed region.
+    # launch); a pass is P rounds in one graph (P L layer-steps, as one
+    # forward over the layers of a model would be), so consecutive kernels
+    # keep their programmatic-dependent-launch overlap.  In every
+    # `sample_every`-th pass the first round replays per-instance pieces
+    # instead, with CUDA events around the projection call on its stream:
+    # those give the projection's live duration for the roofline, inside the
+    # timed region.
+    P = max(1, args.rounds_per_graph)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for st, xb in inst:
@@ -227,6 +231,11 @@ def run_ours(args, rank, ws, local):
         with torch.cuda.graph(g_round, stream=stream):
             for st, xb in inst:
                 st.step(xb, stream=stream)
+        g_pass = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_pass, stream=stream):
+            for _ in range(P):
+                for st, xb in inst:
+                    st.step(xb, stream=stream)
         g_step, g_qkv, g_rest = [], [], []  # one step; the projection call; the attention call
         for st, xb in inst:
             g = torch.cuda.CUDAGraph()
@@ -249,6 +258,7 @@ def run_ours(args, rank, ws, local):
         g_step[i % L].replay()
     torch.cuda.synchronize()
     n_rounds, tail = divmod(K, L)
+    n_passes, tail_rounds = divmod(n_rounds, P)
     qkv_ev = []
     _barrier(ws)
     torch.cuda.synchronize()
@@ -256,8 +266,8 @@ def run_ours(args, rank, ws, local):
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         t_start.record(stream)
-        for r in range(n_rounds):
-            if r % sample_every == sample_every - 1:
+        for k in range(n_passes):
+            if k % sample_every == sample_every - 1:
                 for j in range(L):
                     e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                     e[0].record(stream)
@@ -266,8 +276,12 @@ def run_ours(args, rank, ws, local):
                     g_rest[j].replay()
                     e[2].record(stream)
                     qkv_ev.append(e)
+                for _ in range(P - 1):
+                    g_round.replay()
             else:
-                g_round.replay()
+                g_pass.replay()
+        for _ in range(tail_rounds):
+            g_round.replay()
         for j in range(tail):
             g_step[j].replay()
         t_end.record(stream)
@@ -357,8 +371,9 @@ def run_ours(args, rank, ws, local):
         "data": "synthetic",
         "config": {"workload": describe(cfg),
                    "l2": f"inputs larger than L2: {L} rotating layer instances (~140 MB each)",
-                   "graphs": f"one CUDA graph per round of {L} steps; every {sample_every}th round replayed "
-                             "per call with events around the projection",
+                   "graphs": f"one CUDA graph per pass of {P} rounds x {L} steps ({P * L} layer-steps); the first "
+                             f"round of every {sample_every}th pass replayed per call with events around the "
+                             "projection",
                    "parallelism": f"replicas x{ws} (sequences are independent units)"},
         "qkv_rope_write_us": round(qkv_ms * 1e3, 2),
         "step_attention_us": round(attn_ms * 1e3, 2),
@@ -467,8 +482,10 @@ def main(argv=None):
     ap.add_argument("--config", default=WORKLOAD)
     ap.add_argument("--layers", type=int, default=4, help="rotating layer instances (inputs larger than L2)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
-    ap.add_argument("--sample-every", type=int, default=32,
-                    help="every n-th round of steps carries events around the projection call")
+    ap.add_argument("--rounds-per-graph", type=int, default=8,
+                    help="rounds of steps (one step of every layer instance each) captured in one graph")
+    ap.add_argument("--sample-every", type=int, default=4,
+                    help="the first round of every n-th pass carries events around the projection call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
