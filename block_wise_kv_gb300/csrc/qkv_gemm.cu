@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kbp = 2 * nkb;                            // packed boxes per weight tile
   const int n_wt = 3 * a.n_heads * a.head_dim / kTileM;
   const bool streamk = a.partials != nullptr;
-  const int nt = streamk ? 0 : static_cast<int>(blockIdx.z);
+  const int nt = streamk ? 0 : static_cast<int>(blockIdx.x);  // token tile (x: the tiles of one weight tile
+                                                               // run side by side and share it in L2)
   const long long U = static_cast<long long>(n_wt) * nkb, G = gridDim.x;
   long long u0, u1;  // unit range of this CTA
   if (streamk) {
@@ -669,7 +670,7 @@ cudaError_t launch_bn(const void* w_packed, const QkvArgs& a, const QkvPlan& pla
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   const int n_wt = 3 * HD / kTileM;
-  cfg.gridDim = plan.streamk ? dim3(plan.grid, 1, 1) : dim3(1, n_wt, (a.n_tok + BN - 1) / BN);
+  cfg.gridDim = plan.streamk ? dim3(plan.grid, 1, 1) : dim3((a.n_tok + BN - 1) / BN, n_wt, 1);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
