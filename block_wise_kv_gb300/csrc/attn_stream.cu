@@ -335,7 +335,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           if (slice == 0) {  // O's rows of this row block live in this warp's quadrant
             wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);  // O holds pages 0 .. j-1
             tc_fence_after();
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               float ov[32];
               tmem_ld_32x32b_x32(lane_base + c0, ov);
@@ -385,7 +385,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           if (q % RQ == rb) lt += S.xl[q][lane];
         const float inv = 1.f / lt;
         const size_t orow = (static_cast<size_t>(sm.cus + sm.sb + r) * H + h);
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           float ov[32];
           tmem_ld_32x32b_x32(lane_base + c0, ov);
