@@ -40,13 +40,14 @@ struct StreamCfg {
   static constexpr int TB = tile_bytes<D>();  // bf16 64 x D
   static constexpr int OB = 64 * D * 4;       // fp32 O~ page
   // block role: K/V ring | 128-row query tile | two 128 x 64 score-probability tiles
-  static constexpr int kKStages = 4;
+  static constexpr int kKStages = 5;
   static constexpr int KStage = 2 * TB;
   static constexpr int off_qb = kKStages * KStage;
   static constexpr int QB = 2 * TB;  // 128 rows x D
   static constexpr int off_p = off_qb + QB;
-  static constexpr int PB = 128 * 128;  // 128 rows x 64 keys bf16
-  static constexpr int kBlockSmem = off_p + 2 * PB;
+  static constexpr int PB = 128 * 128;  // 128 rows x 64 keys bf16 (one buffer: a page's P V is done
+                                        // before the next page's P is written)
+  static constexpr int kBlockSmem = off_p + PB;
   // merge role: query page | O~ page | m | l ring, then the gathered block keys / values
   static constexpr int kMStages = 3;
   static constexpr int MStage = TB + OB + 1024;
@@ -60,7 +61,7 @@ struct StreamCfg {
 };
 
 struct Shared {
-  uint64_t full[4], empty[4], qfull, qempty;
+  uint64_t full[5], empty[5], qfull, qempty;
   uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
   uint32_t tmem_base;
   float xmax[2][4][32];  // block role: [page parity][warp][lane] maxima over the warp's keys
@@ -252,7 +253,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
           wait_or_abort(S, &S.pfull[sb], (nn >> 1) & 1, bt.err);
           tc_fence_after();
-          const uint32_t pa = smem_u32(p_tile + sb * C::PB);
+          const uint32_t pa = smem_u32(p_tile);
           const uint32_t va = smem_u32(ring + st * C::KStage + TB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -347,9 +348,9 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           }
         }
         // P = 2^(S - m_ref) as bf16 into this warp's keys of row r of the P tile (K-major, 128-byte swizzle)
-        if (n >= 2) wait_or_abort(S, &S.pvdone[sb], ((n >> 1) - 1) & 1, bt.err);  // P buffer sb is free
+        if (n >= 1) wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);  // P is free
         const float mu = row_ok ? m_ref : 0.f;
-        uint8_t* prow = p_tile + sb * C::PB;
+        uint8_t* prow = p_tile;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   const bool block_role = static_cast<int>(blockIdx.x) < n_block_ctas;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 5; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], block_role ? 1 : 4);  // block role: the MMA completion; merge: one group of 4 warps
     }
