@@ -169,7 +169,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
   // 1/4 or 1/2 of every page's keys, and the four schedulers share each
   // page's softmax.  Row r's state across the warps is combined through
   // shared memory (page max every page, the sums at the end).  Warp 8 issues
-  // the MMAs (and owns TMEM), warp 9 streams the tiles, warps 4-7 idle.
+  // the score MMAs (and owns TMEM), warp 4 the P V MMAs, warp 9 streams the
+  // tiles, warps 5-7 idle.
   if (warp == 8) tmem_alloc(&S.tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -235,10 +236,13 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
       if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
   } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ Q K^T issuer
+    // The score MMAs and the P V MMAs are issued by two threads (warps 8 and
+    // 4): an MMA issue takes tens of ns here, and one thread issuing both
+    // chains in order held the next page's scores behind the previous
+    // page's P V.  A K/V stage is free once both have completed (two commits).
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
-      constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
       int n = 0, nq = 0;  // pages, (b, h) pairs so far
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H);
@@ -248,20 +252,6 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         wait_or_abort(S, &S.qfull, nq & 1, bt.err);
         tc_fence_after();
         const uint32_t qa = smem_u32(q_tile);
-        auto issue_pv = [&](int j, int nn) {  // O += P V for the page j of this (b, h), global page nn
-          const int sb = nn & 1, st = nn % C::kKStages;
-          if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
-          wait_or_abort(S, &S.pfull[sb], (nn >> 1) & 1, bt.err);
-          tc_fence_after();
-          const uint32_t pa = smem_u32(p_tile);
-          const uint32_t va = smem_u32(ring + st * C::KStage + TB);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&S.empty[st]);   // the K/V stage is free
-          umma_commit(&S.pvdone[sb]);  // P buffer free, O holds page j
-        };
         for (int j = 0; j < np; ++j, ++n) {
           const int st = n % C::kKStages, sb = n & 1;
           wait_or_abort(S, &S.full[st], (n / C::kKStages) & 1, bt.err);
@@ -273,10 +263,37 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
             umma_bf16(tmem + C::kTmemS + sb * 64, umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
                       umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
           umma_commit(&S.sfull[sb]);
+          umma_commit(&S.empty[st]);  // K of the stage read
           if (j == np - 1) umma_commit(&S.qempty);  // this (b, h)'s queries are no longer read
-          if (j >= 1) issue_pv(j - 1, n - 1);
         }
-        issue_pv(np - 1, n - 1);
+        ++nq;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
+      int n = 0, nq = 0;
+      for (long long bh = bh0; bh < bh1; ++bh) {
+        const int b = static_cast<int>(bh / H);
+        const SeqMeta sm = load_meta(bt, b);
+        if (!sm.ok) continue;
+        const int np = (sm.nb + kPage - 1) / kPage;
+        for (int j = 0; j < np; ++j, ++n) {  // O += P V for page j (its stage landed before its scores)
+          const int st = n % C::kKStages, sb = n & 1;
+          if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
+          wait_or_abort(S, &S.pfull[sb], (n >> 1) & 1, bt.err);
+          tc_fence_after();
+          const uint32_t pa = smem_u32(p_tile);
+          const uint32_t va = smem_u32(ring + st * C::KStage + TB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&S.empty[st]);   // V of the stage read
+          umma_commit(&S.pvdone[sb]);  // P free, O holds page j
+        }
         umma_commit(&S.ofinal);
         ++nq;
       }
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < 5; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], block_role ? 1 : 4);  // block role: the MMA completion; merge: one group of 4 warps
+      mbar_init(&S.empty[s], block_role ? 2 : 4);  // block role: the Q K^T and P V completions; merge: 4 warps
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qempty, 1);  // block role: the Q K^T completion of a (b, h)
