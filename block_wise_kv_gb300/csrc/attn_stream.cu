@@ -180,6 +180,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
   if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // a page is read once per step
       int nk = 0, nq = 0;
       bool waited = false;  // griddepcontrol.wait done
       for (long long bh = bh0; bh < bh1; ++bh) {
@@ -199,8 +200,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
             mbar_arrive_expect_tx(&S.full[nk], 2 * TB);
 #pragma unroll
             for (int hf = 0; hf < D / 64; ++hf) {
-              tma_load_2d(kt + hf * 8192, &tm_k, &S.full[nk], hf * 64, y);
-              tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.full[nk], hf * 64, y);
+              tma_load_2d_hint(kt + hf * 8192, &tm_k, &S.full[nk], hf * 64, y, pol);
+              tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, &S.full[nk], hf * 64, y, pol);
             }
           }
           griddep_wait();
@@ -226,8 +227,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           mbar_arrive_expect_tx(&S.full[s], 2 * TB);
 #pragma unroll
           for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_2d(kt + hf * 8192, &tm_k, &S.full[s], hf * 64, y);
-            tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.full[s], hf * 64, y);
+            tma_load_2d_hint(kt + hf * 8192, &tm_k, &S.full[s], hf * 64, y, pol);
+            tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, &S.full[s], hf * 64, y, pol);
           }
         }
       }
@@ -519,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   if (warp == 8) {
     // ---------------------------------------------------- merge producer
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // the cached state is read once per step
       int nm = 0;
       for (; w.valid(); w.next(S, bt, H)) {
         if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
@@ -529,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
         uint8_t* mt = ring + s * C::MStage;
         mbar_arrive_expect_tx(&S.full[s], TB + C::OB + 512);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) tma_load_2d(mt + hf * 8192, &tm_q, &S.full[s], hf * 64, y);
+        for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + hf * 8192, &tm_q, &S.full[s], hf * 64, y, pol);
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) tma_load_2d(mt + TB + j * 8192, &tm_o, &S.full[s], j * 32, y);
+        for (int j = 0; j < D / 32; ++j) tma_load_2d_hint(mt + TB + j * 8192, &tm_o, &S.full[s], j * 32, y, pol);
         bulk_load(mt + TB + C::OB, a.m_pool + y, 256, &S.full[s]);
         bulk_load(mt + TB + C::OB + 256, a.l_pool + y, 256, &S.full[s]);
         ++nm;

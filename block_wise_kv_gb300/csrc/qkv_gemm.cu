@@ -241,10 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int npre = n_units < kStages ? n_units : kStages;
     UnitWalk w;
     w.init(u0, u1, nkb);
+    const uint64_t wpol = l2_evict_first_policy();  // each weight byte is read once per call
     if (lane == 0) {
       for (int i = 0; i < npre; ++i, w.next()) {
         mbar_arrive_expect_tx(&full_bar[i], kStageBytes);
-        tma_load_2d(smem + i * kStageBytes, &tm_w, &full_bar[i], 0, (w.tile * kbp + kBoxes * w.kb) * kTileM);
+        tma_load_2d_hint(smem + i * kStageBytes, &tm_w, &full_bar[i], 0, (w.tile * kbp + kBoxes * w.kb) * kTileM,
+                         wpol);
       }
       griddep_wait();
       const uint64_t t0 = global_timer_ns();  // bounded wait for the x^ rows
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sa = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-        tma_load_2d(sa, &tm_w, &full_bar[s], 0, (w.tile * kbp + kBoxes * w.kb) * kTileM);
+        tma_load_2d_hint(sa, &tm_w, &full_bar[s], 0, (w.tile * kbp + kBoxes * w.kb) * kTileM, wpol);
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
           tma_load_2d(sa + kBoxes * kTileABytes + j * kTileBBytes, &tm_x, &full_bar[s], w.kb * kUnitK + j * kTileK,
