@@ -168,9 +168,9 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
   // MMA rows cost nothing): warp q (0-3) reads its quadrant's copy and takes
   // 1/4 or 1/2 of every page's keys, and the four schedulers share each
   // page's softmax.  Row r's state across the warps is combined through
-  // shared memory (page max every page, the sums at the end).  Warp 8 issues
-  // the score MMAs (and owns TMEM), warp 4 the P V MMAs, warp 9 streams the
-  // tiles, warps 5-7 idle.
+  // shared memory (page max every page, the sums at the end).  Warps 8 and 5
+  // issue the score MMAs (warp 8 owns TMEM), warp 4 the P V MMAs, warp 9
+  // streams the tiles, warps 6-7 idle.
   if (warp == 8) tmem_alloc(&S.tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -236,14 +236,17 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
       if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ Q K^T issuer
-    // The score MMAs and the P V MMAs are issued by two threads (warps 8 and
-    // 4): an MMA issue takes tens of ns here, and one thread issuing both
-    // chains in order held the next page's scores behind the previous
-    // page's P V.  A K/V stage is free once both have completed (two commits).
+  } else if (warp == 8 || warp == 5) {
+    // ------------------------------------------------------------ Q K^T issuers
+    // The score MMAs and the P V MMAs are issued by separate threads: an MMA
+    // issue takes tens of ns here, so one thread issuing every MMA in order
+    // set the page rate.  Warps 8 and 5 take the even and the odd pages (S
+    // buffers 0 and 1), warp 4 every P V.  A K/V stage is free once its
+    // Q K^T and its P V have completed (two commits); the query tile once
+    // both score issuers have committed the (b, h)'s last MMAs.
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
+      const int par = warp == 8 ? 0 : 1;
       int n = 0, nq = 0;  // pages, (b, h) pairs so far
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H);
@@ -254,7 +257,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         tc_fence_after();
         const uint32_t qa = smem_u32(q_tile);
         for (int j = 0; j < np; ++j, ++n) {
-          const int st = n % C::kKStages, sb = n & 1;
+          if ((n & 1) != par) continue;
+          const int st = n % C::kKStages, sb = par;
           wait_or_abort(S, &S.full[st], (n / C::kKStages) & 1, bt.err);
           if (n >= 2) wait_or_abort(S, &S.sempty[sb], ((n >> 1) - 1) & 1, bt.err);
           tc_fence_after();
@@ -265,8 +269,8 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
                       umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
           umma_commit(&S.sfull[sb]);
           umma_commit(&S.empty[st]);  // K of the stage read
-          if (j == np - 1) umma_commit(&S.qempty);  // this (b, h)'s queries are no longer read
         }
+        umma_commit(&S.qempty);  // this issuer no longer reads the (b, h)'s queries
         ++nq;
       }
     }
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       mbar_init(&S.empty[s], block_role ? 2 : 4);  // block role: the Q K^T and P V completions; merge: 4 warps
     }
     mbar_init(&S.qfull, 1);
-    mbar_init(&S.qempty, 1);  // block role: the Q K^T completion of a (b, h)
+    mbar_init(&S.qempty, 2);  // block role: the Q K^T completions of a (b, h) (two issuers)
     S.abort_flag = 0;
     fence_barrier_init();
   }
