@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           report_error(bt.err, kErrTimeout);
           break;
         }
-        __nanosleep(100);
+        __nanosleep(20);
       }
       fence_proxy_async_global();  // the rows written by other CTAs' threads, as seen by TMA
     }
@@ -419,10 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           griddep_wait();  // from here on x may be read
           continue;
         }
-        if (at == 0) {
-          __threadfence();  // the whole row and its scale are visible GPU-wide before they are counted
-          atomicAdd(a.norm_ctr + 1, 1);
-        }
+        if (at == 0) red_release_gpu_add(a.norm_ctr + 1, 1);  // the row and its scale, then the count
       }
       // the staging areas are about to be written by TMA (async proxy)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

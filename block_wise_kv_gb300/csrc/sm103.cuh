@@ -349,6 +349,12 @@ __device__ __forceinline__ void named_barrier_arrive(int id, int count) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// Release-ordered atomic add at GPU scope: the calling thread's earlier
+// writes, and those ordered before it by a CTA barrier, are visible to a
+// thread that reads the new value with acquire semantics.
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
