@@ -150,7 +150,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one projection
 # launch, per workload, from one ncu capture of the kernel as it stands
 # (--set full, the launch of an inner step); no entry: not captured.
-QKV_TRAFFIC_BYTES = {"llada_single": 104_140_032}
+QKV_TRAFFIC_BYTES = {"llada_single": 103_979_008}
 
 
 def step_bytes_flops(cfg, st):
