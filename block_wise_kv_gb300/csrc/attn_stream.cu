@@ -45,9 +45,12 @@ struct StreamCfg {
   static constexpr int off_qb = kKStages * KStage;
   static constexpr int QB = 2 * TB;  // 128 rows x D
   static constexpr int off_p = off_qb + QB;
-  static constexpr int PB = 128 * 128;  // 128 rows x 64 keys bf16 (one buffer: a page's P V is done
-                                        // before the next page's P is written)
-  static constexpr int kBlockSmem = off_p + PB;
+  // two P tiles (128 rows x 64 keys bf16, 16 KB each), the second 8 KB after the first: only
+  // rows 0-63 are ever written, and the rows of one tile that overlap the other only reach
+  // rows of O that are never read
+  static constexpr int PB = 128 * 128;
+  static constexpr int kPOff = 8192;
+  static constexpr int kBlockSmem = off_p + kPOff + PB;
   // merge role: query page | O~ page | m | l ring, then the gathered block keys / values
   static constexpr int kMStages = 3;
   static constexpr int MStage = TB + OB + 1024;
@@ -290,7 +293,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
           wait_or_abort(S, &S.pfull[sb], (n >> 1) & 1, bt.err);
           tc_fence_after();
-          const uint32_t pa = smem_u32(p_tile);
+          const uint32_t pa = smem_u32(p_tile + sb * C::kPOff);
           const uint32_t va = smem_u32(ring + st * C::KStage + TB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -370,9 +373,9 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           }
         }
         // P = 2^(S - m_ref) as bf16 into this warp's keys of row r of the P tile (K-major, 128-byte swizzle)
-        if (n >= 1) wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);  // P is free
+        if (n >= 2) wait_or_abort(S, &S.pvdone[sb], ((n - 2) >> 1) & 1, bt.err);  // P tile sb is free
         const float mu = row_ok ? m_ref : 0.f;
-        uint8_t* prow = p_tile;
+        uint8_t* prow = p_tile + sb * C::kPOff;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
