@@ -32,7 +32,7 @@ namespace dllm {
 namespace {
 using namespace attn;
 
-constexpr int kThreads = 320;  // merge role: warps 0-7 compute, 8 streams; block role: 0-3, 8 MMAs, 9 streams
+constexpr int kThreads = 384;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
 constexpr int kMaxBatch = 512;
 
 template <int D>
@@ -58,17 +58,19 @@ struct StreamCfg {
   static constexpr int off_vc = off_kc + TB;
   static constexpr int kMergeSmem = off_vc + TB;
   static constexpr int kSmem = (kBlockSmem > kMergeSmem ? kBlockSmem : kMergeSmem) + 1024;  // + alignment slack
-  // tensor memory of the block role: O (D columns) then two score buffers of 64 columns
-  static constexpr uint32_t kTmemCols = D == 128 ? 256 : 256;
-  static constexpr uint32_t kTmemS = D;
+  // tensor memory of the block role: O of softmax group 0 and of group 1 (D columns each),
+  // then a score buffer of 64 columns per group
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemS = 2 * D;
 };
 
 struct Shared {
   uint64_t full[5], empty[5], qfull, qempty;
   uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
   uint32_t tmem_base;
-  float xmax[2][4][32];  // block role: [page parity][warp][lane] maxima over the warp's keys
-  float xl[4][32];       // block role: [warp][lane] sums over the warp's keys
+  float xmax[2][2][4][32];  // block role: [group][page parity][warp of the group][lane] maxima over the warp's keys
+  float xm[2][64];          // block role: [group][query row] reference max at the end of a (b, h)
+  float xl[8][32];          // block role: [warp][lane] sum over the warp's keys at the end of a (b, h)
   int abort_flag;
   int n_seq_units[kMaxBatch];  // H * pages of sequence b (0: invalid metadata)
   int cu[kMaxBatch + 1];       // unit prefix
@@ -127,16 +129,28 @@ __device__ __forceinline__ void wait_or_abort(Shared& S, uint64_t* bar, uint32_t
 
 // ---------------------------------------------------------------------------
 // Block role on the 5th-generation tensor cores.  For each (b, h) the CTA
-// owns: the block queries stay in shared memory as a 128-row MMA tile; per
-// 64-key page, warp 8 issues S = Q K^T (M = 128, N = 64, into one of two TMEM
-// score buffers) and, once the softmax warps have written P for it, O += P V
-// (M = 128, N = D, V as an MN-major operand) into TMEM, so the scores of page
-// p + 1 are computed while page p's softmax runs.  The softmax (warps 0-3):
-// exact row max over the page, P = 2^(S - m_ref) with a reference max m_ref
-// that is raised (and O, l rescaled) only when a page's max exceeds it by
-// more than 2^8 (every P stays <= 2^8; the result is exact for any
-// reference), running sum l in fp32, and at the end of the (b, h) O / l and
-// L = m_ref + log2 l.
+// owns, the block queries stay in shared memory as a 128-row MMA tile and the
+// pages go alternately to two softmax groups of four warps (group g takes the
+// pages j with j mod 2 == g), each with its own online-softmax state
+// (LaCache Eq. (2)-(6)): a reference max and running sums per row and its own
+// O accumulator O_g in TMEM.  Per page of group g, warp 8 (g = 0) or 10
+// (g = 1) issues S = Q K^T (M = 128, N = 64) into the group's TMEM score
+// buffer; the group's warps write P = 2^(S - m_ref) as bf16 into the group's
+// P tile, and warp 11 issues O_g += P V (M = 128, N = D, V as an MN-major
+// operand), for both groups in page order.  The reference max is raised (O_g
+// and the sums rescaled) only when a page's max exceeds it by more than 2^8,
+// so every P stays <= 2^8 and the result is exact for any reference.  At the
+// end of the (b, h) the two groups' states are merged exactly (the merge rule
+// of LaCache §3.3.3) and O / l and L = m + log2 l are written.  Warp 9
+// streams the tiles.
+//
+// A TMEM lane quadrant q is read only by warps q mod 4, which all issue from
+// scheduler q, so the block queries (<= 32 or <= 64 rows) are loaded into
+// every quadrant of the 128-row query tile (4 or 2 copies; the extra MMA rows
+// cost nothing): warp q of a group reads its quadrant's copy and takes 1/4 or
+// 1/2 of every page's keys, so the four schedulers share each page's softmax
+// and each scheduler hosts one warp of either group.  A row's page max is
+// exchanged within the group through shared memory once per page.
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CUtensorMap& tm_qb,
@@ -155,25 +169,16 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
   uint8_t* q_tile = smem + C::off_qb;
   uint8_t* p_tile = smem + C::off_p;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.sfull[i], 1);
-      mbar_init(&S.sempty[i], 4);
-      mbar_init(&S.pfull[i], 4);
-      mbar_init(&S.pvdone[i], 1);
+    for (int i = 0; i < 2; ++i) {  // per softmax group
+      mbar_init(&S.sfull[i], 1);   // the Q K^T commit
+      mbar_init(&S.sempty[i], 4);  // the group's warps
+      mbar_init(&S.pfull[i], 4);   // the group's warps
+      mbar_init(&S.pvdone[i], 1);  // the P V commit
     }
     mbar_init(&S.ofinal, 1);
-    mbar_init(&S.oempty, 4);
+    mbar_init(&S.oempty, 8);  // the eight softmax warps
     fence_barrier_init();
   }
-  // A TMEM lane quadrant q is read only by warps q mod 4, which all issue
-  // from scheduler q, so the block queries (<= 32 or <= 64 rows) are loaded
-  // into every quadrant of the 128-row query tile (4 or 2 copies; the extra
-  // MMA rows cost nothing): warp q (0-3) reads its quadrant's copy and takes
-  // 1/4 or 1/2 of every page's keys, and the four schedulers share each
-  // page's softmax.  Row r's state across the warps is combined through
-  // shared memory (page max every page, the sums at the end).  Warps 8 and 5
-  // issue the score MMAs (warp 8 owns TMEM), warp 4 the P V MMAs, warp 9
-  // streams the tiles, warps 6-7 idle.
   if (warp == 8) tmem_alloc(&S.tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -239,18 +244,16 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
       if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
-  } else if (warp == 8 || warp == 5) {
+  } else if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ Q K^T issuers
-    // The score MMAs and the P V MMAs are issued by separate threads: an MMA
-    // issue takes tens of ns here, so one thread issuing every MMA in order
-    // set the page rate.  Warps 8 and 5 take the even and the odd pages (S
-    // buffers 0 and 1), warp 4 every P V.  A K/V stage is free once its
-    // Q K^T and its P V have completed (two commits); the query tile once
-    // both score issuers have committed the (b, h)'s last MMAs.
+    // An MMA issue takes tens of ns here, so the score MMAs of the two groups
+    // and the P V MMAs have their own threads.  A K/V stage is free once its
+    // Q K^T and its P V have completed (two commits); the query tile once both
+    // score issuers have committed the (b, h)'s last MMAs.
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
-      const int par = warp == 8 ? 0 : 1;
-      int n = 0, nq = 0;  // pages, (b, h) pairs so far
+      const int g = warp == 8 ? 0 : 1;
+      int n0 = 0, k = 0, nq = 0;  // pages of earlier (b, h) pairs, the group's pages so far, (b, h) pairs
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H);
         const SeqMeta sm = load_meta(bt, b);
@@ -259,123 +262,129 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         wait_or_abort(S, &S.qfull, nq & 1, bt.err);
         tc_fence_after();
         const uint32_t qa = smem_u32(q_tile);
-        for (int j = 0; j < np; ++j, ++n) {
-          if ((n & 1) != par) continue;
-          const int st = n % C::kKStages, sb = par;
+        for (int j = g; j < np; j += 2, ++k) {
+          const int n = n0 + j, st = n % C::kKStages;
           wait_or_abort(S, &S.full[st], (n / C::kKStages) & 1, bt.err);
-          if (n >= 2) wait_or_abort(S, &S.sempty[sb], ((n >> 1) - 1) & 1, bt.err);
+          if (k >= 1) wait_or_abort(S, &S.sempty[g], (k - 1) & 1, bt.err);  // the group has read its last scores
           tc_fence_after();
           const uint32_t ka = smem_u32(ring + st * C::KStage);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16(tmem + C::kTmemS + sb * 64, umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
+            umma_bf16(tmem + C::kTmemS + g * 64, umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
                       umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
-          umma_commit(&S.sfull[sb]);
+          umma_commit(&S.sfull[g]);
           umma_commit(&S.empty[st]);  // K of the stage read
         }
         umma_commit(&S.qempty);  // this issuer no longer reads the (b, h)'s queries
+        n0 += np;
         ++nq;
       }
     }
     __syncwarp();
-  } else if (warp == 4) {
+  } else if (warp == 11) {
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
       constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
-      int n = 0, nq = 0;
+      int n = 0, nq = 0, k0 = 0, k1 = 0;  // pages, (b, h) pairs, each group's pages so far
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H);
         const SeqMeta sm = load_meta(bt, b);
         if (!sm.ok) continue;
         const int np = (sm.nb + kPage - 1) / kPage;
-        for (int j = 0; j < np; ++j, ++n) {  // O += P V for page j (its stage landed before its scores)
-          const int st = n % C::kKStages, sb = n & 1;
-          if (j == 0 && nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // previous O read out
-          wait_or_abort(S, &S.pfull[sb], (n >> 1) & 1, bt.err);
+        if (nq >= 1) wait_or_abort(S, &S.oempty, (nq - 1) & 1, bt.err);  // the previous (b, h)'s O read out
+        for (int j = 0; j < np; ++j, ++n) {  // O_g += P V for page j (its stage landed before its scores)
+          const int g = j & 1, st = n % C::kKStages;
+          const int k = g == 0 ? k0++ : k1++;
+          wait_or_abort(S, &S.pfull[g], k & 1, bt.err);
           tc_fence_after();
-          const uint32_t pa = smem_u32(p_tile + sb * C::kPOff);
+          const uint32_t pa = smem_u32(p_tile + g * C::kPOff);
           const uint32_t va = smem_u32(ring + st * C::KStage + TB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&S.empty[st]);   // V of the stage read
-          umma_commit(&S.pvdone[sb]);  // P free, O holds page j
+            umma_bf16(tmem + g * D, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
+                      (j > g || kk > 0) ? 1u : 0u);
+          umma_commit(&S.empty[st]);  // V of the stage read
+          umma_commit(&S.pvdone[g]);  // the group's P tile free, O_g holds page j
         }
         umma_commit(&S.ofinal);
         ++nq;
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warps
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int g = warp >> 2, wq = warp & 3;  // group, warp of the group (= TMEM lane quadrant)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
-    int n = 0, nq = 0;
+    uint8_t* p_own = p_tile + g * C::kPOff;
+    int k = 0, nq = 0;  // the group's pages so far, (b, h) pairs
     for (long long bh = bh0; bh < bh1; ++bh) {
       const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
       const SeqMeta sm = load_meta(bt, b);
       if (!sm.ok) continue;
       const int np = (sm.nb + kPage - 1) / kPage;
       const int RQ = sm.bb > 32 ? 2 : 1;        // quadrants per copy of the queries
-      const int rb = warp % RQ, slice = warp / RQ;  // row block, key slice
+      const int rb = wq % RQ, slice = wq / RQ;  // row block, key slice
       const int KW = 16 * RQ;                   // keys per warp per page
       const int r = rb * 32 + lane;             // query row
       const bool row_ok = r < sm.bb;
       float m_ref = neg_inf(), l = 0.f;  // l: over this warp's keys
-      for (int j = 0; j < np; ++j, ++n) {
-        const int sb = n & 1;
-        wait_or_abort(S, &S.sfull[sb], (n >> 1) & 1, bt.err);
+      for (int j = g; j < np; j += 2, ++k) {  // the group's pages (the same for its four warps)
+        wait_or_abort(S, &S.sfull[g], k & 1, bt.err);
         tc_fence_after();
         float sc[32];
-        const uint32_t scol = lane_base + C::kTmemS + sb * 64 + slice * KW;
+        const uint32_t scol = lane_base + C::kTmemS + g * 64 + slice * KW;
         if (RQ == 1)
           tmem_ld_32x32b_x16(scol, *reinterpret_cast<float(*)[16]>(sc));
         else
           tmem_ld_32x32b_x32(scol, sc);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.sempty[sb]);
+        if (lane == 0) mbar_arrive(&S.sempty[g]);
         // scale, mask keys past the sequence, this warp's max; the row's page max
         const int nvalid = sm.nb - j * kPage - slice * KW;
         float mx4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (k >= KW) break;
-          sc[k] = k < nvalid ? sc[k] * a.scale_log2 : neg_inf();
-          mx4[k & 3] = fmaxf(mx4[k & 3], sc[k]);
+        for (int c = 0; c < 32; ++c) {
+          if (c >= KW) break;
+          sc[c] = c < nvalid ? sc[c] * a.scale_log2 : neg_inf();
+          mx4[c & 3] = fmaxf(mx4[c & 3], sc[c]);
         }
-        S.xmax[j & 1][warp][lane] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        named_barrier(4, 128);
+        S.xmax[g][k & 1][wq][lane] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        if (g == 0)
+          named_barrier(4, 128);
+        else
+          named_barrier(5, 128);
         float mx = neg_inf();
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q % RQ == rb) mx = fmaxf(mx, S.xmax[j & 1][q][lane]);
-        // a new reference max (first page, or a rise beyond the threshold) rescales O and l;
-        // every warp of the row takes the same decision from the same values
-        const bool raise = row_ok && (j == 0 || mx > m_ref + kRescale);
-        const float factor = raise && j > 0 ? fast_exp2(m_ref - mx) : 1.f;
+          if (q % RQ == rb) mx = fmaxf(mx, S.xmax[g][k & 1][q][lane]);
+        // a new reference max (the group's first page, or a rise beyond the threshold) rescales
+        // O_g and l; every warp of the row takes the same decision from the same values
+        const bool first = j == g;
+        const bool raise = row_ok && (first || mx > m_ref + kRescale);
+        const float factor = raise && !first ? fast_exp2(m_ref - mx) : 1.f;
         if (raise) m_ref = mx;
-        if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+        if (!first && __any_sync(0xffffffffu, factor != 1.f)) {
           l *= factor;
-          if (slice == 0) {  // O's rows of this row block live in this warp's quadrant
-            wait_or_abort(S, &S.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1, bt.err);  // O holds pages 0 .. j-1
+          if (slice == 0) {  // O_g's rows of this row block live in this warp's quadrant
+            wait_or_abort(S, &S.pvdone[g], (k - 1) & 1, bt.err);  // O_g holds the group's earlier pages
             tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               float ov[32];
-              tmem_ld_32x32b_x32(lane_base + c0, ov);
+              tmem_ld_32x32b_x32(lane_base + g * D + c0, ov);
 #pragma unroll
               for (int i = 0; i < 32; ++i) ov[i] *= factor;
-              tmem_st_32x32b_x32(lane_base + c0, ov);
+              tmem_st_32x32b_x32(lane_base + g * D + c0, ov);
             }
             tmem_st_wait();
           }
         }
-        // P = 2^(S - m_ref) as bf16 into this warp's keys of row r of the P tile (K-major, 128-byte swizzle)
-        if (n >= 2) wait_or_abort(S, &S.pvdone[sb], ((n - 2) >> 1) & 1, bt.err);  // P tile sb is free
+        // P = 2^(S - m_ref) as bf16 into this warp's keys of row r of the group's P tile
+        // (K-major, 128-byte swizzle), once the group's previous P V has read the tile
+        if (k >= 1) wait_or_abort(S, &S.pvdone[g], (k - 1) & 1, bt.err);
         const float mu = row_ok ? m_ref : 0.f;
-        uint8_t* prow = p_tile + sb * C::kPOff;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -391,46 +400,70 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           u.y = pack_bf16x2(pv[2], pv[3]);
           u.z = pack_bf16x2(pv[4], pv[5]);
           u.w = pack_bf16x2(pv[6], pv[7]);
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, slice * (KW / 8) + cc)) = u;
+          *reinterpret_cast<uint4*>(p_own + sw128_offset(r, slice * (KW / 8) + cc)) = u;
         }
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.pfull[sb]);
+        if (lane == 0) mbar_arrive(&S.pfull[g]);
       }
-      // ---- the (b, h) is complete: O / l out (the warps of copy 0), then release O
+      // ---- the (b, h) is complete: merge the groups' states, O / l out, release O.  A row's
+      // O_0 and O_1 live in the same TMEM lanes, so the warps of group 0 that hold the row
+      // read both; only the maxima and sums go through shared memory.
+      const bool has1 = np > 1;  // group 1 has pages
+      if (slice == 0) S.xm[g][r] = m_ref;
       S.xl[warp][lane] = l;
-      named_barrier(4, 128);
-      wait_or_abort(S, &S.ofinal, nq & 1, bt.err);
-      tc_fence_after();
-      if (slice == 0) {
-        float lt = 0.f;
+      named_barrier(6, 256);
+      if (g == 0 && slice == 0) {
+        wait_or_abort(S, &S.ofinal, nq & 1, bt.err);
+        tc_fence_after();
+        float w0 = 0.f, w1 = 0.f, inv = 0.f, M = 0.f, L = 1.f;
+        if (row_ok) {
+          float lg[2] = {0.f, 0.f};  // each group's sum for row r
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q % RQ == rb) lt += S.xl[q][lane];
-        const float inv = 1.f / lt;
+          for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q % RQ == rb) lg[gg] += S.xl[gg * 4 + q][lane];
+          const float m0 = S.xm[0][r], m1 = has1 ? S.xm[1][r] : neg_inf();
+          M = fmaxf(m0, m1);
+          w0 = fast_exp2(m0 - M);
+          w1 = has1 ? fast_exp2(m1 - M) : 0.f;
+          L = w0 * lg[0] + w1 * lg[1];
+          inv = 1.f / L;
+          w0 *= inv;
+          w1 *= inv;
+        }
         const size_t orow = (static_cast<size_t>(sm.cus + sm.sb + r) * H + h);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-          float ov[32];
+          float ov[32], ow[32];
           tmem_ld_32x32b_x32(lane_base + c0, ov);
+          if (has1)
+            tmem_ld_32x32b_x32(lane_base + D + c0, ow);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ow[i] = 0.f;
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(of + orow * D + c0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = ov[q * 8 + e] * w0 + ow[q * 8 + e] * w1;
               uint4 u;
-              u.x = pack_bf16x2(ov[q * 8 + 0] * inv, ov[q * 8 + 1] * inv);
-              u.y = pack_bf16x2(ov[q * 8 + 2] * inv, ov[q * 8 + 3] * inv);
-              u.z = pack_bf16x2(ov[q * 8 + 4] * inv, ov[q * 8 + 5] * inv);
-              u.w = pack_bf16x2(ov[q * 8 + 6] * inv, ov[q * 8 + 7] * inv);
+              u.x = pack_bf16x2(v[0], v[1]);
+              u.y = pack_bf16x2(v[2], v[3]);
+              u.z = pack_bf16x2(v[4], v[5]);
+              u.w = pack_bf16x2(v[6], v[7]);
               dst[q] = u;
             }
           }
         }
-        if (row_ok && a.lse != nullptr) a.lse[orow] = (m_ref + log2f(lt)) * kLn2;
+        if (row_ok && a.lse != nullptr) a.lse[orow] = (M + log2f(L)) * kLn2;
       }
-      named_barrier(4, 128);  // xl is read before the next (b, h) writes it
+      named_barrier(6, 256);  // xm and xl are read before the next (b, h) writes them
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.oempty);
@@ -550,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     }
     return;
   }
-  if (warp == 9) return;  // not used by the merge role
+  if (warp >= 9) return;  // not used by the merge role
   // ------------------------------------------------ merge compute (2 groups of 4 warps)
   const int grp = warp >> 2, mw = warp & 3;
   const int g = lane >> 2, t = lane & 3;
