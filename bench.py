@@ -19,7 +19,10 @@ layer instances (about 140 MB each), so no step finds its inputs in the
 fused RMSNorm + projection + RoPE + K/V write, and the block attention +
 FACache merge launch); a sample of the steps (one round in 32) carries CUDA
 events around the projection call on its stream, which give its live
-duration for the roofline.
+duration for the roofline.  The end-to-end figure calls the public step API
+with the block rows copied in from pinned host memory and o_full read back to
+pinned host memory every step (the read-back on a copy stream, under the next
+step).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (sequences are independent units: weak scaling, no collective on the data
@@ -307,27 +310,44 @@ def run_ours(args, rank, ws, local):
     for st, _ in inst:
         assert st.batch.error_bits() == 0, "device-side error during the timed steps"
 
-    # end to end through the public API: pinned host input -> step -> host output
+    # end to end through the public API: pinned host input -> step -> host output.
+    # The read-back of a step's o_full runs on a copy stream while the next
+    # step (another layer instance) computes; a layer instance's next step
+    # waits until its previous o_full has been read out.
     x_host = [xb.cpu().pin_memory() for _, xb in inst]
     o_host = [torch.empty_like(st.o_full, device="cpu").pin_memory() for st, _ in inst]
     x_dev = [torch.empty_like(xb) for _, xb in inst]
     Ke = max(1, min(K, args.e2e_steps))
+    main = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    read_out = [None] * L
+
+    def e2e_step(i):
+        j = i % L
+        st, _ = inst[j]
+        if read_out[j] is not None:
+            main.wait_event(read_out[j])
+        x_dev[j].copy_(x_host[j], non_blocking=True)
+        st.step(x_dev[j])
+        done = torch.cuda.Event()
+        done.record(main)
+        copy_stream.wait_event(done)
+        with torch.cuda.stream(copy_stream):
+            o_host[j].copy_(st.o_full, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(copy_stream)
+        read_out[j] = ev
+
     for i in range(min(W, 8)):
-        st, _ = inst[i % L]
-        x_dev[i % L].copy_(x_host[i % L], non_blocking=True)
-        st.step(x_dev[i % L])
-        o_host[i % L].copy_(st.o_full, non_blocking=True)
+        e2e_step(i)
     torch.cuda.synchronize()
     _barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(main)
     for i in range(Ke):
-        j = i % L
-        st, _ = inst[j]
-        x_dev[j].copy_(x_host[j], non_blocking=True)
-        st.step(x_dev[j])
-        o_host[j].copy_(st.o_full, non_blocking=True)
-    e1.record()
+        e2e_step(i)
+    main.wait_stream(copy_stream)  # the last read-back is inside the timed region
+    e1.record(main)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     h2d = x_host[0].numel() * x_host[0].element_size()
