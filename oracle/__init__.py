@@ -21,7 +21,7 @@ of the step:
                                                        sampler recomputes the
                                                        full sequence every step)
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
 scale = 1/sqrt(d_h); rotate-half RoPE pairs (i, i + d/2) with angle
 p * theta^(-2i/d); RMSNorm eps = 1e-5 with gain g; the only rounding points
 mirrored are the two storage formats of the method: x^ -> bf16 (the GEMM
