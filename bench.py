@@ -17,7 +17,7 @@ layer instances (about 140 MB each), so no step finds its inputs in the
 129 MB L2.  The steps replay CUDA graphs of 32 layer-steps (8 rounds of the
 4 instances, as one forward over 32 layers would be; two kernels a step: the
 fused RMSNorm + projection + RoPE + K/V write, and the block attention +
-FACache merge launch); a sample of the steps (one round in 32) carries CUDA
+FACache merge launch); a sample of the steps (one round in 128) carries CUDA
 events around the projection call on its stream, which give its live
 duration for the roofline.  The end-to-end figure calls the public step API
 with the block rows copied in from pinned host memory and o_full read back to
@@ -554,7 +554,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--rounds-per-graph", type=int, default=8,
                     help="rounds of steps (one step of every layer instance each) captured in one graph")
-    ap.add_argument("--sample-every", type=int, default=4,
+    ap.add_argument("--sample-every", type=int, default=16,
                     help="the first round of every n-th pass carries events around the projection call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
