@@ -65,7 +65,12 @@ struct StreamCfg {
 };
 
 struct Shared {
-  uint64_t full[5], empty[5], qfull, qempty;
+  // A ring stage alternates between the two consumer groups (pages go to the groups
+  // alternately), so each (group, stage) has its own "full" barrier: a waiter must see
+  // every phase of the barrier it waits on, since a parity wait cannot tell phase p from
+  // phase p + 2 (with one barrier per stage a group would skip the other group's phases
+  // and could take a stale stage whenever loads complete out of order).
+  uint64_t full[2][5], empty[5], qfull, qempty;
   uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
   uint32_t tmem_base;
   float xmax[2][2][4][32];  // block role: [group][page parity][warp of the group][lane] maxima over the warp's keys
@@ -190,6 +195,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();  // a page is read once per step
       int nk = 0, nq = 0;
+      int loads[2 * C::kKStages] = {};  // loads per (group, stage) "full" barrier
       bool waited = false;  // griddepcontrol.wait done
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
@@ -205,11 +211,13 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
             if (p * kPage < sm.sb + sm.bb && (p + 1) * kPage > sm.sb) break;  // a page with block rows
             const int y = (page_of(bt, b, p) * H + h) * kPage;
             uint8_t* kt = ring + nk * C::KStage;
-            mbar_arrive_expect_tx(&S.full[nk], 2 * TB);
+            uint64_t* fb = &S.full[p & 1][nk];
+            ++loads[(p & 1) * C::kKStages + nk];
+            mbar_arrive_expect_tx(fb, 2 * TB);
 #pragma unroll
             for (int hf = 0; hf < D / 64; ++hf) {
-              tma_load_2d_hint(kt + hf * 8192, &tm_k, &S.full[nk], hf * 64, y, pol);
-              tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, &S.full[nk], hf * 64, y, pol);
+              tma_load_2d_hint(kt + hf * 8192, &tm_k, fb, hf * 64, y, pol);
+              tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, fb, hf * 64, y, pol);
             }
           }
           griddep_wait();
@@ -232,17 +240,26 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
           if (nk >= C::kKStages) wait_or_abort(S, &S.empty[s], (nk / C::kKStages - 1) & 1, bt.err);
           const int y = (page_of(bt, b, p) * H + h) * kPage;
           uint8_t* kt = ring + s * C::KStage;
-          mbar_arrive_expect_tx(&S.full[s], 2 * TB);
+          uint64_t* fb = &S.full[p & 1][s];
+          ++loads[(p & 1) * C::kKStages + s];
+          mbar_arrive_expect_tx(fb, 2 * TB);
 #pragma unroll
           for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_2d_hint(kt + hf * 8192, &tm_k, &S.full[s], hf * 64, y, pol);
-            tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, &S.full[s], hf * 64, y, pol);
+            tma_load_2d_hint(kt + hf * 8192, &tm_k, fb, hf * 64, y, pol);
+            tma_load_2d_hint(kt + TB + hf * 8192, &tm_v, fb, hf * 64, y, pol);
           }
         }
       }
-      for (int i = (nk > C::kKStages ? nk - C::kKStages : 0); i < nk; ++i)  // every copy has landed
-        if (!mbar_wait(&S.full[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
+      for (int i = 0; i < 2 * C::kKStages; ++i)  // every copy has landed: the last phase of each barrier
+        if (loads[i] > 0 && !mbar_wait(&S.full[i / C::kKStages][i % C::kKStages], (loads[i] - 1) & 1))
+          report_error(bt.err, kErrTimeout);
       if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
+      // Tail: the MMA issuers' last commits on the stages (Q K^T and P V) and on the
+      // query tile have arrived, so no asynchronous arrival reaches this CTA's shared
+      // memory after it exits (the next kernel's CTA may start on this SM at once).
+      for (int i = (nk > C::kKStages ? nk - C::kKStages : 0); i < nk; ++i)
+        if (!mbar_wait(&S.empty[i % C::kKStages], (i / C::kKStages) & 1)) report_error(bt.err, kErrTimeout);
+      if (nq >= 1 && !mbar_wait(&S.qempty, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
   } else if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ Q K^T issuers
@@ -254,6 +271,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
       const int g = warp == 8 ? 0 : 1;
       int n0 = 0, k = 0, nq = 0;  // pages of earlier (b, h) pairs, the group's pages so far, (b, h) pairs
+      int uses[C::kKStages] = {};  // pages of this group taken from each stage so far
       for (long long bh = bh0; bh < bh1; ++bh) {
         const int b = static_cast<int>(bh / H);
         const SeqMeta sm = load_meta(bt, b);
@@ -264,7 +282,7 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         const uint32_t qa = smem_u32(q_tile);
         for (int j = g; j < np; j += 2, ++k) {
           const int n = n0 + j, st = n % C::kKStages;
-          wait_or_abort(S, &S.full[st], (n / C::kKStages) & 1, bt.err);
+          wait_or_abort(S, &S.full[g][st], uses[st]++ & 1, bt.err);
           if (k >= 1) wait_or_abort(S, &S.sempty[g], (k - 1) & 1, bt.err);  // the group has read its last scores
           tc_fence_after();
           const uint32_t ka = smem_u32(ring + st * C::KStage);
@@ -309,6 +327,11 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
         umma_commit(&S.ofinal);
         ++nq;
       }
+      // Tail: this thread's last commits (each group's last P V, the last (b, h)) have
+      // arrived before the CTA can exit.
+      if (k0 >= 1 && !mbar_wait(&S.pvdone[0], (k0 - 1) & 1)) report_error(bt.err, kErrTimeout);
+      if (k1 >= 1 && !mbar_wait(&S.pvdone[1], (k1 - 1) & 1)) report_error(bt.err, kErrTimeout);
+      if (nq >= 1 && !mbar_wait(&S.ofinal, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -497,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 5; ++s) {
-      mbar_init(&S.full[s], 1);
+      mbar_init(&S.full[0][s], 1);
+      mbar_init(&S.full[1][s], 1);
       mbar_init(&S.empty[s], block_role ? 2 : 4);  // block role: the Q K^T and P V completions; merge: 4 warps
     }
     mbar_init(&S.qfull, 1);
@@ -569,17 +593,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
         if (nm >= C::kMStages) wait_or_abort(S, &S.empty[s], (nm / C::kMStages - 1) & 1, bt.err);
         const int y = (page_of(bt, w.b, w.p) * H + w.h) * kPage;
         uint8_t* mt = ring + s * C::MStage;
-        mbar_arrive_expect_tx(&S.full[s], TB + C::OB + 512);
+        uint64_t* fb = &S.full[nm & 1][s];  // page nm goes to group nm & 1
+        mbar_arrive_expect_tx(fb, TB + C::OB + 512);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + hf * 8192, &tm_q, &S.full[s], hf * 64, y, pol);
+        for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + hf * 8192, &tm_q, fb, hf * 64, y, pol);
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) tma_load_2d_hint(mt + TB + j * 8192, &tm_o, &S.full[s], j * 32, y, pol);
-        bulk_load(mt + TB + C::OB, a.m_pool + y, 256, &S.full[s]);
-        bulk_load(mt + TB + C::OB + 256, a.l_pool + y, 256, &S.full[s]);
+        for (int j = 0; j < D / 32; ++j) tma_load_2d_hint(mt + TB + j * 8192, &tm_o, fb, j * 32, y, pol);
+        bulk_load(mt + TB + C::OB, a.m_pool + y, 256, fb);
+        bulk_load(mt + TB + C::OB + 256, a.l_pool + y, 256, fb);
         ++nm;
       }
-      for (int i = (nm > C::kMStages ? nm - C::kMStages : 0); i < nm; ++i)  // every copy has landed
-        if (!mbar_wait(&S.full[i % C::kMStages], (i / C::kMStages) & 1)) report_error(bt.err, kErrTimeout);
+      // every copy has landed: page i is phase i / (2 kMStages) of barrier (i & 1, i % kMStages)
+      for (int i = (nm > C::kMStages ? nm - C::kMStages : 0); i < nm; ++i)
+        if (!mbar_wait(&S.full[i & 1][i % C::kMStages], (i / (2 * C::kMStages)) & 1))
+          report_error(bt.err, kErrTimeout);
     }
     return;
   }
@@ -616,10 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     if (!w.has_u_rows()) continue;
     const int mine = (nm & 1) == grp;
     const int s = nm % C::kMStages;
-    const int uses = nm / C::kMStages;
+    const int uses = nm / (2 * C::kMStages);  // earlier pages of this group in stage s
     ++nm;
     if (!mine) continue;  // the other group's page
-    wait_or_abort(S, &S.full[s], uses & 1, bt.err);
+    wait_or_abort(S, &S.full[grp][s], uses & 1, bt.err);
     uint8_t* q_tile = ring + s * C::MStage;
     const uint8_t* o_tile = q_tile + TB;
     const float* m_s = reinterpret_cast<const float*>(q_tile + TB + C::OB);

@@ -296,6 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: every issued load has landed before the CTA can retire.
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
         if (!mbar_wait(&full_bar[i % kStages], (i / kStages) & 1)) report_error(bt.err, kErrTimeout);
+      // Tail: the MMA issuer's last releases of the ring (tcgen05.commit arrivals on
+      // empty_bar, which nothing else waits for) have landed too.  No asynchronous
+      // arrival may reach this CTA's shared memory after it exits: under programmatic
+      // dependent launch the next kernel's CTA can start on this SM at once, with its
+      // own barriers at the same offsets.
+      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        if (!mbar_wait(&empty_bar[i % kStages], (i / kStages) & 1)) report_error(bt.err, kErrTimeout);
     }
     __syncwarp();
   } else if (warp == 1) {
