@@ -26,13 +26,19 @@
 // rows) overlap that kernel's tail; every read of data it may write comes
 // after griddepcontrol.wait.  Every wait is bounded; after a timeout the CTA
 // stops waiting, flags DLLM_DEVERR_TIMEOUT and drains its own copies.
+#include <math.h>
+
 #include "attn_common.cuh"
 
 namespace dllm {
 namespace {
 using namespace attn;
 
-constexpr int kThreads = 384;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
+constexpr int kThreads = 384;
+// Time of a merge-role page over that of a block-role page on GB300: measured over the
+// 32-layer stack, long-context and ragged workloads (attention time falls from the even
+// split to a minimum at 2.5 on all three: 275 -> 229, 259 -> 191, 1162 -> 870 us).
+constexpr double kMergePageCost = 2.5;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
 constexpr int kMaxBatch = 512;
 
 template <int D>
@@ -82,6 +88,25 @@ struct Shared {
 };
 
 __device__ __forceinline__ long long split_begin(long long c, long long U, long long G) { return c * U / G; }
+
+// The first (b, h) pair, in (sequence, head) order, whose first unit (page) is at or after
+// unit x: the units of (b, h) start at cu[b] + h * (units of b) / H.  Block-role CTA c owns
+// the pairs that start in [c U / G, (c + 1) U / G), so every CTA of the role gets about the
+// same number of pages (pairs of long sequences count for more than short ones).
+__device__ __forceinline__ long long first_pair_at(const Shared& S, int batch, int H, long long x) {
+  if (x >= S.cu[batch]) return static_cast<long long>(batch) * H;
+  int lo = 0, hi = batch - 1;  // the sequence holding unit x: the smallest b with cu[b + 1] > x
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (S.cu[mid + 1] > x)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  const long long np = S.n_seq_units[lo] / H;  // > 0: the sequence holds unit x
+  const long long h = (x - S.cu[lo] + np - 1) / np;
+  return static_cast<long long>(lo) * H + h;  // h == H is the next sequence's head 0
+}
 
 // Walk over the units [u, u1).
 struct UWalk {
@@ -161,15 +186,13 @@ template <int D>
 __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CUtensorMap& tm_qb,
                                               const CUtensorMap& tm_qb64, const CUtensorMap& tm_k,
                                               const CUtensorMap& tm_v, const AttnArgs& a,
-                                              long long c, long long G) {
+                                              long long bh0, long long bh1) {
   using C = StreamCfg<D>;
   constexpr int TB = C::TB;
   constexpr float kRescale = 8.f;  // log2 units
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BatchArgs& bt = a.bt;
   const int H = a.n_heads;
-  const long long BH = static_cast<long long>(bt.batch) * H;
-  const long long bh0 = split_begin(c, BH, G), bh1 = split_begin(c + 1, BH, G);
   uint8_t* ring = smem;
   uint8_t* q_tile = smem + C::off_qb;
   uint8_t* p_tile = smem + C::off_p;
@@ -558,16 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     if (lane == 0) S.cu[bt.batch] = carry;
   }
   __syncthreads();
-  // Block role: CTA c owns the (b, h) pairs [c BH / G, (c + 1) BH / G), whole.
-  // Merge role: CTA c owns the units [c U / G, (c + 1) U / G).
+  // Block role: CTA c owns the (b, h) pairs, whole, that start in the units
+  // [c U / G, (c + 1) U / G) (about U / G pages each).  Merge role: CTA c owns the
+  // units [c U / G, (c + 1) U / G).
   const long long U = S.cu[bt.batch];
   const long long n_role = block_role ? n_block_ctas : n_merge_ctas;
   const long long c = block_role ? blockIdx.x : blockIdx.x - n_block_ctas;
   if (block_role) {
-    const long long BH = static_cast<long long>(bt.batch) * H;
-    const long long G = BH < n_role ? BH : n_role;
-    if (c >= G) return;  // uniform across the CTA
-    block_role_tc<D>(S, smem, tm_qb, tm_qb64, tm_k, tm_v, a, c, G);
+    const long long bh0 = first_pair_at(S, bt.batch, H, split_begin(c, U, n_role));
+    const long long bh1 = first_pair_at(S, bt.batch, H, split_begin(c + 1, U, n_role));
+    if (bh0 >= bh1) return;  // no pair starts in this CTA's range (uniform across the CTA)
+    block_role_tc<D>(S, smem, tm_qb, tm_qb64, tm_k, tm_v, a, bh0, bh1);
     return;
   }
   const long long G = U < n_role ? U : n_role;
@@ -730,8 +754,8 @@ cudaError_t launch_d(const AttnArgs& a, const AttnPlan& plan, cudaStream_t strea
 
 }  // namespace
 
-AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int num_sms, bool block,
-                   bool merge) {
+AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int total_seq_rows,
+                   int total_block_rows, int num_sms, bool block, bool merge) {
   (void)head_dim;
   (void)max_block_len;
   AttnPlan p = {};
@@ -740,10 +764,16 @@ AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int ma
   const long long units = bh * max_pages;  // upper bound of the merge role's units
   const int g = static_cast<int>(units < num_sms ? (units < 1 ? 1 : units) : num_sms);
   if (block && merge) {
-    // one block-role CTA per (b, h) while that is at most half of the CTAs (each
-    // owns whole (b, h) pairs: no cross-CTA merge); the rest take the merge role
-    const int half = g / 2 < 1 ? 1 : g / 2;
-    p.n_block_ctas = bh < half ? static_cast<int>(bh) : half;
+    // Split the CTAs between the roles by their work: both walk every page of every
+    // (sequence, head) (the block role its keys, the merge role its invariant rows), and a
+    // merge page (query page, fp32 O~ page, row out) costs kMergePageCost block pages.
+    const double merge_frac =
+        total_seq_rows > 0 ? static_cast<double>(total_seq_rows - total_block_rows) / total_seq_rows : 0.0;
+    long long nb = llround(g / (1.0 + kMergePageCost * merge_frac));
+    if (nb < 1) nb = 1;
+    if (nb > g - 1) nb = g - 1 < 1 ? 1 : g - 1;
+    if (nb > bh) nb = bh;
+    p.n_block_ctas = static_cast<int>(nb);
     p.n_merge_ctas = g - p.n_block_ctas < 1 ? 1 : g - p.n_block_ctas;
   } else {
     p.n_block_ctas = block ? static_cast<int>(bh < num_sms ? bh : num_sms) : 0;

@@ -109,7 +109,8 @@ AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cac
 }
 
 AttnPlan plan_of(const dllm_layer_desc* d, const dllm_batch* b, bool block, bool merge) {
-  return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, b->max_block_len, device_sms(), block, merge);
+  return attn_plan(b->batch, d->n_heads, d->head_dim, b->max_seq_len, b->max_block_len, b->total_seq_rows,
+                   b->total_block_rows, device_sms(), block, merge);
 }
 
 

@@ -113,8 +113,8 @@ struct AttnPlan {
   int n_block_ctas, n_merge_ctas;  // CTAs of each role (one CTA per SM in all)
   size_t total_bytes;              // workspace (none needed: 0)
 };
-AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int num_sms, bool block,
-                   bool merge);
+AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int total_seq_rows,
+                   int total_block_rows, int num_sms, bool block, bool merge);
 bool attn_batch_supported(int batch);
 
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) ------
