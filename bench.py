@@ -6,34 +6,41 @@ One step = one pass of the whole hot path for one layer: the fused RMSNorm +
 QKV projection + RoPE + paged K/V write of the block rows, the block
 attention over [prefix | block | suffix], and the FACache merge of every
 invariant row.  The metric is block-query tokens per second per layer-step
-(block rows of all sequences / step time).
+(block rows of all sequences / time of one layer-step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config stack|ragged|long|llada_single|tiny]
 
-Workload: the LLaDA-8B-shaped single layer (batch 1, d_model 4096, 32 heads
-x 128, RoPE theta 5e5, prompt 512, gen 256, block 32), synthetic seeded
-bf16 inputs and N(0, 0.02) weights.  Steps rotate over several independent
-layer instances (about 140 MB each), so no step finds its inputs in the
-129 MB L2.  The steps replay CUDA graphs of 32 layer-steps (8 rounds of the
-4 instances, as one forward over 32 layers would be; two kernels a step: the
-fused RMSNorm + projection + RoPE + K/V write, and the block attention +
-FACache merge launch); a sample of the steps (one round in 128) carries CUDA
-events around the projection call on its stream, which give its live
-duration for the roofline.  The end-to-end figure calls the public step API
-with the block rows copied in from pinned host memory and o_full read back to
-pinned host memory every step (the read-back on a copy stream, under the next
-step).
+Headline workload: the LLaDA-8B-shaped 32-layer attention stack (16
+sequences, prompt 1024, gen 512, block 32, d_model 4096, 32 heads x 128,
+RoPE theta 5e5), every layer with its own weights, paged cache and block
+rows: the timed steps walk the 32 layers in order, round after round (the
+metric is the mean over the layers).  Synthetic seeded bf16 inputs drawn on
+the device (N(0, 1) rows, N(0, 0.02) weights); each layer holds ~1.5 GB, so
+no step finds its inputs in the 129 MB L2.  The other LLaDA-shaped workloads
+(single layer, long context, ragged batch) are measured the same way on 4
+layer instances each and reported under "configs".
+
+Timing: CUDA graphs of 32 layer-steps (two kernels a step, chained by
+programmatic dependent launch), replayed back to back between CUDA events on
+the launching stream.  Inside the timed region one round of layer-steps in
+every 16 (always the first) is replayed call by call with events around each
+kernel: those give each kernel's duration for the roofline objects.  The
+end-to-end figure calls the public step API with the block rows copied in
+from pinned host memory and the block rows' outputs read back to pinned host
+memory every step (the read-back on a copy stream, under the next step).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload
 (sequences are independent units: weak scaling, no collective on the data
 path); the time is the max over ranks.
 
---impl reference times the fp64 CPU oracle (full recompute of the step) on
-the host cores, on a bounded sample of the same workload.
+--impl reference times the fp64 CPU oracle (full recompute of the step, all
+heads) on the host cores, one sequence of the workload per step.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -48,7 +55,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "llada_single"
+HEADLINE = "stack"
+SECONDARY = ("llada_single", "long", "ragged")
 METRIC = "block-query tokens/s per layer-step"
 UNIT = "tokens/s"
 
@@ -150,15 +158,38 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one projection
-# launch, per workload, from one ncu capture of the kernel as it stands
-# (--set full, the launch of an inner step); no entry: not captured.
-QKV_TRAFFIC_BYTES = {"llada_single": 103_979_008}
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a
+# kernel on a workload, from one ncu capture (summarised under profiles/),
+# with the hash of the kernel's sources at capture time: the figure is
+# reported only while the sources still hash the same (else null).
+KERNEL_SOURCES = {
+    "qkv": ("qkv_gemm.cu", "norm.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
+    "attention": ("attn_stream.cu", "attn_common.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
+}
+TRAFFIC = {
+    # (workload, kernel): (bytes per launch, sources hash)
+}
+
+
+def sources_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_wise_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(workload: str, kernel: str):
+    t = TRAFFIC.get((workload, kernel))
+    return t[0] if t is not None and t[1] == sources_hash(kernel) else None
 
 
 def step_bytes_flops(cfg, st):
     """Algorithmic bytes and flops of one layer-step (what the method must
-    move and compute), per part."""
+    move and compute), per part: the projection (a1-a4), the block attention
+    (a5) and the FACache merge (a6)."""
     D, H, d = cfg.d_model, cfg.n_heads, cfg.head_dim
     HD = H * d
     lay = st.batch.host
@@ -175,7 +206,7 @@ def step_bytes_flops(cfg, st):
     return dict(qkv=(qkv_bytes, qkv_flops), attention=(att_bytes, att_flops), merge=(mrg_bytes, mrg_flops))
 
 
-def describe(cfg) -> str:
+def describe(cfg, layers: int) -> str:
     """The workload, named by what it is with its sizes."""
     N = np.array([cfg.seq_len(b) for b in range(cfg.batch)], dtype=np.int64)
     M = int(sum(cfg.block))
@@ -185,14 +216,287 @@ def describe(cfg) -> str:
     else:
         seqs += f", prompt {min(cfg.t_prefix)}..{max(cfg.t_prefix)}, gen {sorted(set(cfg.gen_len))}, " \
                 f"block {sorted(set(cfg.block))}"
-    return (f"{cfg.name}: 1 layer step, d_model {cfg.d_model}, {cfg.n_heads}x{cfg.head_dim} heads, {seqs} "
+    what = f"{cfg.layers}-layer attention stack, layer-steps over all {layers} layers" if cfg.layers > 1 else \
+        f"1 layer step ({layers} independent layer instances rotated)"
+    return (f"{cfg.name}: {what}, d_model {cfg.d_model}, {cfg.n_heads}x{cfg.head_dim} heads, {seqs} "
             f"(M={M} block rows, N={int(N.sum())} rows)")
+
+
+def kernel_roofline(name, bytes_, flops, seconds, hbm, tflops_peak, workload, kernel_id):
+    """Roofline object of one kernel: bound by HBM or by the tensor pipe,
+    whichever gives the longer time at the measured peaks."""
+    t_hbm = bytes_ / (hbm * 1e9)
+    t_tc = flops / (tflops_peak * 1e12)
+    if t_tc > t_hbm:
+        achieved = flops / seconds / 1e12
+        obj = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1), "peak": tflops_peak,
+               "unit": "TFLOP/s", "frac": round(achieved / tflops_peak, 4), "algorithmic_flops": flops}
+    else:
+        achieved = bytes_ / seconds / 1e9
+        obj = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+               "frac": round(achieved / hbm, 4)}
+    obj["traffic"] = traffic_of(workload, kernel_id)
+    obj["algorithmic_bytes"] = bytes_
+    obj["t_roof_us"] = round(max(t_hbm, t_tc) * 1e6, 2)
+    obj["frac_of_roofline"] = round(max(t_hbm, t_tc) / seconds, 4)
+    obj["duration_us"] = round(seconds * 1e6, 2)
+    return obj
+
+
+class Instances:
+    """L independent layer instances of a workload (weights, paged cache after
+    the block boundary, block rows of one inner step), inputs drawn on the
+    device."""
+
+    def __init__(self, cfg, L, dev, seed):
+        from block_wise_kv_gb300.inputs import Workload
+        from block_wise_kv_gb300.step import LayerStep
+
+        self.cfg = cfg
+        wl = Workload(cfg.with_(seed=seed))
+        blocks = cfg.block_index
+        self.items = []
+        for layer in range(L):
+            W, g = wl.weights_device(layer, dev)
+            st = LayerStep(cfg, layer=layer, weights=(W, g), device=dev)
+            del W
+            x_full, x_blk = wl.batch_rows_device(layer, 1, blocks, dev)
+            st.boundary(x_full)
+            self.items.append((st, x_blk, x_full))
+        torch.cuda.synchronize()
+        for st, _, _ in self.items:
+            assert st.batch.error_bits() == 0, "device-side error during the block boundary"
+
+    def __len__(self):
+        return len(self.items)
+
+
+def measure(cfg, L, K, W, P, sample_every, dev, rank, ws, extras=True, e2e_steps=0):
+    """Time K layer-steps of workload `cfg` over L layer instances (max over
+    ranks), with per-kernel durations sampled inside the timed region; with
+    `extras`, also each call alone in steady state, the block-rows-only
+    variant, the block boundary, and (e2e_steps > 0) the end-to-end figure."""
+    inst = Instances(cfg, L, dev, seed=rank)
+    items = inst.items
+    M = items[0][0].batch.total_block_rows
+    P = max(1, P)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for st, xb, _ in items:
+            st.step(xb, stream=stream)
+        stream.synchronize()
+        # a round: one step of every instance (the projection call, then the block
+        # attention and the FACache merge in one launch); a pass: P rounds in one graph
+        g_round = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_round, stream=stream):
+            for st, xb, _ in items:
+                st.step(xb, stream=stream)
+        if P > 1:
+            g_pass = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_pass, stream=stream):
+                for _ in range(P):
+                    for st, xb, _ in items:
+                        st.step(xb, stream=stream)
+        else:
+            g_pass = g_round
+        g_step, g_qkv, g_att = [], [], []  # per instance: one step; the projection call; the attention call
+        for st, xb, _ in items:
+            for lst, fn in ((g_step, lambda: st.step(xb, stream=stream)), (g_qkv, lambda: st.qkv(xb, stream=stream)),
+                            (g_att, lambda: st.step_attention(stream))):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                lst.append(g)
+    torch.cuda.synchronize()
+
+    for i in range(W):
+        g_step[i % L].replay()
+    torch.cuda.synchronize()
+    n_rounds, tail = divmod(K, L)
+    n_passes, tail_rounds = divmod(n_rounds, P)
+    samples = []
+
+    def call_by_call(j):  # one step of instance j, each kernel between events
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        g_qkv[j].replay()
+        e[1].record(stream)
+        g_att[j].replay()
+        e[2].record(stream)
+        samples.append(e)
+
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks, torch.cuda.stream(stream):
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        t_start.record(stream)
+        for k in range(n_passes):
+            if k % sample_every == 0:  # the first round of this pass call by call
+                for j in range(L):
+                    call_by_call(j)
+                for _ in range(P - 1):
+                    g_round.replay()
+            else:
+                g_pass.replay()
+        for r in range(tail_rounds):
+            if not samples and r == 0:
+                for j in range(L):
+                    call_by_call(j)
+            else:
+                g_round.replay()
+        for j in range(tail):
+            if not samples:
+                call_by_call(j)
+            else:
+                g_step[j].replay()
+        t_end.record(stream)
+        stream.synchronize()
+        t1 = time.perf_counter()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    total_ms = _max_over_ranks(t_start.elapsed_time(t_end), ws)
+    qkv_ms = _max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in samples) / len(samples), ws)
+    att_ms = _max_over_ranks(sum(e[1].elapsed_time(e[2]) for e in samples) / len(samples), ws)
+    for st, _, _ in items:
+        assert st.batch.error_bits() == 0, "device-side error during the timed steps"
+    res = {"cfg": cfg, "L": L, "M": M, "st": items[0][0], "K": K, "total_ms": total_ms, "qkv_ms": qkv_ms,
+           "att_ms": att_ms, "n_samples": len(samples), "clocks": clocks.summary(), "host_wall_s": t1 - t0,
+           "P": P, "sample_every": sample_every}
+    if not extras:
+        return res
+
+    # each call alone in steady state: a graph of P rounds of one call kind, so
+    # consecutive launches of the same kernel overlap as in the step's graphs
+    steady = {}
+    n_rep = max(2, min(50, (K // (P * L)) or 2))
+    with torch.cuda.stream(stream):
+        for name, call in (("qkv_rope_write", lambda st, xb: st.qkv(xb, stream=stream)),
+                           ("step_attention", lambda st, xb: st.step_attention(stream)),
+                           ("block_rows_only", lambda st, xb: (st.qkv(xb, stream=stream), st.attention(stream)))):
+            g_one = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_one, stream=stream):
+                for _ in range(P):
+                    for st, xb, _ in items:
+                        call(st, xb)
+            for _ in range(2):
+                g_one.replay()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(n_rep):
+                g_one.replay()
+            s1.record(stream)
+            s1.synchronize()
+            steady[name] = _max_over_ranks(s0.elapsed_time(s1) / (n_rep * P * L), ws)
+            del g_one
+    res["steady_ms"] = steady
+
+    # the block boundary (cache build: projection of every row, FACache state over
+    # U x U), timed apart: once per block, amortised over the block's inner steps
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nb = max(2, min(2 * L, 16))
+    b0.record()
+    for i in range(nb):
+        st, _, x_full = items[i % L]
+        st.boundary(x_full)
+    b1.record()
+    torch.cuda.synchronize()
+    res["build_ms"] = _max_over_ranks(b0.elapsed_time(b1) / nb, ws)
+    for st, _, _ in items:
+        assert st.batch.error_bits() == 0, "device-side error in the block boundary"
+
+    if e2e_steps > 0:
+        res["e2e"] = e2e(items, min(K, e2e_steps), W, ws)
+    del g_round, g_pass, g_step, g_qkv, g_att
+    return res
+
+
+def e2e(items, Ke, W, ws):
+    """End to end through the public step API: every step copies its block
+    rows in from pinned host memory, runs the step and reads the block rows'
+    outputs (the rows a sampler consumes) back to pinned host memory.  The
+    read-back runs on a copy stream under the next step (another layer); a
+    layer's next step waits until its previous read-back is done."""
+    L = len(items)
+    st0 = items[0][0]
+    cu, sb, bl = (st0.batch.host[k] for k in ("cu_seq", "block_start", "block_len"))
+    rows = [(int(cu[b] + sb[b]), int(cu[b] + sb[b] + bl[b])) for b in range(st0.batch.batch)]
+    x_host = [xb.cpu().pin_memory() for _, xb, _ in items]
+    o_host = [torch.empty(st.q_block.shape, dtype=torch.bfloat16).pin_memory() for st, _, _ in items]
+    main = torch.cuda.current_stream()
+    copy_stream = torch.cuda.Stream()
+    read_out = [None] * L
+
+    def step(i):
+        j = i % L
+        st, xb, _ = items[j]
+        if read_out[j] is not None:
+            main.wait_event(read_out[j])
+        xb.copy_(x_host[j], non_blocking=True)
+        st.step(xb)
+        done = torch.cuda.Event()
+        done.record(main)
+        copy_stream.wait_event(done)
+        with torch.cuda.stream(copy_stream):
+            at = 0
+            for lo, hi in rows:
+                o_host[j][at:at + hi - lo].copy_(st.o_full[lo:hi], non_blocking=True)
+                at += hi - lo
+        ev = torch.cuda.Event()
+        ev.record(copy_stream)
+        read_out[j] = ev
+
+    for i in range(min(W, 8)):
+        step(i)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for i in range(Ke):
+        step(i)
+    main.wait_stream(copy_stream)  # the last read-back is inside the timed region
+    e1.record(main)
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(e0.elapsed_time(e1), ws)
+    return {"ms": ms, "steps": Ke, "h2d": x_host[0].numel() * x_host[0].element_size(),
+            "d2h": o_host[0].numel() * o_host[0].element_size()}
+
+
+def summarize(res, hbm, tf_burst, ws):
+    """Throughput, per-kernel durations and roofline objects of one measure()."""
+    cfg, st, M = res["cfg"], res["st"], res["M"]
+    bf = step_bytes_flops(cfg, st)
+    att_bytes = bf["attention"][0] + bf["merge"][0]
+    att_flops = bf["attention"][1] + bf["merge"][1]
+    q = kernel_roofline("dllm_block_qkv_rope_write (one kernel: RMSNorm, tcgen05 QKV GEMM, RoPE, paged K/V write)",
+                        bf["qkv"][0], bf["qkv"][1], res["qkv_ms"] * 1e-3, hbm, tf_burst, cfg.name, "qkv")
+    a = kernel_roofline("dllm_step_attention (one kernel: block attention over all keys + FACache merge of "
+                        "every invariant row)", att_bytes, att_flops, res["att_ms"] * 1e-3, hbm, tf_burst, cfg.name,
+                        "attention")
+    out = {"value": round(res["K"] * M * ws / (res["total_ms"] * 1e-3), 1), "ms_per_step": res["total_ms"] / res["K"],
+           "qkv_rope_write_us": round(res["qkv_ms"] * 1e3, 2), "step_attention_us": round(res["att_ms"] * 1e3, 2),
+           "roofline_kernels": {"qkv_rope_write": q, "step_attention": a},
+           "sampled_calls": res["n_samples"]}
+    if "steady_ms" in res:
+        sd = res["steady_ms"]
+        out["steady_state_us"] = {k: round(v * 1e3, 2) for k, v in sd.items()}
+        out["steady_state_us"]["how"] = (f"graphs of {res['P'] * res['L']} calls of one kind, replayed back to "
+                                         "back (launches overlapped as in the step)")
+        out["steady_state_frac"] = {
+            "qkv_rope_write": round(q["t_roof_us"] / (sd["qkv_rope_write"] * 1e3), 4),
+            "step_attention": round(att_bytes / (sd["step_attention"] * 1e-3) / 1e9 / hbm, 4),
+            "how": "qkv: t_roof over the steady-state duration; attention: algorithmic bytes / duration / HBM peak"}
+        out["block_rows_only"] = {"value": round(M * ws / (sd["block_rows_only"] * 1e-3), 1), "unit": UNIT,
+                                  "us_per_step": round(sd["block_rows_only"] * 1e3, 2)}
+    if "build_ms" in res:
+        out["cache_build_us"] = {"per_boundary": round(res["build_ms"] * 1e3, 1),
+                                 "per_inner_step": round(res["build_ms"] * 1e3 / cfg.steps_per_block, 2)}
+    return out
 
 
 def run_ours(args, rank, ws, local):
     from block_wise_kv_gb300 import build, dllm
-    from block_wise_kv_gb300.inputs import Workload, make_config
-    from block_wise_kv_gb300.step import LayerStep, block_rows_of, full_rows_of
+    from block_wise_kv_gb300.inputs import make_config
 
     if rank == 0:
         build.build()
@@ -200,274 +504,72 @@ def run_ours(args, rank, ws, local):
     dllm.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    hbm, tf_burst, tf_sus, peak_kind = _peaks()
     cfg = make_config(args.config)
-    wl = Workload(cfg.with_(seed=rank))
-    blocks = cfg.block_index
-    L = args.layers
-    inst = []
-    for layer in range(L):
-        st = LayerStep(cfg, layer=layer)
-        st.boundary(full_rows_of(wl, layer, 0, blocks).to(dev))
-        xb = block_rows_of(wl, layer, 1, blocks).to(dev)
-        inst.append((st, xb))
-    torch.cuda.synchronize()
-    for st, _ in inst:
-        assert st.batch.error_bits() == 0, "device-side error during setup"
-    M = inst[0][0].batch.total_block_rows
-
-    # CUDA graphs.  A round is one step of every instance (L steps: the
-    # projection call, then the block attention and the FACache merge in one
-    # launch); a pass is P rounds in one graph (P L layer-steps, as one
-    # forward over the layers of a model would be), so consecutive kernels
-    # keep their programmatic-dependent-launch overlap.  In every
-    # `sample_every`-th pass the first round replays per-instance pieces
-    # instead, with CUDA events around the projection call on its stream:
-    # those give the projection's live duration for the roofline, inside the
-    # timed region.
-    P = max(1, args.rounds_per_graph)
-    stream = torch.cuda.Stream()
-    with torch.cuda.stream(stream):
-        for st, xb in inst:
-            st.step(xb, stream=stream)
-        stream.synchronize()
-        g_round = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_round, stream=stream):
-            for st, xb in inst:
-                st.step(xb, stream=stream)
-        g_pass = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_pass, stream=stream):
-            for _ in range(P):
-                for st, xb in inst:
-                    st.step(xb, stream=stream)
-        g_step, g_qkv, g_rest = [], [], []  # one step; the projection call; the attention call
-        for st, xb in inst:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st.step(xb, stream=stream)
-            g_step.append(g)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st.qkv(xb, stream=stream)
-            g_qkv.append(g)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st.step_attention(stream)
-            g_rest.append(g)
-    torch.cuda.synchronize()
-
-    K, W = args.steps, args.warmup
-    sample_every = max(1, args.sample_every)
-    for i in range(W):
-        g_step[i % L].replay()
-    torch.cuda.synchronize()
-    n_rounds, tail = divmod(K, L)
-    n_passes, tail_rounds = divmod(n_rounds, P)
-    qkv_ev = []
-    _barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks, torch.cuda.stream(stream):
-        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        t_start.record(stream)
-        for k in range(n_passes):
-            if k % sample_every == sample_every - 1:
-                for j in range(L):
-                    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-                    e[0].record(stream)
-                    g_qkv[j].replay()
-                    e[1].record(stream)
-                    g_rest[j].replay()
-                    e[2].record(stream)
-                    qkv_ev.append(e)
-                for _ in range(P - 1):
-                    g_round.replay()
-            else:
-                g_pass.replay()
-        for _ in range(tail_rounds):
-            g_round.replay()
-        for j in range(tail):
-            g_step[j].replay()
-        t_end.record(stream)
-        stream.synchronize()
-        t1 = time.perf_counter()
-    torch.cuda.synchronize()
-    _barrier(ws)
-    total_ms = t_start.elapsed_time(t_end)
-    if not qkv_ev:  # too few rounds to sample: time the projection alone after the region
-        with torch.cuda.stream(stream):
-            for j in range(L):
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-                e[0].record(stream)
-                g_qkv[j].replay()
-                e[1].record(stream)
-                g_rest[j].replay()
-                e[2].record(stream)
-                qkv_ev.append(e)
-        torch.cuda.synchronize()
-    qkv_ms = sum(e[0].elapsed_time(e[1]) for e in qkv_ev) / len(qkv_ev)
-    attn_ms = sum(e[1].elapsed_time(e[2]) for e in qkv_ev) / len(qkv_ev)
-    total_ms = _max_over_ranks(total_ms, ws)
-    for st, _ in inst:
-        assert st.batch.error_bits() == 0, "device-side error during the timed steps"
-
-    # end to end through the public API: pinned host input -> step -> host output.
-    # The read-back of a step's o_full runs on a copy stream while the next
-    # step (another layer instance) computes; a layer instance's next step
-    # waits until its previous o_full has been read out.
-    x_host = [xb.cpu().pin_memory() for _, xb in inst]
-    o_host = [torch.empty_like(st.o_full, device="cpu").pin_memory() for st, _ in inst]
-    x_dev = [torch.empty_like(xb) for _, xb in inst]
-    Ke = max(1, min(K, args.e2e_steps))
-    main = torch.cuda.current_stream()
-    copy_stream = torch.cuda.Stream()
-    read_out = [None] * L
-
-    def e2e_step(i):
-        j = i % L
-        st, _ = inst[j]
-        if read_out[j] is not None:
-            main.wait_event(read_out[j])
-        x_dev[j].copy_(x_host[j], non_blocking=True)
-        st.step(x_dev[j])
-        done = torch.cuda.Event()
-        done.record(main)
-        copy_stream.wait_event(done)
-        with torch.cuda.stream(copy_stream):
-            o_host[j].copy_(st.o_full, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(copy_stream)
-        read_out[j] = ev
-
-    for i in range(min(W, 8)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    _barrier(ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    for i in range(Ke):
-        e2e_step(i)
-    main.wait_stream(copy_stream)  # the last read-back is inside the timed region
-    e1.record(main)
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
-    h2d = x_host[0].numel() * x_host[0].element_size()
-    d2h = o_host[0].numel() * o_host[0].element_size()
-
-    # secondary: the block rows only (projection + block attention, no FACache
-    # merge of the invariant rows: what a DualCache consumer of the block
-    # outputs needs), graph-replayed like the main loop
-    with torch.cuda.stream(stream):
-        g_blk = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_blk, stream=stream):
-            for _ in range(P):
-                for st, xb in inst:
-                    st.qkv(xb, stream=stream)
-                    st.attention(stream)
-        for _ in range(3):
-            g_blk.replay()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_blk = max(1, min(n_passes, 100))
-        k0.record(stream)
-        for _ in range(n_blk):
-            g_blk.replay()
-        k1.record(stream)
-    torch.cuda.synchronize()
-    blk_ms = _max_over_ranks(k0.elapsed_time(k1), ws) / (n_blk * P * L)
-
-    # secondary: each call of the step alone in steady state (a graph of P
-    # rounds of that call only, so consecutive launches of the same kernel
-    # overlap through programmatic dependent launch as in the step's graphs)
-    steady = {}
-    with torch.cuda.stream(stream):
-        for name, call in (("qkv_rope_write", lambda st, xb: st.qkv(xb, stream=stream)),
-                           ("step_attention", lambda st, xb: st.step_attention(stream))):
-            g_one = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_one, stream=stream):
-                for _ in range(P):
-                    for st, xb in inst:
-                        call(st, xb)
-            for _ in range(3):
-                g_one.replay()
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n_one = max(1, min(n_passes, 100))
-            s0.record(stream)
-            for _ in range(n_one):
-                g_one.replay()
-            s1.record(stream)
-            s1.synchronize()
-            steady[name] = s0.elapsed_time(s1) / (n_one * P * L)
-    steady = {k: _max_over_ranks(v, ws) for k, v in steady.items()}
-
-    # the block boundary (cache build: projection of every row, FACache state
-    # over U x U), timed apart: once per block, amortised over its inner steps
-    x_full = [full_rows_of(wl, layer, 0, blocks).to(dev) for layer in range(L)]
-    for j in range(L):
-        inst[j][0].boundary(x_full[j])
-    torch.cuda.synchronize()
-    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nb = 2 * L
-    b0.record()
-    for i in range(nb):
-        inst[i % L][0].boundary(x_full[i % L])
-    b1.record()
-    torch.cuda.synchronize()
-    build_ms = b0.elapsed_time(b1) / nb
-
+    L = cfg.layers if cfg.layers > 1 else args.layers
+    P = max(1, 32 // L)  # a graph holds 32 layer-steps
+    res = measure(cfg, L, args.steps, args.warmup, P, args.sample_every, dev, rank, ws, extras=True,
+                  e2e_steps=args.e2e_steps)
+    head = summarize(res, hbm, tf_burst, ws)
+    e = res["e2e"]
+    M = res["M"]
+    clocks, wall = res["clocks"], res["host_wall_s"]
+    del res
+    torch.cuda.empty_cache()
+    configs = {}
+    if not args.headline_only and cfg.name == HEADLINE:
+        for name in SECONDARY:
+            c2 = make_config(name)
+            r2 = measure(c2, args.layers, args.secondary_steps, args.warmup, max(1, 32 // args.layers),
+                         args.sample_every, dev, rank, ws, extras=True)
+            s2 = summarize(r2, hbm, tf_burst, ws)
+            s2["workload"] = describe(c2, args.layers)
+            s2["steps"] = args.secondary_steps
+            configs[name] = s2
+            del r2
+            torch.cuda.empty_cache()
     if rank != 0:
         return None
-    hbm, tf_burst, tf_sus, peak_kind = _peaks()
-    bf = step_bytes_flops(cfg, inst[0][0])
-    qkv_bytes, qkv_flops = bf["qkv"]
-    t_qkv = qkv_ms * 1e-3
-    achieved = qkv_bytes / t_qkv / 1e9
-    value = K * M * ws / (total_ms * 1e-3)
+    rk = head["roofline_kernels"]
+    dominant = max(rk.values(), key=lambda o: o["duration_us"])
     line = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": head["value"],
         "unit": UNIT,
         "n_gpus": ws,
-        "steps": K,
-        "warmup": W,
-        "ms_per_step": total_ms / K,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": describe(cfg),
-                   "l2": f"inputs larger than L2: {L} rotating layer instances (~140 MB each)",
-                   "graphs": f"one CUDA graph per pass of {P} rounds x {L} steps ({P * L} layer-steps); the first "
-                             f"round of every {sample_every}th pass replayed per call with events around the "
-                             "projection",
+        "data": "synthetic (seeded, drawn on the device)",
+        "config": {"workload": describe(cfg, L),
+                   "l2": f"inputs larger than L2: {L} layer instances of ~1-3 GB each, walked in order",
+                   "graphs": f"CUDA graphs of {P * L} layer-steps (2 kernels each, chained by programmatic "
+                             f"dependent launch); the first round of every {args.sample_every}th graph (always the "
+                             "first) replayed call by call with events around each kernel",
                    "parallelism": f"replicas x{ws} (sequences are independent units)"},
-        "qkv_rope_write_us": round(qkv_ms * 1e3, 2),
-        "step_attention_us": round(attn_ms * 1e3, 2),
-        "step_attention_gbs": round((bf["attention"][0] + bf["merge"][0]) / (attn_ms * 1e-3) / 1e9, 1),
-        "steady_state_us": {"qkv_rope_write": round(steady["qkv_rope_write"] * 1e3, 2),
-                            "step_attention": round(steady["step_attention"] * 1e3, 2),
-                            "how": f"graphs of {P * L} calls of one kind, replayed back to back"},
-        "block_rows_only": {"value": round(M * ws / (blk_ms * 1e-3), 1), "unit": UNIT,
-                            "us_per_step": round(blk_ms * 1e3, 2)},
-        "cache_build_us": {"per_boundary": round(build_ms * 1e3, 1),
-                           "per_inner_step": round(build_ms * 1e3 / cfg.steps_per_block, 2)},
-        "roofline": {"kernel": "dllm_block_qkv_rope_write (one kernel: RMSNorm, tcgen05 QKV GEMM, RoPE and the "
-                               "paged K/V write)",
-                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": QKV_TRAFFIC_BYTES.get(cfg.name),
-                     "algorithmic_bytes": qkv_bytes, "peak_source": f"{peak_kind} hbm_gbs",
-                     "steady_state": {"achieved": round(qkv_bytes / (steady["qkv_rope_write"] * 1e-3) / 1e9, 1),
-                                      "frac": round(qkv_bytes / (steady["qkv_rope_write"] * 1e-3) / 1e9 / hbm, 4),
-                                      "how": "the same bytes over the per-call duration in graphs of "
-                                             f"{P * L} projection calls (launches overlapped as in the step)"}},
-        "e2e": {"value": round(Ke * M * ws / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
-        "gpu_launches": 2 * K,
-        "host_wall_s": t1 - t0,
+        "qkv_rope_write_us": head["qkv_rope_write_us"],
+        "step_attention_us": head["step_attention_us"],
+        "steady_state_us": head["steady_state_us"],
+        "steady_state_frac": head["steady_state_frac"],
+        "block_rows_only": head["block_rows_only"],
+        "cache_build_us": head["cache_build_us"],
+        "roofline": {k: v for k, v in dominant.items()},
+        "roofline_kernels": rk,
+        "peak_source": f"{peak_kind} MEASURED_PEAKS hbm_gbs / bf16_tflops (burst: each kernel timed alone)",
+        "e2e": {"value": round(e["steps"] * M * ws / (e["ms"] * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "steps": e["steps"],
+                "how": "x_block in from pinned host memory, the step through the public API, the block rows' "
+                       "outputs read back to pinned host memory, every step"},
+        "gpu_launches": 2 * args.steps,
+        "sampled_calls": head["sampled_calls"],
+        "host_wall_s": wall,
+        "clocks": clocks,
+        "configs": configs,
     }
-    cl = clocks.summary()
-    line["clocks"] = cl
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
     return line
 
 
@@ -485,9 +587,9 @@ def _oracle_inputs(cfg, wl, step):
     return _ORACLE_INPUTS[key]
 
 
-def _oracle_sample(cfg, wl, heads, step):
-    """The oracle's full-recompute layer step restricted to `heads` (every
-    row's output for those heads; RMSNorm, K/V of all rows, attention)."""
+def _oracle_step(cfg, wl, heads, step):
+    """The oracle's full-recompute layer step of sequence 0 (every row's output
+    for `heads`, None = all: RMSNorm, the projection, RoPE, attention)."""
     import oracle as orc
 
     x, g, W = _oracle_inputs(cfg, wl, step)
@@ -496,25 +598,24 @@ def _oracle_sample(cfg, wl, heads, step):
 
 def cpu_baseline(cfg, seconds: float):
     """The oracle as it stands, timed on this host's cores on a bounded
-    sample: the full step for one head at a time, repeated for about
-    `seconds`, scaled to all heads."""
+    sample: sequence 0's full-recompute step for one head at a time, repeated
+    for about `seconds`, scaled to all heads."""
     import oracle as orc
     from block_wise_kv_gb300.inputs import Workload
 
     wl = Workload(cfg)
     M = cfg.block[0]  # the sample is sequence 0: its block rows per step
-    _oracle_sample(cfg, wl, [0], 1)  # warm: builds/loads the library, generates the inputs
+    _oracle_step(cfg, wl, [0], 1)  # warm: builds/loads the library, generates the inputs
     n, t = 0, 0.0
     while t < seconds and n < cfg.n_heads:
         t0 = time.perf_counter()
-        _oracle_sample(cfg, wl, [n % cfg.n_heads], 1)
+        _oracle_step(cfg, wl, [n % cfg.n_heads], 1)
         t += time.perf_counter() - t0
         n += 1
     per_step = t / n * cfg.n_heads
     return {"value": round(M / per_step, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
-            "sample": f"full-recompute layer step (fp64) of sequence 0 for {n} of {cfg.n_heads} heads of "
-                      f"{cfg.name}, {t:.1f} s, scaled to all heads" + ("" if cfg.batch == 1 else
-                                                                        " (sequence 0 only)")}
+            "sample": f"full-recompute layer step (fp64) of sequence 0 of {cfg.batch} for {n} of {cfg.n_heads} "
+                      f"heads of {cfg.name}, {t:.1f} s, scaled to all heads; rate of that one sequence"}
 
 
 def run_reference(args, rank, ws):
@@ -525,23 +626,22 @@ def run_reference(args, rank, ws):
 
     cfg = make_config(args.config)
     wl = Workload(cfg)
-    M = cfg.block[0]  # each step samples sequence 0: its block rows per step
+    M = cfg.block[0]  # each step is sequence 0: its block rows
     _oracle_inputs(cfg, wl, 1)
     K, W = args.steps_ref, args.warmup_ref
-    for i in range(W):
-        _oracle_sample(cfg, wl, [i % cfg.n_heads], 1)
+    for _ in range(W):
+        _oracle_step(cfg, wl, None, 1)
     t0 = time.perf_counter()
-    for i in range(K):
-        _oracle_sample(cfg, wl, [i % cfg.n_heads], 1)
+    for _ in range(K):
+        _oracle_step(cfg, wl, None, 1)
     t = time.perf_counter() - t0
-    per_step = t / K * cfg.n_heads
+    per_step = t / K
     value = M / per_step
-    sample = (f"each step: full-recompute layer step (fp64) of sequence 0 for one head of {cfg.n_heads}, scaled "
-              "to all heads" + ("" if cfg.batch == 1 else "; rate of one sequence"))
+    sample = (f"each step: the full-recompute layer step (fp64, all {cfg.n_heads} heads) of sequence 0 of "
+              f"{cfg.batch} of {cfg.name}; value = that sequence's block rows / step time")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
             "steps": K, "warmup": W, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(cfg)},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": describe(cfg, 1)},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -550,29 +650,34 @@ def run_reference(args, rank, ws):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=6400)
+    ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", default=WORKLOAD)
-    ap.add_argument("--layers", type=int, default=4, help="rotating layer instances (inputs larger than L2)")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
-    ap.add_argument("--rounds-per-graph", type=int, default=8,
-                    help="rounds of steps (one step of every layer instance each) captured in one graph")
+    ap.add_argument("--config", default=HEADLINE)
+    ap.add_argument("--layers", type=int, default=4,
+                    help="layer instances of a one-layer workload (the stack uses all of its layers)")
+    ap.add_argument("--e2e-steps", type=int, default=512)
+    ap.add_argument("--secondary-steps", type=int, default=1024)
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads' figures")
     ap.add_argument("--sample-every", type=int, default=16,
-                    help="the first round of every n-th pass carries events around the projection call")
+                    help="the first round of every n-th graph (and always of the first) runs call by call")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     rank, ws, local = _dist()
     if args.impl == "reference":
-        # each reference step is one head's full recompute: keep the run to minutes
-        args.steps_ref = max(1, min(args.steps, 32))
-        args.warmup_ref = max(1, min(args.warmup, 2))
+        # each reference step is one sequence's full recompute: keep the run to minutes
+        args.steps_ref = max(1, min(args.steps, 8))
+        args.warmup_ref = max(1, min(args.warmup, 1))
         line = run_reference(args, rank, ws)
     else:
         if ws != args.gpus and rank == 0:
             print(f"note: --gpus {args.gpus} but WORLD_SIZE {ws}", file=sys.stderr)
         line = run_ours(args, rank, ws, local)
+        if line is not None and not args.no_cpu_baseline:
+            from block_wise_kv_gb300.inputs import make_config
+
+            line["cpu_baseline"] = cpu_baseline(make_config(args.config), args.cpu_seconds)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if ws > 1:

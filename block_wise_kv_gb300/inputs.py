@@ -2,9 +2,10 @@
 
 This module is the only piece shared by the CUDA path's tests/bench and the
 oracle: it draws numbers and lays out the batch, and holds none of the
-method's arithmetic.  Everything is generated on the CPU with
-``torch.Generator`` seeded through SplitMix64, so both sides see identical
-bf16 values.
+method's arithmetic.  Everything the parity checks use is generated on the
+CPU with ``torch.Generator`` seeded through SplitMix64, so both sides see
+identical bf16 values; the ``*_device`` variants draw the same layout and
+distributions on a CUDA device, for throughput measurements only.
 
 Workloads (named after the shapes they have):
 
@@ -203,6 +204,40 @@ class Workload:
         blocks = c.block_index if blocks is None else blocks
         full = [self.seq_rows(layer, b, blocks[b], step) for b in range(c.batch)]
         blk = [self.block_rows(layer, b, blocks[b], step) for b in range(c.batch)]
+        return torch.cat(full, 0).contiguous(), torch.cat(blk, 0).contiguous()
+
+    # ------------------------------------------------- device-drawn variants
+    # The same layout and distributions drawn on a CUDA device by a seeded device
+    # generator, for throughput measurements at sizes where drawing on the CPU
+    # takes minutes (the 32-layer stack holds 25 k rows x 4096 per layer).  The
+    # values differ from the CPU draws above, which the parity tests use.
+    def weights_device(self, layer: int, device) -> tuple:
+        c = self.cfg
+        HD = c.n_heads * c.head_dim
+        g = torch.Generator(device=device)
+        g.manual_seed(derive_seed(c.seed, _R_WEIGHT, layer))
+        W = (torch.randn(3 * HD, c.d_model, generator=g, device=device) * 0.02).to(torch.bfloat16)
+        return W, torch.ones(c.d_model, dtype=torch.bfloat16, device=device)
+
+    def batch_rows_device(self, layer: int, step: int, blocks, device) -> tuple:
+        """(x_full [R, D], x_block [M, D]) on the device, packed in sequence
+        order: per sequence prompt | decoded blocks | block (this step) | the
+        shared mask row repeated over the suffix."""
+        c = self.cfg
+        if c.embedding:
+            full, blk = self.batch_rows(layer, step, blocks)
+            return full.to(device), blk.to(device)
+        full, blk = [], []
+        for b in range(c.batch):
+            g = torch.Generator(device=device)
+            g.manual_seed(derive_seed(c.seed, _R_PROMPT, layer, b, blocks[b], step))
+            k = blocks[b]
+            s0 = c.t_prefix[b] + k * c.block[b]
+            head = torch.randn(s0 + c.block[b], c.d_model, generator=g, device=device).to(torch.bfloat16)
+            mask = torch.randn(1, c.d_model, generator=g, device=device).to(torch.bfloat16)
+            n_suffix = c.gen_len[b] - (k + 1) * c.block[b]
+            full.append(torch.cat([head, mask.expand(n_suffix, c.d_model)], 0))
+            blk.append(head[s0:])
         return torch.cat(full, 0).contiguous(), torch.cat(blk, 0).contiguous()
 
     # ---------------------------------------------------------------- layout

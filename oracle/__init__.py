@@ -6,8 +6,8 @@ TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 package.  The CUDA library and its Python binding never do; the two sides
 share no code (only the seeded input generator feeds both).
 
-The arithmetic lives in ``oracle.cpp`` (fp64, OpenMP over independent
-outputs).  This module loads it with ctypes and composes the plain definition
+All of the arithmetic lives in ``oracle.cpp`` (fp64, OpenMP over independent
+outputs), the projection included.  This module loads it with ctypes and composes the plain definition
 of the step:
 
   1. x^ = RMSNorm(x) for every row                  (LaCache §3.3.2, Eq. (1))
@@ -221,10 +221,9 @@ def alg1(q, k, v, scale: float, c_lo: int, c_hi: int, br: int, bc: int, genstep:
 
 
 def project(x: np.ndarray, W: np.ndarray) -> np.ndarray:
-    """x [rows, D] times W^T through numpy's fp64 matmul (a library primitive,
-    used for the projection at full model sizes; the plain loop `linear`
-    pins it on small inputs)."""
-    return np.ascontiguousarray(np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T)
+    """x [rows, D] times W^T: the projection of the step, `orc_linear`'s plain
+    sums in oracle.cpp (pinned against numpy's matmul)."""
+    return linear(x, W)
 
 
 # ---------------------------------------------------------------- the step

@@ -90,15 +90,25 @@ void orc_rmsnorm(const double* x, int64_t rows, int64_t D, const double* g, doub
 
 // Linear projection without bias (LaCache Eq. (1), H^ W):
 //   out[r][n] = sum_k x[r][k] * W[n][k]      (W stored [nout][D], row-major)
+// Each output is the plain sum over k in order, starting from 0.  Eight
+// outputs of a row are summed side by side (eight independent running sums,
+// so the additions of different outputs overlap in the pipeline); the last
+// group repeats the last weight row for the missing outputs and drops them.
 void orc_linear(const double* x, int64_t rows, int64_t D, const double* W, int64_t nout, double* out) {
+  const int64_t ngroups = (nout + 7) / 8;
 #pragma omp parallel for schedule(static)
-  for (int64_t n = 0; n < nout; ++n) {
-    const double* w = W + n * D;
+  for (int64_t gi = 0; gi < ngroups; ++gi) {
+    const double* w[8];
+    for (int i = 0; i < 8; ++i) {
+      const int64_t n = gi * 8 + i < nout ? gi * 8 + i : nout - 1;
+      w[i] = W + n * D;
+    }
     for (int64_t r = 0; r < rows; ++r) {
       const double* xr = x + r * D;
-      double acc = 0.0;
-      for (int64_t k = 0; k < D; ++k) acc += xr[k] * w[k];
-      out[r * nout + n] = acc;
+      double acc[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
+      for (int64_t k = 0; k < D; ++k)
+        for (int i = 0; i < 8; ++i) acc[i] += xr[k] * w[i][k];
+      for (int i = 0; i < 8 && gi * 8 + i < nout; ++i) out[r * nout + gi * 8 + i] = acc[i];
     }
   }
 }

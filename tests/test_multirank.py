@@ -58,7 +58,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     rank 0 alone runs the oracle and prints one JSON line; rank 1 exits 0."""
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
            "127.0.0.1", "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"), "--impl", "reference",
-           "--gpus", "2", "--steps", "1", "--warmup", "1"]
+           "--gpus", "2", "--steps", "1", "--warmup", "1", "--config", "llada_single"]
     env = dict(os.environ, OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]

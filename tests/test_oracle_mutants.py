@@ -19,7 +19,9 @@ MUTANTS = {
     "rope_sign": ("v[i] = a * c - b * s;", "v[i] = a * c + b * s;"),
     "rope_frequency": ("-2.0 * (double)i / (double)d", "-1.0 * (double)i / (double)d"),
     "rope_pairing": ("const double a = v[i], b = v[i + half];", "const double a = v[i], b = v[(i + 1) % d];"),
-    "linear_transposed": ("acc += xr[k] * w[k];", "acc += xr[k] * W[k * nout + n];"),
+    "linear_transposed": ("acc[i] += xr[k] * w[i][k];", "acc[i] += xr[k] * W[k * nout + gi * 8 + i];"),
+    "linear_group_offset": ("const int64_t n = gi * 8 + i < nout ? gi * 8 + i : nout - 1;",
+                            "const int64_t n = gi * 8 + i + 1 < nout ? gi * 8 + i + 1 : nout - 1;"),
     "rms_mean_divisor": ("ss / (double)D + eps", "ss / (double)(D - 1) + eps"),
     "rms_no_eps": ("ss / (double)D + eps", "ss / (double)D"),
     "attention_no_scale": ("S[j] = scale * dot;", "S[j] = dot;"),

@@ -82,12 +82,15 @@ def test_rmsnorm_constant_and_scale_invariance():
 
 # ---------------------------------------------------------------- linear ----
 def test_linear_matches_numpy():
-    # the plain C loop and numpy's matmul (used by the step at full size) agree
+    # the step's projection is orc_linear's plain sums; numpy's matmul (a library
+    # routine) pins it, for output counts below, at and above a group of eight and
+    # with a ragged last group
     g = _rng(4)
-    x = g.standard_normal((9, 48))
-    W = g.standard_normal((30, 48))
-    np.testing.assert_allclose(orc.linear(x, W), x @ W.T, rtol=1e-13, atol=1e-13)
-    np.testing.assert_allclose(orc.project(x, W), orc.linear(x, W), rtol=1e-13, atol=1e-13)
+    for rows, D, nout in ((9, 48, 30), (3, 17, 5), (4, 64, 16), (2, 33, 8), (5, 40, 1)):
+        x = g.standard_normal((rows, D))
+        W = g.standard_normal((nout, D))
+        np.testing.assert_allclose(orc.linear(x, W), x @ W.T, rtol=1e-13, atol=1e-13)
+        np.testing.assert_array_equal(orc.project(x, W), orc.linear(x, W))
 
 
 # ------------------------------------------------------------------ RoPE ----
