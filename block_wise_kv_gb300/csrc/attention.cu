@@ -8,7 +8,7 @@
 // query page and every 64-token K/V page of the sequence with TMA (128-byte
 // swizzle) into an mbarrier ring; 4 warps run QK^T / PV of their 16 query
 // rows on mma.sync m16n8k16 with keys of C masked out.  The block attention
-// and the FACache merge of the inner steps are in step_attention.cu.
+// and the FACache merge of the inner steps are in attn_stream.cu.
 #include "attn_common.cuh"
 
 namespace dllm {

@@ -14,7 +14,11 @@
 // host code its name is only a host-side stand-in, so its device address is
 // looked up once per device with cudaGetSymbolAddress (with that device
 // current) and cached; that lookup happens on the first call on each device,
-// so the first call on a device should come before any stream capture.
+// so the first call on a device should come before any stream capture.  The
+// cached address belongs to the device's current context: after a
+// cudaDeviceReset the library's module is loaded again and the array may move,
+// so a process that resets a device must not call this entry point on that
+// device again (the cached address would be stale).
 //
 // All calls share the array and it keeps the last call's contents.  A call
 // writes every scale and partial tile before it reads it, and the counters
@@ -43,7 +47,10 @@ dllm_status scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DLLM_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // clear the failed lookup's error: later, unrelated calls must not report it
+      return DLLM_ERR_CUDA;
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];

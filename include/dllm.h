@@ -231,7 +231,10 @@ dllm_status dllm_block_qkv_rope_write(const dllm_layer_desc* desc, const dllm_ba
  * rows); a larger need returns DLLM_ERR_WORKSPACE_TOO_SMALL and launches
  * nothing.  The first call
  * on each device looks up the array's device address with that device
- * current (make that first call before any stream capture).  All calls share
+ * current (make that first call before any stream capture) and keeps it for the
+ * life of the process: after cudaDeviceReset on a device the array may move,
+ * so do not call this entry point on a device again after resetting it.  All
+ * calls share
  * the array: calls whose GPU work may overlap (different streams without
  * ordering) race on it.  Arguments, layouts and results are otherwise those
  * of dllm_block_qkv_rope_write. */

@@ -8,7 +8,11 @@ the same blocks and steps; for the ragged batch (shuffled physical pages),
 every sequence at its own block index, steps {first, last}.  Each sampled
 sequence is compared on every row (block rows and invariant rows) for two
 heads (one for the ragged batch, rotating over the sequences), together
-with the block rows' stored k and v.
+with the block rows' stored k and v.  Further units compare all 32 heads
+(the 32-layer stack and the long-context batch: sequences {0, last}; the
+ragged batch: four sequences), and one stack unit runs the attention as the
+two separate calls (block attention, then the FACache merge), each with its
+own launch plan.
 """
 import numpy as np
 import pytest
@@ -32,7 +36,7 @@ def _lib():
     torch.cuda.init()
 
 
-def _check(cfg, layer, k_of, steps, seqs, heads_of):
+def _check(cfg, layer, k_of, steps, seqs, heads_of, split=False):
     wl = Workload(cfg)
     W, g = wl.weights(layer)
     st = LayerStep(cfg, layer=layer, blocks=k_of, weights=(W, g))
@@ -41,13 +45,14 @@ def _check(cfg, layer, k_of, steps, seqs, heads_of):
     assert st.batch.error_bits() == 0
     Wd, gd = W.double().numpy(), g.double().numpy()
     for s in steps:
-        st.step(block_rows_of(wl, layer, s, k_of).cuda())
+        st.step(block_rows_of(wl, layer, s, k_of).cuda(), split=split)
         torch.cuda.synchronize()
         assert st.batch.error_bits() == 0
         for b in seqs:
             heads = list(heads_of(b))
             x = wl.seq_rows(layer, b, k_of[b], s).double().numpy()
-            ref = orc.layer_step(x, gd, Wd, cfg.n_heads, cfg.head_dim, cfg.rope_theta, cfg.rms_eps, heads=heads)
+            ref = orc.layer_step(x, gd, Wd, cfg.n_heads, cfg.head_dim, cfg.rope_theta, cfg.rms_eps,
+                                 heads=None if len(heads) == cfg.n_heads else heads)
             what = f"{cfg.name} layer {layer} seq {b} block {k_of[b]} step {s} heads {heads}"
             o = to_np(st.o_full[st.seq_slice(b)][:, heads])
             lse = to_np(st.lse[st.seq_slice(b)][:, heads])
@@ -86,3 +91,28 @@ def test_ragged_every_sequence():
     assert cfg.shuffle_pages
     _check(cfg, 0, list(cfg.block_index), (0, cfg.steps_per_block - 1), range(cfg.batch),
            lambda b: ((7 * b) % cfg.n_heads,))
+
+
+ALL = lambda b: range(32)  # noqa: E731
+
+
+def test_stack_all_heads():
+    cfg = make_config("stack")
+    mid = cfg.num_blocks(0) // 2
+    _check(cfg, 0, [mid] * cfg.batch, (cfg.steps_per_block - 1,), (0, cfg.batch - 1), ALL)
+
+
+def test_stack_split_calls():
+    cfg = make_config("stack")
+    _check(cfg, cfg.layers - 1, [0] * cfg.batch, (0,), (0, cfg.batch - 1), lambda b: (5, 17), split=True)
+
+
+def test_long_context_all_heads():
+    cfg = make_config("long")
+    mid = cfg.num_blocks(0) // 2
+    _check(cfg, 0, [mid] * cfg.batch, (cfg.steps_per_block - 1,), (0, cfg.batch - 1), ALL)
+
+
+def test_ragged_all_heads_four_sequences():
+    cfg = make_config("ragged")
+    _check(cfg, 0, list(cfg.block_index), (cfg.steps_per_block - 1,), (0, 10, 20, cfg.batch - 1), ALL)

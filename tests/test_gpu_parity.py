@@ -1,9 +1,12 @@
 """GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle.
 
-Every test runs the block boundary (dllm_cache_build) and inner steps
-(dllm_block_qkv_rope_write -> dllm_block_attention -> dllm_state_merge) on
-seeded synthetic inputs and compares all rows' outputs with the oracle's
-full recompute of the same step.
+Every test runs the block boundary (dllm_cache_build) and inner steps on
+seeded synthetic inputs and compares all rows' outputs with the oracle's full
+recompute of the same step.  An inner step is dllm_block_qkv_rope_write then
+dllm_step_attention (the block attention and the FACache merge in one
+launch); test_split_calls_match_oracle_and_fused runs dllm_block_attention
+and dllm_state_merge as two separate calls instead, and checks them against
+the oracle and bit for bit against the fused call.
 """
 import numpy as np
 import pytest
@@ -27,10 +30,11 @@ def _lib():
 
 
 def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=True, rows_of=None, seqs=None,
-               gain=None):
+               gain=None, split=False):
     """Boundary of the blocks `k_of` (one per sequence) then the given inner
     steps; every listed sequence is compared with the oracle after each step.
-    `gain` replaces the workload's RMSNorm gain (all ones)."""
+    `gain` replaces the workload's RMSNorm gain (all ones); `split` runs the
+    attention as the two separate calls."""
     wl = Workload(cfg)
     W, g = wl.weights(layer)
     if gain is not None:
@@ -53,7 +57,7 @@ def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=Tr
             assert_close(gl / np.exp(m - gm), l, f"cache l seq {b}", max_abs=np.inf, rel=5e-3)
             assert_close(go / gl[..., None], Ot / l[..., None], f"cache O~/l seq {b}")
     for s in steps:
-        st.step(block_rows_of(wl, layer, s, k_of).cuda())
+        st.step(block_rows_of(wl, layer, s, k_of).cuda(), split=split)
         torch.cuda.synchronize()
         assert st.batch.error_bits() == 0
         for b in seqs:
@@ -126,10 +130,10 @@ def test_weight_pack_is_the_documented_permutation():
         assert np.array_equal(got, want), (D, H, d)
 
 
-def test_llada_single_blocks():
+def test_llada_single_every_block_first_and_last_step():
     cfg = make_config("llada_single")
-    for k in (0, 3, cfg.num_blocks(0) - 1):
-        _run_block(cfg, [k], (0, cfg.steps_per_block - 1), check_cache=(k == 3))
+    for k in range(cfg.num_blocks(0)):
+        _run_block(cfg, [k], (0, cfg.steps_per_block - 1), check_cache=(k in (0, 3, cfg.num_blocks(0) - 1)))
 
 
 def _mini_ragged(**kw):
@@ -152,6 +156,30 @@ def test_mini_ragged_edge_cases():
 def test_mini_ragged_head_dim_128():
     cfg = _mini_ragged(d_model=512, n_heads=2, head_dim=128, rope_theta=5e5)
     _run_block(cfg, cfg.block_index, (1,))
+
+
+def test_split_calls_match_oracle_and_fused():
+    """dllm_block_attention (block rows) and dllm_state_merge (invariant rows)
+    called separately run their own launch plans (every CTA in one role); the
+    rows they write match the oracle, and the fused dllm_step_attention on the
+    same inputs gives the same bytes (each (sequence, head) and each page is
+    computed whole by one CTA in either plan)."""
+    cases = [(make_config("tiny"), [2], (1,)), (make_config("tiny"), [7], (3,)),
+             (_mini_ragged(), None, (1,)),
+             (_mini_ragged(d_model=512, n_heads=2, head_dim=128, rope_theta=5e5), None, (0,)),
+             (make_config("llada_single"), [5], (7,))]
+    for cfg, k_of, steps in cases:
+        k_of = list(cfg.block_index) if k_of is None else k_of
+        st = _run_block(cfg, k_of, steps, check_cache=False, check_qkv=False, split=True)
+        split_out = (st.o_full.clone(), st.lse.clone())
+        st.o_full.zero_()
+        st.lse.zero_()
+        wl = Workload(cfg)
+        st.step(block_rows_of(wl, 0, steps[-1], k_of).cuda())
+        torch.cuda.synchronize()
+        assert st.batch.error_bits() == 0
+        assert torch.equal(split_out[0].view(torch.int16), st.o_full.view(torch.int16)), cfg.name
+        assert torch.equal(split_out[1].view(torch.int32), st.lse.view(torch.int32)), cfg.name
 
 
 def test_rmsnorm_gain_not_one():
