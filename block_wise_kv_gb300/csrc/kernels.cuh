@@ -71,23 +71,27 @@ inline size_t qkv_packed_bytes(int d_model, int n_heads, int head_dim) {
 cudaError_t launch_qkv_pack(const void* w, void* packed, int rows, int d_model, cudaStream_t stream);
 
 // Workspace layout and schedule of the fused projection for n_tok rows:
-// [counters: 1 KB][row scales: n_tok (hi, lo) pairs][x^: n_tok bf16 rows]
+// [counters: 4 KB][row scales: n_tok (hi, lo) pairs][x^: n_tok bf16 rows]
 // [stream-K partials].  The
-// counters (3 for the RMSNorm row claims, then one per weight tile) sit in a
-// region of fixed size at the start, so calls of different shapes sharing a
-// workspace never find another call's partials there; they are zero before
-// and after every call.
-constexpr size_t kQkvCounterBytes = 1024;
+// counters (3 for the RMSNorm row claims, then one per output tile of a
+// stream-K schedule) sit in a region of fixed size at the start, so calls of
+// different shapes sharing a workspace never find another call's partials
+// there; they are zero before and after every call.
+constexpr size_t kQkvCounterBytes = 4096;
 constexpr int kQkvNormCounters = 4;  // 3 used, the 4th keeps the tile counters 16-byte aligned
 constexpr int kQkvMaxTileCounters = static_cast<int>(kQkvCounterBytes / 4) - kQkvNormCounters;
 struct QkvPlan {
-  int bn;            // token tile (32, 64 or 128)
-  bool streamk;      // stream-K over (weight tile, k-unit) units, else one CTA per (weight tile, token tile)
-  int grid;          // CTAs of the stream-K schedule
-  int max_contrib;   // stream-K: most CTAs sharing one weight tile
+  int bn;            // token tile (32, 64 or 128; 256 in the wide kernel)
+  bool wide;         // the persistent wide-tile kernel (qkv_wide.cu): 256 or more token rows
+  bool streamk;      // stream-K over (output tile, k-unit) units, else whole tiles per CTA
+  int grid;          // CTAs of the stream-K schedule / of the persistent wide kernel
+  int n_tiles;       // wide kernel: output tiles (128 weight rows x 256 token rows)
+  int max_contrib;   // stream-K: most CTAs sharing one output tile
   size_t inv_offset, inv_bytes, xhat_offset, xhat_bytes, part_offset, part_bytes, total_bytes;
 };
 QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms);
+void qkv_wide_schedule(int n_tok, int d_model, int n_heads, int head_dim, int num_sms, QkvPlan* p);
+cudaError_t launch_qkv_wide(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream);
 constexpr int kModeBlock = 0;     // tokens are the packed block rows (cu_block)
 constexpr int kModeBoundary = 1;  // tokens are all rows of every sequence (cu_seq)
 

@@ -74,6 +74,7 @@ constexpr int kBoxes = 2;                   // boxes per unit: a unit covers K =
 constexpr int kUnitK = kTileK * kBoxes;
 constexpr int kTileABytes = kTileM * kTileK * 2;
 constexpr int kMinUnitsPerCta = 4;
+constexpr int kWideMinTokens = 256;         // from here on the wide-tile kernel (qkv_wide.cu)
 constexpr int kSmemLimit = 232448 - 4096;   // opt-in maximum less room for the static shared data
 
 template <int BN>
@@ -694,13 +695,19 @@ QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms)
   QkvPlan p = {};
   const long long n_wt = 3LL * n_heads * head_dim / kTileM;
   const long long nkb = (d_model + kUnitK - 1) / kUnitK;
-  p.bn = n_tok <= 32 ? 32 : (n_tok <= 64 ? 64 : 128);
-  p.streamk = p.bn <= 64 && 2 * n_wt <= num_sms && n_wt <= kQkvMaxTileCounters;
   p.inv_offset = kQkvCounterBytes;
   p.inv_bytes = align256(static_cast<size_t>(n_tok) * 8);
   p.xhat_offset = p.inv_offset + p.inv_bytes;
   p.xhat_bytes = align256(static_cast<size_t>(n_tok) * d_model * 2);
   p.part_offset = p.xhat_offset + p.xhat_bytes;
+  if (n_tok >= kWideMinTokens) {  // tensor-bound: the persistent wide-tile kernel
+    qkv_wide_schedule(n_tok, d_model, n_heads, head_dim, num_sms, &p);
+    p.part_bytes = align256(p.part_bytes);
+    p.total_bytes = p.part_offset + p.part_bytes;
+    return p;
+  }
+  p.bn = n_tok <= 32 ? 32 : (n_tok <= 64 ? 64 : 128);
+  p.streamk = p.bn <= 64 && 2 * n_wt <= num_sms && n_wt <= kQkvMaxTileCounters;
   if (p.streamk) {
     const long long U = n_wt * nkb;
     long long G = U / kMinUnitsPerCta;
@@ -721,6 +728,7 @@ QkvPlan qkv_plan(int n_tok, int d_model, int n_heads, int head_dim, int num_sms)
 
 cudaError_t launch_qkv_gemm(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream) {
   if (a.n_tok <= 0) return cudaSuccess;
+  if (plan.wide) return launch_qkv_wide(w_packed, a, plan, stream);
   if (plan.bn == 32) return launch_bn<32>(w_packed, a, plan, stream);
   if (plan.bn == 64) return launch_bn<64>(w_packed, a, plan, stream);
   return launch_bn<128>(w_packed, a, plan, stream);

@@ -43,15 +43,20 @@ def _batch(batch=2, max_pages=12, M=64, R=1536, max_block=32, max_seq=768):
 
 def test_workspace_sizes(lib):
     d, b = _desc(), _batch()
-    # 1 KB of counters, one RMSNorm scale pair (8 bytes) per row, the bf16 x^
+    # 4 KB of counters, one RMSNorm scale pair (8 bytes) per row, the bf16 x^
     # rows (each region 256-byte aligned); 96 weight tiles: no stream-K partials
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) == 1024 + 512 + 64 * 4096 * 2
-    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD) == 1024 + 1536 * 8 + 1536 * 4096 * 2
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE) == 4096 + 512 + 64 * 4096 * 2
+    # the boundary's 1536 rows take the wide-tile kernel: 96 x 6 output tiles of
+    # 128 x 256, fewer than four per SM, so its K chunks are split over the CTAs
+    # and fp32 partial tiles of 128 x 256 per tile and contributor follow
+    n = dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_BUILD)
+    base = 4096 + 1536 * 8 + 1536 * 4096 * 2
+    assert n > base and (n - base) % (96 * 6 * 128 * 256 * 4) == 0
     # a small model (12 weight tiles) splits each tile's K range over several
     # CTAs: fp32 partial tiles of 128 x 64 per tile and contributor follow
     small = _desc(d_model=1024, n_heads=8, head_dim=64)
     n = dllm.dllm_workspace_size(small, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE)
-    base = 1024 + 512 + 64 * 1024 * 2
+    base = 4096 + 512 + 64 * 1024 * 2
     assert n > base and (n - base) % (12 * 128 * 64 * 4) == 0
     for op in (dllm.DLLM_OP_BLOCK_ATTENTION, dllm.DLLM_OP_STATE_MERGE, dllm.DLLM_OP_STEP_ATTENTION):
         assert dllm.dllm_workspace_size(d, b, op) == 0

@@ -103,15 +103,15 @@ def test_rmsnorm_rows_and_scales_in_the_workspace():
         st.qkv(xb.cuda())
         torch.cuda.synchronize()
         M, D = xb.shape
-        pairs = st.ws_step[1024:1024 + M * 8].view(torch.float32).view(M, 2).double().cpu().numpy()
+        pairs = st.ws_step[4096:4096 + M * 8].view(torch.float32).view(M, 2).double().cpu().numpy()
         x = xb.double().numpy()
         want = 1.0 / np.sqrt((x * x).mean(axis=1) + cfg.rms_eps)
         assert np.max(np.abs((pairs[:, 0] + pairs[:, 1]) / want - 1.0)) < 2.0 ** -38
-        off = 1024 + 256 * ((M * 8 + 255) // 256)
+        off = 4096 + 256 * ((M * 8 + 255) // 256)
         got = st.ws_step[off:off + M * D * 2].view(torch.bfloat16).view(M, D).double().cpu().numpy()
         xh = orc.bf16_round(orc.rmsnorm(x, st.gain.double().cpu().numpy(), cfg.rms_eps))
         assert np.array_equal(got, xh), f"{int((got != xh).sum())} elements of x^ differ"
-        assert int(st.ws_step[:1024].view(torch.int32).abs().sum()) == 0, "counters left non-zero"
+        assert int(st.ws_step[:4096].view(torch.int32).abs().sum()) == 0, "counters left non-zero"
 
 
 def test_weight_pack_is_the_documented_permutation():
@@ -212,7 +212,7 @@ def test_split_stream_k_tiles_and_repeatability():
                      steps_per_block=2)
         st = _run_block(cfg, cfg.block_index, (1,))
         M = sum(block)
-        plain = 1024 + 256 * ((M * 8 + 255) // 256) + 256 * ((M * 4096 * 2 + 255) // 256)
+        plain = 4096 + 256 * ((M * 8 + 255) // 256) + 256 * ((M * 4096 * 2 + 255) // 256)
         assert st.ws_step.numel() > plain, "expected the split schedule (partials)"
         wl = Workload(cfg)
         xb = block_rows_of(wl, 0, 1, cfg.block_index).cuda()
@@ -224,7 +224,7 @@ def test_split_stream_k_tiles_and_repeatability():
             for x, y in zip(first, again):
                 iv = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
                 assert torch.equal(x.view(iv), y.view(iv)), name
-        assert int(st.ws_step[:1024].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
+        assert int(st.ws_step[:4096].view(torch.int32).abs().sum()) == 0, "arrival counters left non-zero"
 
 
 def test_placement_is_bit_exact_and_sentinels_survive():

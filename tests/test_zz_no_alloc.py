@@ -63,7 +63,7 @@ def test_noalloc_split_schedule_uses_its_scratch():
     wl = Workload(cfg)
     st = LayerStep(cfg)
     M = st.batch.total_block_rows
-    assert st.ws_step.numel() > 1024 + 512 + M * 4096 * 2  # partial tiles beyond counters, scales and x^ rows
+    assert st.ws_step.numel() > 4096 + 512 + M * 4096 * 2  # partial tiles beyond counters, scales and x^ rows
     st.boundary(full_rows_of(wl, 0, 0, cfg.block_index).cuda())
     torch.cuda.synchronize()
     for step in (0, 1, 1):
