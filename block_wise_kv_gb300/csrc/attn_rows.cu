@@ -1,0 +1,656 @@
+// attn_rows.cu — attention of 128-row query tiles on the 5th-generation tensor
+// cores (sm_103a), in three modes that share one persistent kernel:
+//
+//   kRowsState   the FACache build of a block boundary: every row r of U
+//                over the keys of U only, the online-softmax state
+//                (m, l, O~) into m_pool / l_pool / o_pool (LaCache §3.3.3;
+//                Algorithm 1 with GenStep = True).
+//   kRowsBlock   the block attention of blocks longer than one page: the
+//                block rows (from q_block) over every key of the sequence,
+//                O = O~ / l and L = m + ln l (Fast-dLLM DualCache "Inner step
+//                on block k", LaCache Eq. (2)-(6)).  This is the prefix-only
+//                cache mode of the Fast-dLLM page, where the block is the
+//                whole region after the prefix.
+//   kRowsMerge   the FACache merge for such blocks: every row of U over the
+//                block keys, merged exactly with its cached state (LaCache
+//                §3.3.3, Algorithm 1 with GenStep = False).
+//
+// A unit of work is (sequence b, head h, a pair of query tiles): two tiles of
+// 128 query rows that share every K/V page the unit streams.  Warp 9 streams
+// the query tiles and the K/V pages (TMA, 128-byte swizzle) into an mbarrier
+// ring; warp 8 issues, per page, S_t = Q_t K^T into one of two score buffers
+// of tile t and then O_t += P_t V of the previous page (P_t from shared
+// memory, V as an MN-major operand), with S, O in tensor memory; warps 0-3
+// (tile 0) and 4-7 (tile 1) run the softmax, one thread per query row (TMEM
+// lane = row).  The reference max of a row is raised (its O row and sum
+// rescaled) only when a page's max exceeds it by more than 2^8, so every P
+// stays <= 2^8; the exact max is tracked beside it for the state build's m.
+// Units are split over the CTAs by their K/V pages (every unit of a sequence
+// streams the same pages), and a CTA walks its units in order, loading the
+// next unit's query tiles while the current one finishes.
+#include <math.h>
+
+#include "attn_common.cuh"
+
+namespace dllm {
+namespace {
+using namespace attn;
+
+constexpr int kThreads = 320;  // warps 0-7 softmax, 8 MMA issuer, 9 producer
+constexpr int kMaxSeqs = 1024;  // sequences per launch (the host launches larger batches in slices)
+constexpr float kRescale = 8.f;  // log2 units
+
+template <int D>
+struct RowsCfg {
+  static constexpr int TB = tile_bytes<D>();  // bf16 64 rows x D
+  static constexpr int QB = 2 * TB;           // one 128-row query tile
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int KVB = 2 * TB;          // a K page and a V page
+  static constexpr int off_q = 0;             // two query tiles
+  static constexpr int off_kv = 2 * QB;
+  static constexpr int off_p = off_kv + kStages * KVB;  // two P tiles (128 x 64 bf16)
+  static constexpr int PB = 128 * 128;
+  static constexpr int kSmem = off_p + 2 * PB + 1024;  // + alignment slack
+  // tensor memory: O_0, O_1 (D columns each), then four 64-column score buffers
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemS = 256;
+};
+
+struct RowsShared {
+  uint64_t kvfull[6], kvempty[6], qfull, qempty;
+  uint64_t sfull[2][2], sfree[2][2], pfull[2], pfree[2], ofull[2], ofree[2];
+  uint32_t tmem_base;
+  int abort_flag;
+  long long cu_units[kMaxSeqs + 1];  // unit prefix over the launch's sequences
+  long long cu_cost[kMaxSeqs + 1];   // K/V page prefix (the cost of the units)
+};
+
+// Per-sequence shape of the work of one mode: which query tiles (of 128 rows)
+// and which K/V pages (of 64 keys) a unit of the sequence covers.
+struct RowsSeq {
+  SeqMeta sm;
+  int np;        // pages of the sequence
+  int nq;        // query tiles
+  int lo_t, hi_t;  // query tile k -> tile index: k < lo_t ? k : hi_t + (k - lo_t)
+  int lo_p, hi_p, end_p;  // K/V pages [0, lo_p) and [hi_p, end_p) (kRowsMerge: [lo_p, hi_p) only)
+  int nk;        // K/V pages per unit
+};
+
+__device__ __forceinline__ SeqMeta load_meta_rows(const BatchArgs& bt, int b) {
+  SeqMeta m;
+  m.nb = __ldg(bt.seq_len + b);
+  m.bb = __ldg(bt.block_len + b);
+  m.sb = __ldg(bt.block_start + b);
+  m.cub = __ldg(bt.cu_block + b);
+  m.cus = __ldg(bt.cu_seq + b);
+  m.ok = m.nb >= 1 && m.nb <= bt.max_seq_len && m.bb >= 1 && m.bb <= bt.max_block_len && m.sb >= 0 &&
+         m.sb + m.bb <= m.nb && (m.nb + kPage - 1) / kPage <= bt.max_pages && m.cub >= 0 &&
+         m.cub + m.bb <= bt.total_block_rows && m.cus >= 0 && m.cus + m.nb <= bt.total_seq_rows;
+  return m;
+}
+
+__device__ __forceinline__ RowsSeq rows_seq(const BatchArgs& bt, int b, int mode) {
+  RowsSeq s;
+  s.sm = load_meta_rows(bt, b);
+  s.nq = 0;
+  s.nk = 0;
+  s.lo_t = s.hi_t = s.lo_p = s.hi_p = s.end_p = 0;
+  s.np = 0;
+  if (!s.sm.ok) return s;
+  const int nb = s.sm.nb, sb = s.sm.sb, ce = s.sm.sb + s.sm.bb;  // C = [sb, ce)
+  s.np = (nb + kPage - 1) / kPage;
+  if (mode == kRowsBlock) {
+    s.nq = (s.sm.bb + 127) / 128;
+    s.lo_t = s.nq;
+    s.hi_t = 0;
+  } else {
+    // the tiles that hold rows of U = [0, sb) u [ce, nb)
+    s.lo_t = (sb + 127) / 128;
+    s.hi_t = s.lo_t;
+    int hi_end = s.lo_t;
+    if (ce < nb) {
+      s.hi_t = max(ce / 128, s.lo_t);
+      hi_end = (nb + 127) / 128;
+    }
+    s.nq = s.lo_t + (hi_end - s.hi_t);
+  }
+  if (mode == kRowsState) {  // the pages that hold keys of U
+    s.lo_p = (sb + kPage - 1) / kPage;
+    s.hi_p = s.lo_p;
+    s.end_p = s.lo_p;
+    if (ce < nb) {
+      s.hi_p = max(ce / kPage, s.lo_p);
+      s.end_p = s.np;
+    }
+    s.nk = s.lo_p + (s.end_p - s.hi_p);
+  } else if (mode == kRowsMerge) {  // the pages that hold keys of C
+    s.lo_p = sb / kPage;
+    s.hi_p = (ce - 1) / kPage + 1;
+    s.nk = s.hi_p - s.lo_p;
+  } else {
+    s.lo_p = s.np;
+    s.hi_p = s.end_p = s.np;
+    s.nk = s.np;
+  }
+  return s;
+}
+
+// The i-th K/V page of a unit of sequence s.
+__device__ __forceinline__ int key_page(const RowsSeq& s, int mode, int i) {
+  if (mode == kRowsMerge) return s.lo_p + i;
+  return i < s.lo_p ? i : s.hi_p + (i - s.lo_p);
+}
+
+// The first unit, in unit order, whose first page is at or after page x of the launch's
+// cost (K/V pages): CTA c owns the units that start in [c W / G, (c + 1) W / G).  Every
+// unit of a sequence streams the same pages.
+__device__ __forceinline__ long long first_unit_at(const RowsShared& S, int nseq, long long x) {
+  if (x >= S.cu_cost[nseq]) return S.cu_units[nseq];
+  int lo = 0, hi = nseq - 1;  // the sequence holding page x: the smallest b with cu_cost[b + 1] > x
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (S.cu_cost[mid + 1] > x)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  const long long nk = (S.cu_cost[lo + 1] - S.cu_cost[lo]) / (S.cu_units[lo + 1] - S.cu_units[lo]);
+  return S.cu_units[lo] + (x - S.cu_cost[lo] + nk - 1) / nk;
+}
+
+// Walk over the units [u, u1): sequence, head, pair of query tiles.
+struct RWalk {
+  long long u, u1;
+  int b, h, pr, npairs;
+  RowsSeq s;
+  __device__ __forceinline__ void seek(const RowsShared& S, const BatchArgs& bt, int mode, int b_begin, int nseq,
+                                       int H) {
+    int lo = 0, hi = nseq - 1;  // the largest b with cu_units[b] <= u: skips sequences without units
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (S.cu_units[mid] <= u)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    b = lo;
+    s = rows_seq(bt, b_begin + b, mode);
+    npairs = static_cast<int>((S.cu_units[b + 1] - S.cu_units[b]) / H);
+    const int r = static_cast<int>(u - S.cu_units[b]);
+    h = r / npairs;
+    pr = r % npairs;
+  }
+  __device__ __forceinline__ bool valid() const { return u < u1; }
+  __device__ __forceinline__ void next(const RowsShared& S, const BatchArgs& bt, int mode, int b_begin, int nseq,
+                                       int H) {
+    if (++u >= u1) return;
+    if (++pr == npairs) {
+      pr = 0;
+      if (++h == H) seek(S, bt, mode, b_begin, nseq, H);
+    }
+  }
+  __device__ __forceinline__ bool has1() const { return 2 * pr + 1 < s.nq; }
+  // tile index (of 128 rows) of query tile t of the unit
+  __device__ __forceinline__ int tile(int t) const {
+    const int k = 2 * pr + t;
+    return k < s.lo_t ? k : s.hi_t + (k - s.lo_t);
+  }
+};
+
+// Bounded wait that gives up (and makes the whole CTA give up) after a timeout.
+__device__ __forceinline__ void wait_or_abort(RowsShared& S, uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return;
+  if (!mbar_wait(bar, parity)) {
+    S.abort_flag = 1;
+    report_error(err, kErrTimeout);
+  }
+}
+
+// Is key position kp (of page key0 + c) a key of this mode?
+template <int MODE>
+__device__ __forceinline__ bool key_valid(int kp, int nb, int sb, int ce) {
+  if (MODE == kRowsState) return kp < nb && (kp < sb || kp >= ce);
+  if (MODE == kRowsMerge) return kp >= sb && kp < ce;
+  return kp < nb;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    rows_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qb,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const AttnArgs a, int b_begin, int nseq) {
+  using C = RowsCfg<D>;
+  constexpr int TB = C::TB;
+  constexpr int NST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* q_tiles = smem + C::off_q;
+  uint8_t* kv_ring = smem + C::off_kv;
+  uint8_t* p_tiles = smem + C::off_p;
+  __shared__ RowsShared S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BatchArgs& bt = a.bt;
+  const int H = a.n_heads;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&S.kvfull[s], 1);
+      mbar_init(&S.kvempty[s], 1);  // one commit after the last MMA that reads the stage
+    }
+    mbar_init(&S.qfull, 1);
+    mbar_init(&S.qempty, 1);
+    for (int t = 0; t < 2; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&S.sfull[t][b], 1);
+        mbar_init(&S.sfree[t][b], 4);  // the tile's four softmax warps
+      }
+      mbar_init(&S.pfull[t], 4);
+      mbar_init(&S.pfree[t], 1);
+      mbar_init(&S.ofull[t], 1);
+      mbar_init(&S.ofree[t], 4);
+    }
+    S.abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Units and their cost (K/V pages) per sequence, then their prefix sums (warp 0).
+  for (int i = threadIdx.x; i < nseq; i += kThreads) {
+    const RowsSeq s = rows_seq(bt, b_begin + i, MODE);
+    if (!s.sm.ok) report_error(bt.err, kErrBadShape);
+    const long long units = s.nk > 0 ? static_cast<long long>(H) * ((s.nq + 1) / 2) : 0;
+    S.cu_units[i + 1] = units;
+    S.cu_cost[i + 1] = units * s.nk;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (nseq + 31) / 32, i0 = lane * per, i1 = min(nseq, i0 + per);
+    long long su = 0, sc = 0;
+    for (int i = i0; i < i1; ++i) {
+      su += S.cu_units[i + 1];
+      sc += S.cu_cost[i + 1];
+    }
+    long long xu = su, xc = sc;  // inclusive scan over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long yu = __shfl_up_sync(0xffffffffu, xu, o), yc = __shfl_up_sync(0xffffffffu, xc, o);
+      if (lane >= o) {
+        xu += yu;
+        xc += yc;
+      }
+    }
+    long long ru = xu - su, rc = xc - sc;  // exclusive
+    for (int i = i0; i < i1; ++i) {
+      ru += S.cu_units[i + 1];
+      rc += S.cu_cost[i + 1];
+      S.cu_units[i + 1] = ru;
+      S.cu_cost[i + 1] = rc;
+    }
+    if (lane == 0) {
+      S.cu_units[0] = 0;
+      S.cu_cost[0] = 0;
+    }
+  }
+  if (warp == 8) tmem_alloc(&S.tmem_base, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  griddep_launch_dependents();
+  // Every read of the pools, q_block and the cached state comes after the preceding
+  // kernel (the projection that writes them) has completed.
+  griddep_wait();
+
+  const long long W = S.cu_cost[nseq];
+  const long long G = gridDim.x, c = blockIdx.x;
+  RWalk w0;
+  w0.u = first_unit_at(S, nseq, c * W / G);
+  w0.u1 = first_unit_at(S, nseq, (c + 1) * W / G);
+  if (w0.u < w0.u1) w0.seek(S, bt, MODE, b_begin, nseq, H);
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int nkv = 0, nq = 0;
+      for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+        if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
+        const int gb = b_begin + w.b;
+        const int T = w.has1() ? 2 : 1;
+        // the unit's query tiles, once the previous unit's score MMAs have read theirs
+        if (nq >= 1) wait_or_abort(S, &S.qempty, (nq - 1) & 1, bt.err);
+        mbar_arrive_expect_tx(&S.qfull, T * C::QB);
+        for (int t = 0; t < T; ++t) {
+          const int tq = w.tile(t);
+          uint8_t* qt = q_tiles + t * C::QB;
+          for (int cp = 0; cp < 2; ++cp) {  // two boxes of 64 rows
+            if (MODE == kRowsBlock) {
+              // block rows cu_block[b] + 128 tq + 64 cp ...: rows past the end of q_block read as
+              // zeros, rows of the next sequence are loaded but never written out
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf)
+                tma_load_3d(qt + hf * 16384 + cp * 8192, &tm_qb, &S.qfull, hf * 64, w.h, w.s.sm.cub + 128 * tq + 64 * cp);
+            } else {
+              // page 2 tq + cp of the sequence (a tile's second page past the end repeats its
+              // first: those rows are never written out)
+              const int p = 2 * tq + cp < w.s.np ? 2 * tq + cp : 2 * tq;
+              const int y = (page_of(bt, gb, p) * H + w.h) * kPage;
+#pragma unroll
+              for (int hf = 0; hf < D / 64; ++hf) tma_load_2d(qt + hf * 16384 + cp * 8192, &tm_q, &S.qfull, hf * 64, y);
+            }
+          }
+        }
+        ++nq;
+        for (int i = 0; i < w.s.nk; ++i, ++nkv) {
+          const int st = nkv % NST;
+          if (nkv >= NST) wait_or_abort(S, &S.kvempty[st], (nkv / NST - 1) & 1, bt.err);
+          const int y = (page_of(bt, gb, key_page(w.s, MODE, i)) * H + w.h) * kPage;
+          uint8_t* kt = kv_ring + st * C::KVB;
+          mbar_arrive_expect_tx(&S.kvfull[st], C::KVB);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_load_2d(kt + hf * 8192, &tm_k, &S.kvfull[st], hf * 64, y);
+            tma_load_2d(kt + TB + hf * 8192, &tm_v, &S.kvfull[st], hf * 64, y);
+          }
+        }
+      }
+      // Tail: every copy has landed, and the MMA issuer's last commits on the stages and on
+      // the query tiles have arrived, before the CTA can exit.
+      for (int i = (nkv > NST ? nkv - NST : 0); i < nkv; ++i)
+        if (!mbar_wait(&S.kvfull[i % NST], (i / NST) & 1)) report_error(bt.err, kErrTimeout);
+      if (nq >= 1 && !mbar_wait(&S.qfull, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
+      for (int i = (nkv > NST ? nkv - NST : 0); i < nkv; ++i)
+        if (!mbar_wait(&S.kvempty[i % NST], (i / NST) & 1)) report_error(bt.err, kErrTimeout);
+      if (nq >= 1 && !mbar_wait(&S.qempty, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per page i of a unit: S_t(i) = Q_t K_i^T for each tile, then O_t += P_t(i-1) V_{i-1}
+    // (the scores of page i run while the softmax of page i-1 finishes).
+    if (lane == 0) {
+      constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
+      constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
+      int nkv = 0, nq = 0;
+      int ns[2] = {0, 0}, npv[2] = {0, 0}, no[2] = {0, 0};  // per tile: S buffers, P V, units
+      const uint32_t qa0 = smem_u32(q_tiles), ring0 = smem_u32(kv_ring), pa0 = smem_u32(p_tiles);
+      for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+        const int T = w.has1() ? 2 : 1;
+        const int nk = w.s.nk;
+        wait_or_abort(S, &S.qfull, nq & 1, bt.err);
+        tc_fence_after();
+        // O_t += P_t V of page i (stage st); the unit's first overwrites O_t once the
+        // softmax warps have read the previous unit's O_t out
+        auto pv = [&](int i, int st) {
+          const uint32_t va = ring0 + st * C::KVB + TB;
+          for (int t = 0; t < T; ++t) {
+            wait_or_abort(S, &S.pfull[t], npv[t] & 1, bt.err);
+            if (i == 0 && no[t] >= 1) wait_or_abort(S, &S.ofree[t], (no[t] - 1) & 1, bt.err);
+            tc_fence_after();
+            const uint32_t pa = pa0 + t * C::PB;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + t * D, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&S.pfree[t]);
+            ++npv[t];
+            if (i == nk - 1) {
+              umma_commit(&S.ofull[t]);
+              ++no[t];
+            }
+          }
+          umma_commit(&S.kvempty[st]);  // every MMA that reads the stage has completed
+        };
+        int prev_st = 0;
+        for (int i = 0; i < nk; ++i, ++nkv) {
+          const int st = nkv % NST;
+          wait_or_abort(S, &S.kvfull[st], (nkv / NST) & 1, bt.err);
+          tc_fence_after();
+          const uint32_t ka = ring0 + st * C::KVB;
+          for (int t = 0; t < T; ++t) {
+            const int bsel = ns[t] & 1;
+            if (ns[t] >= 2) wait_or_abort(S, &S.sfree[t][bsel], ((ns[t] >> 1) - 1) & 1, bt.err);
+            tc_fence_after();
+            const uint32_t qa = qa0 + t * C::QB;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_bf16(tmem + C::kTmemS + (2 * t + bsel) * 64,
+                        umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
+                        umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
+            umma_commit(&S.sfull[t][bsel]);
+            ++ns[t];
+          }
+          if (i == nk - 1) umma_commit(&S.qempty);  // the unit's queries are no longer read
+          if (i >= 1) pv(i - 1, prev_st);
+          prev_st = st;
+        }
+        if (nk >= 1) pv(nk - 1, prev_st);
+        ++nq;
+      }
+      // Tail: each tile's last P V commit has arrived before the CTA can exit.
+      for (int t = 0; t < 2; ++t)
+        if (npv[t] >= 1 && !mbar_wait(&S.pfree[t], (npv[t] - 1) & 1)) report_error(bt.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int t = warp >> 2, wq = warp & 3;  // query tile, warp of the tile (= TMEM lane quadrant)
+    const int r = wq * 32 + lane;            // query row of the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    uint8_t* p_own = p_tiles + t * C::PB;
+    int ns = 0, pw = 0, no = 0;  // S buffers read, P tiles written, units finished
+    for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+      if (t == 1 && !w.has1()) continue;
+      const int gb = b_begin + w.b;
+      const int nb = w.s.sm.nb, sb = w.s.sm.sb, ce = w.s.sm.sb + w.s.sm.bb;
+      const int tq = w.tile(t);
+      // the position of this thread's query row, and whether it is written out
+      int pos;
+      bool row_out;
+      if (MODE == kRowsBlock) {
+        const int i = 128 * tq + r;
+        pos = sb + i;
+        row_out = i < w.s.sm.bb;
+      } else {
+        pos = 128 * tq + r;
+        row_out = pos < nb && (pos < sb || pos >= ce);
+      }
+      float m_ref = neg_inf(), m_true = neg_inf(), l = 0.f;
+      for (int i = 0; i < w.s.nk; ++i) {
+        const int bsel = ns & 1;
+        wait_or_abort(S, &S.sfull[t][bsel], (ns >> 1) & 1, bt.err);
+        tc_fence_after();
+        float sc[64];
+        tmem_ld_32x32b_x64(lane_base + C::kTmemS + (2 * t + bsel) * 64, sc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.sfree[t][bsel]);
+        ++ns;
+        // scale, mask the keys outside this mode's key set, this row's page max
+        const int key0 = key_page(w.s, MODE, i) * kPage;
+        float mx4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) {
+          sc[cc] = key_valid<MODE>(key0 + cc, nb, sb, ce) ? sc[cc] * a.scale_log2 : neg_inf();
+          mx4[cc & 3] = fmaxf(mx4[cc & 3], sc[cc]);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        m_true = fmaxf(m_true, mx);
+        // a new reference max (the unit's first page, or a rise beyond the threshold)
+        float factor = 1.f;
+        if (i == 0) {
+          m_ref = mx;
+        } else if (mx > m_ref + kRescale) {
+          factor = fast_exp2(m_ref - mx);
+          m_ref = mx;
+        }
+        const float mu = m_ref == neg_inf() ? 0.f : m_ref;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) {
+          sc[cc] = fast_exp2(sc[cc] - mu);
+          l4[cc & 3] += sc[cc];
+        }
+        l = l * factor + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        // the tile's previous P V has completed: its P tile is free and O_t holds every
+        // earlier page (rescaled here when the reference max rose)
+        if (pw >= 1) wait_or_abort(S, &S.pfree[t], (pw - 1) & 1, bt.err);
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] *= factor;
+            tmem_st_32x32b_x32(lane_base + t * D + c0, ov);
+          }
+          tmem_st_wait();
+        }
+        // P = 2^(S - m_ref) as bf16 into row r of the tile's P tile (K-major, 128-byte swizzle)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 u;
+          u.x = pack_bf16x2(sc[8 * cc], sc[8 * cc + 1]);
+          u.y = pack_bf16x2(sc[8 * cc + 2], sc[8 * cc + 3]);
+          u.z = pack_bf16x2(sc[8 * cc + 4], sc[8 * cc + 5]);
+          u.w = pack_bf16x2(sc[8 * cc + 6], sc[8 * cc + 7]);
+          *reinterpret_cast<uint4*>(p_own + sw128_offset(r, cc)) = u;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pfull[t]);
+        ++pw;
+      }
+      // ---- the unit is complete for this tile: O_t out, then released for the next unit
+      wait_or_abort(S, &S.ofull[t], no & 1, bt.err);
+      tc_fence_after();
+      if (MODE == kRowsState) {
+        // state relative to the exact max over the row's keys of U
+        size_t srow = 0;
+        float corr = 0.f;
+        if (row_out) {
+          srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
+          corr = fast_exp2(m_ref - m_true);
+          a.m_pool[srow] = m_true * kLn2;  // natural units
+          a.l_pool[srow] = l * corr;
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
+          if (row_out) {
+            float4* dst = reinterpret_cast<float4*>(a.o_pool + srow * D + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(ov[4 * q] * corr, ov[4 * q + 1] * corr, ov[4 * q + 2] * corr, ov[4 * q + 3] * corr);
+          }
+        }
+      } else {
+        // O = (w_c O~_c + w_f O_t) / L with the cached state (merge) or O_t / l (block rows)
+        float wc = 0.f, wf = 1.f, M = m_ref, L = l;
+        size_t srow = 0;
+        if (MODE == kRowsMerge && row_out) {
+          srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
+          const float mc = __ldg(a.m_pool + srow) * 1.4426950408889634f;  // base-2 units
+          const float lc = __ldg(a.l_pool + srow);
+          M = fmaxf(mc, m_ref);
+          wc = mc == neg_inf() ? 0.f : fast_exp2(mc - M);
+          wf = fast_exp2(m_ref - M);
+          L = wc * lc + wf * l;
+        }
+        const float inv = row_out ? 1.f / L : 0.f;
+        wc *= inv;
+        wf *= inv;
+        const size_t orow = static_cast<size_t>(w.s.sm.cus + pos) * H + w.h;
+        __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float ov[32];
+          tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
+          if (row_out) {
+            if (MODE == kRowsMerge) {
+              const float4* oc = reinterpret_cast<const float4*>(a.o_pool + srow * D + c0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 v = __ldg(oc + q);
+                ov[4 * q] = wc * v.x + wf * ov[4 * q];
+                ov[4 * q + 1] = wc * v.y + wf * ov[4 * q + 1];
+                ov[4 * q + 2] = wc * v.z + wf * ov[4 * q + 2];
+                ov[4 * q + 3] = wc * v.w + wf * ov[4 * q + 3];
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] *= wf;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(of + orow * D + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              u.x = pack_bf16x2(ov[8 * q], ov[8 * q + 1]);
+              u.y = pack_bf16x2(ov[8 * q + 2], ov[8 * q + 3]);
+              u.z = pack_bf16x2(ov[8 * q + 4], ov[8 * q + 5]);
+              u.w = pack_bf16x2(ov[8 * q + 6], ov[8 * q + 7]);
+              dst[q] = u;
+            }
+          }
+        }
+        if (row_out && a.lse != nullptr) a.lse[orow] = (M + log2f(L)) * kLn2;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ofree[t]);
+      ++no;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int MODE>
+cudaError_t launch_rows_dm(const AttnArgs& a, int num_sms, cudaStream_t stream) {
+  PoolMaps m;
+  cudaError_t e = encode_pool_maps(a, MODE != kRowsBlock, false, &m);
+  if (e != cudaSuccess) return e;
+  if (MODE == kRowsBlock) m.q = m.k;  // unused
+  CUtensorMap tm_qb = m.k;            // the block queries in boxes of 64 rows
+  if (MODE == kRowsBlock) {
+    e = encode_3d_rows_sw128(&tm_qb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_block, D, a.n_heads,
+                             a.bt.total_block_rows, 64, 64);
+    if (e != cudaSuccess) return e;
+  }
+  constexpr int smem = RowsCfg<D>::kSmem;
+  auto kern = rows_attn_kernel<D, MODE>;
+  e = set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  const long long rows = MODE == kRowsBlock ? a.bt.max_block_len : a.bt.max_seq_len;
+  const long long pairs = (rows + 255) / 256;  // upper bound of a sequence's tile pairs
+  for (int b0 = 0; b0 < a.bt.batch; b0 += kMaxSeqs) {
+    const int n = a.bt.batch - b0 < kMaxSeqs ? a.bt.batch - b0 : kMaxSeqs;
+    const long long units = static_cast<long long>(n) * a.n_heads * pairs;
+    const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+    e = launch_pdl(kern, dim3(grid), kThreads, smem, 0, stream, m.q, tm_qb, m.k, m.v, a, b0, n);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_rows_d(const AttnArgs& a, int mode, int num_sms, cudaStream_t stream) {
+  if (mode == kRowsState) return launch_rows_dm<D, kRowsState>(a, num_sms, stream);
+  if (mode == kRowsBlock) return launch_rows_dm<D, kRowsBlock>(a, num_sms, stream);
+  return launch_rows_dm<D, kRowsMerge>(a, num_sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_rows_attention(const AttnArgs& a, int mode, int num_sms, cudaStream_t stream) {
+  if (a.bt.batch <= 0) return cudaSuccess;
+  if (mode == kRowsBlock && a.bt.total_block_rows <= 0) return cudaSuccess;
+  return a.head_dim == 128 ? launch_rows_d<128>(a, mode, num_sms, stream) : launch_rows_d<64>(a, mode, num_sms, stream);
+}
+
+}  // namespace dllm

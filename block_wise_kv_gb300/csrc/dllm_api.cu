@@ -38,7 +38,7 @@ dllm_status check_batch(const dllm_batch* b) {
     return DLLM_ERR_INVALID_ARGUMENT;
   if (b->error_flag != nullptr && !aligned(b->error_flag, 4)) return DLLM_ERR_INVALID_ARGUMENT;
   if (b->max_pages_per_seq < 1 || b->max_seq_len < 1 || b->max_block_len < 1) return DLLM_ERR_INVALID_ARGUMENT;
-  if (b->max_block_len > 64) return DLLM_ERR_UNSUPPORTED;
+  if (b->max_block_len > b->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
   if (static_cast<int64_t>(b->max_pages_per_seq) * kPage < b->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
   if (b->max_seq_len > 65535 * kPage) return DLLM_ERR_UNSUPPORTED;
   if (b->total_block_rows < 0 || b->total_seq_rows < 0) return DLLM_ERR_INVALID_ARGUMENT;
@@ -257,7 +257,7 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
   DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, qa, plan, s));
   const AttnArgs aa = attn_args(desc, batch, cache);
-  DLLM_CUDA_TRY(launch_state_build(aa, s));
+  DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsState, device_sms(), s));
   return DLLM_OK;
 }
 
@@ -299,7 +299,11 @@ dllm_status attention_call(const dllm_layer_desc* desc, const dllm_batch* batch,
   if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
   if (block && batch->total_block_rows == 0) block = false;
   if (!block && !merge) return DLLM_OK;
-  if (!attn_batch_supported(batch->batch)) return DLLM_ERR_UNSUPPORTED;
+  // Blocks of at most one page run on the fused streaming kernel; longer blocks (the
+  // prefix-only cache mode, where the block is everything after the prefix) on the
+  // 128-row query-tile kernel, one launch per part.
+  const bool wide = batch->max_block_len > kPage;
+  if (!wide && !attn_batch_supported(batch->batch)) return DLLM_ERR_UNSUPPORTED;
   DLLM_TRY(check_cache(cache, desc, merge, merge));
   if (block && !aligned(q_block, 16)) return DLLM_ERR_INVALID_ARGUMENT;
   if (!aligned(o_full, 16)) return DLLM_ERR_INVALID_ARGUMENT;
@@ -311,7 +315,13 @@ dllm_status attention_call(const dllm_layer_desc* desc, const dllm_batch* batch,
   aa.q_block = q_block;
   aa.o_full = o_full;
   aa.lse = lse;
-  DLLM_CUDA_TRY(launch_step_attention(aa, plan, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wide) {
+    if (block) DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsBlock, device_sms(), s));
+    if (merge) DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsMerge, device_sms(), s));
+    return DLLM_OK;
+  }
+  DLLM_CUDA_TRY(launch_step_attention(aa, plan, s));
   return DLLM_OK;
 }
 }  // namespace

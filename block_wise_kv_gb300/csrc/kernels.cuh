@@ -130,6 +130,13 @@ cudaError_t launch_qkv_gemm(const void* w_packed, const QkvArgs& a, const QkvPla
 // The block attention (LaCache Eq. (2)-(6) over all keys of each block row)
 // and/or the FACache merge of every invariant row, as planned by attn_plan.
 cudaError_t launch_step_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
-cudaError_t launch_state_build(const AttnArgs& a, cudaStream_t stream);
+// Attention of 128-row query tiles on the tensor cores (attn_rows.cu):
+//   kRowsState  every row of U over the keys of U: (m, l, O~) into the pools (the cache build)
+//   kRowsBlock  the block rows over every key: O and L (blocks of more than 64 rows)
+//   kRowsMerge  every row of U over the block keys, merged with its cached state: O and L
+constexpr int kRowsState = 0;
+constexpr int kRowsBlock = 1;
+constexpr int kRowsMerge = 2;
+cudaError_t launch_rows_attention(const AttnArgs& a, int mode, int num_sms, cudaStream_t stream);
 
 }  // namespace dllm

@@ -39,7 +39,8 @@ _M64 = (1 << 64) - 1
 PAGE = 64
 
 # role ids folded into seeds
-_R_WEIGHT, _R_PROMPT, _R_BLOCK, _R_MASK, _R_EMBED, _R_IDS_PROMPT, _R_IDS_BLOCK, _R_SHAPE, _R_PAGES = range(1, 10)
+(_R_WEIGHT, _R_PROMPT, _R_BLOCK, _R_MASK, _R_EMBED, _R_IDS_PROMPT, _R_IDS_BLOCK, _R_SHAPE, _R_PAGES,
+ _R_SUFFIX) = range(1, 11)
 
 
 def splitmix64(x: int) -> int:
@@ -89,6 +90,13 @@ class Config:
     vocab: int = 1024
     mask_id: int = 0
     shuffle_pages: bool = True
+    # Cache modes of the Fast-dLLM page: prefix-only caching recomputes every row after
+    # the prefix at every inner step (the fresh region C is the current block and the
+    # whole suffix); with suffix_varies the suffix rows change from one inner step to the
+    # next (as the hidden states of masked positions do in deeper layers), which a suffix
+    # refresh every r inner steps picks up.
+    prefix_only: bool = False
+    suffix_varies: bool = False
     spare_pages: int = 3
     seed: int = 0
     extra: dict = field(default_factory=dict)
@@ -103,6 +111,13 @@ class Config:
     def block_start(self, b: int, k: int | None = None) -> int:
         k = self.block_index[b] if k is None else k
         return self.t_prefix[b] + k * self.block[b]
+
+    def c_len(self, b: int, k: int | None = None) -> int:
+        """Rows of the fresh region C of sequence b at block k: the block, or
+        (prefix-only) everything from the block start to the end."""
+        if self.prefix_only:
+            return self.seq_len(b) - self.block_start(b, k)
+        return self.block[b]
 
     def num_blocks(self, b: int) -> int:
         return self.gen_len[b] // self.block[b]
@@ -190,12 +205,22 @@ class Workload:
         parts.append(self._rows_block(layer, b, k, step))
         n_suffix = c.gen_len[b] - (k + 1) * c.block[b]
         if n_suffix > 0:
-            parts.append(self._row_mask(layer, b).expand(n_suffix, c.d_model))
+            parts.append(self._rows_suffix(layer, b, k, step, n_suffix))
         return torch.cat(parts, dim=0).contiguous()
 
+    def _rows_suffix(self, layer: int, b: int, k: int, step: int, n: int) -> torch.Tensor:
+        c = self.cfg
+        if c.suffix_varies:
+            return randn_bf16((n, c.d_model), derive_seed(c.seed, _R_SUFFIX, layer, b, k, step))
+        return self._row_mask(layer, b).expand(n, c.d_model)
+
     def block_rows(self, layer: int, b: int, k: int | None = None, step: int = 0) -> torch.Tensor:
+        """The rows of C: the block's rows at this inner step, followed (prefix-only)
+        by the suffix rows."""
         c = self.cfg
         k = c.block_index[b] if k is None else k
+        if c.prefix_only:
+            return self.seq_rows(layer, b, k, step)[c.block_start(b, k):].contiguous()
         return self._rows_block(layer, b, k, step).contiguous()
 
     def batch_rows(self, layer: int = 0, step: int = 0, blocks=None):
@@ -237,7 +262,7 @@ class Workload:
             mask = torch.randn(1, c.d_model, generator=g, device=device).to(torch.bfloat16)
             n_suffix = c.gen_len[b] - (k + 1) * c.block[b]
             full.append(torch.cat([head, mask.expand(n_suffix, c.d_model)], 0))
-            blk.append(head[s0:])
+            blk.append(full[-1][s0:] if c.prefix_only else head[s0:])
         return torch.cat(full, 0).contiguous(), torch.cat(blk, 0).contiguous()
 
     # ---------------------------------------------------------------- layout
@@ -272,7 +297,7 @@ def layout(cfg: Config, blocks=None):
         bt[b, :len(pl)] = pl
     seq_len = np.array([cfg.seq_len(b) for b in range(B)], dtype=np.int32)
     bstart = np.array([cfg.block_start(b, blocks[b]) for b in range(B)], dtype=np.int32)
-    blen = np.array(cfg.block, dtype=np.int32)
+    blen = np.array([cfg.c_len(b, blocks[b]) for b in range(B)], dtype=np.int32)
     cu_block = np.concatenate([[0], np.cumsum(blen)]).astype(np.int32)
     cu_seq = np.concatenate([[0], np.cumsum(seq_len)]).astype(np.int32)
     return dict(block_table=bt, seq_len=seq_len, block_start=bstart, block_len=blen, cu_block=cu_block,

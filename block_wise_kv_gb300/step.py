@@ -81,6 +81,22 @@ class LayerStep:
         else:
             self.step_attention(stream, lse)
 
+    def inner_step(self, step: int, x_block: torch.Tensor, x_full: torch.Tensor | None = None,
+                   refresh_interval: int | None = None, stream=None, lse: bool = True) -> bool:
+        """Inner step `step` (0-based) of the current block with the suffix
+        refresh schedule of the Fast-dLLM page ("Suffix Cache Refresh"): with
+        refresh_interval = r the cache is rebuilt from the rows of this step
+        (x_full) before the steps r, 2r, ... of the block; with None only the
+        block boundary builds it (the caller's boundary() before step 0).
+        Returns whether the cache was rebuilt."""
+        due = refresh_due(step, refresh_interval)
+        if due:
+            if x_full is None:
+                raise ValueError(f"inner step {step} refreshes the cache: x_full is needed")
+            self.boundary(x_full, stream)
+        self.step(x_block, stream, lse)
+        return due
+
     # ---------------------------------------------------------- inspection
     def seq_slice(self, b: int) -> slice:
         cu = self.batch.host["cu_seq"]
@@ -95,6 +111,17 @@ class LayerStep:
         return dllm.gather_rows(pool, self.batch.host["block_table"], b, n)
 
 
+def refresh_due(step: int, refresh_interval: int | None) -> bool:
+    """Whether inner step `step` (> 0) of a block rebuilds the cache first:
+    every r-th step for refresh_interval = r, never for None (the block
+    boundary, before step 0, always builds it)."""
+    if refresh_interval is None:
+        return False
+    if refresh_interval < 1:
+        raise ValueError("refresh_interval must be >= 1 or None")
+    return step > 0 and step % refresh_interval == 0
+
+
 def block_rows_of(wl: Workload, layer: int, step: int, blocks) -> torch.Tensor:
     cfg = wl.cfg
     return torch.cat([wl.block_rows(layer, b, blocks[b], step) for b in range(cfg.batch)], 0).contiguous()
@@ -105,4 +132,4 @@ def full_rows_of(wl: Workload, layer: int, step: int, blocks) -> torch.Tensor:
     return torch.cat([wl.seq_rows(layer, b, blocks[b], step) for b in range(cfg.batch)], 0).contiguous()
 
 
-__all__ = ["LayerStep", "block_rows_of", "full_rows_of"]
+__all__ = ["LayerStep", "block_rows_of", "full_rows_of", "refresh_due"]

@@ -57,17 +57,18 @@ def oracle_step(wl: Workload, layer: int, b: int, k: int, step: int, rows=None, 
                           cfg.rms_eps, rows=rows)
 
 
-def oracle_cache_state(wl: Workload, layer: int, b: int, k: int, W=None, g=None):
-    """Oracle FACache contents after the boundary of block k of sequence b:
-    (rows of U, m, l, O~) over the keys of U."""
+def oracle_cache_state(wl: Workload, layer: int, b: int, k: int, W=None, g=None, step: int = 0):
+    """Oracle FACache contents after a cache build of block k of sequence b
+    from the rows of inner step `step` (0: the block boundary): (rows of U,
+    m, l, O~) over the keys of U."""
     cfg = wl.cfg
     if W is None:
         W, g = wl.weights(layer)
-    x = wl.seq_rows(layer, b, k, 0).double().numpy()
+    x = wl.seq_rows(layer, b, k, step).double().numpy()
     ref = orc.layer_step(x, g.double().numpy(), W.double().numpy(), cfg.n_heads, cfg.head_dim, cfg.rope_theta,
                          cfg.rms_eps)
     s = cfg.block_start(b, k)
-    e = s + cfg.block[b]
+    e = s + cfg.c_len(b, k)
     U = np.r_[0:s, e:x.shape[0]]
     m, l, Ot = orc.state_build(ref["q"][U], ref["k"], ref["v"], 1.0 / np.sqrt(cfg.head_dim), s, e)
     return U, m, l, Ot

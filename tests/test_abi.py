@@ -92,7 +92,7 @@ def test_bad_layer_desc(lib, kw, status):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(batch=-1), dllm.DLLM_ERR_INVALID_ARGUMENT),
-    (dict(max_block=65), dllm.DLLM_ERR_UNSUPPORTED),
+    (dict(max_block=769), dllm.DLLM_ERR_INVALID_ARGUMENT),  # a block longer than the longest sequence
     (dict(max_pages=2), dllm.DLLM_ERR_INVALID_ARGUMENT),   # 2 pages cannot hold 768 tokens
     (dict(M=100), dllm.DLLM_ERR_INVALID_ARGUMENT),         # more block rows than batch * max_block_len
     (dict(R=2000), dllm.DLLM_ERR_INVALID_ARGUMENT),        # more rows than batch * max_seq_len

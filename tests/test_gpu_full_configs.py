@@ -59,7 +59,7 @@ def _check(cfg, layer, k_of, steps, seqs, heads_of, split=False):
             assert_close(o, ref["O"], f"O {what}")
             assert_close(lse, ref["L"], f"LSE {what}", max_abs=2e-2, rel=1e-3)
             c0 = cfg.block_start(b, k_of[b])
-            blk = slice(c0, c0 + cfg.block[b])
+            blk = slice(c0, c0 + cfg.c_len(b, k_of[b]))
             kk = to_np(st.pool_rows(st.cache.k, b))[blk][:, heads]
             vv = to_np(st.pool_rows(st.cache.v, b))[blk][:, heads]
             assert_bf16_close(kk, ref["k"][blk], f"k block rows {what}")

@@ -70,7 +70,7 @@ def _run_block(cfg: Config, k_of, steps, layer=0, check_cache=True, check_qkv=Tr
             assert_close(lse[sel], ref["L"], f"LSE seq {b} step {s}", max_abs=2e-2, rel=1e-3)
             if check_qkv:
                 c0 = cfg.block_start(b, k_of[b])
-                blk = slice(c0, c0 + cfg.block[b])
+                blk = slice(c0, c0 + cfg.c_len(b, k_of[b]))
                 kk = to_np(st.pool_rows(st.cache.k, b))
                 vv = to_np(st.pool_rows(st.cache.v, b))
                 assert_bf16_close(kk[blk], ref["k"][blk], f"k block rows seq {b}")
