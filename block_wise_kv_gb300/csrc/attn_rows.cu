@@ -18,9 +18,10 @@
 // A unit of work is (sequence b, head h, a pair of query tiles): two tiles of
 // 128 query rows that share every K/V page the unit streams.  Warp 9 streams
 // the query tiles and the K/V pages (TMA, 128-byte swizzle) into an mbarrier
-// ring; warp 8 issues, per page, S_t = Q_t K^T into one of two score buffers
-// of tile t and then O_t += P_t V of the previous page (P_t from shared
-// memory, V as an MN-major operand), with S, O in tensor memory; warps 0-3
+// ring; warps 8 (tile 0) and 10 (tile 1) issue, per page, S_t = Q_t K^T into
+// one of two score buffers of tile t and then O_t += P_t V of the previous
+// page (P_t from shared memory, V as an MN-major operand), with S, O in
+// tensor memory; warps 0-3
 // (tile 0) and 4-7 (tile 1) run the softmax, one thread per query row (TMEM
 // lane = row).  The reference max of a row is raised (its O row and sum
 // rescaled) only when a page's max exceeds it by more than 2^8, so every P
@@ -36,7 +37,7 @@ namespace dllm {
 namespace {
 using namespace attn;
 
-constexpr int kThreads = 320;  // warps 0-7 softmax, 8 MMA issuer, 9 producer
+constexpr int kThreads = 352;  // warps 0-7 softmax, 8 and 10 MMA issuers, 9 producer
 constexpr int kMaxSeqs = 1024;  // sequences per launch (the host launches larger batches in slices)
 constexpr float kRescale = 8.f;  // log2 units
 
@@ -236,10 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&S.kvfull[s], 1);
-      mbar_init(&S.kvempty[s], 1);  // one commit after the last MMA that reads the stage
+      mbar_init(&S.kvempty[s], 2);  // a commit of each issuer after its last MMA that reads the stage
     }
     mbar_init(&S.qfull, 1);
-    mbar_init(&S.qempty, 1);
+    mbar_init(&S.qempty, 2);  // both issuers
     for (int t = 0; t < 2; ++t) {
       for (int b = 0; b < 2; ++b) {
         mbar_init(&S.sfull[t][b], 1);
@@ -362,61 +363,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq >= 1 && !mbar_wait(&S.qempty, (nq - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
     __syncwarp();
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per page i of a unit: S_t(i) = Q_t K_i^T for each tile, then O_t += P_t(i-1) V_{i-1}
-    // (the scores of page i run while the softmax of page i-1 finishes).
+  } else if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per query tile t (warp 8: tile 0, warp 10: tile 1), so that neither
+    // tile's MMAs wait for the other tile's softmax.  Per page i of a unit: S_t(i) =
+    // Q_t K_i^T, then O_t += P_t(i-1) V_{i-1} (the scores of page i run while the softmax
+    // of page i-1 finishes).  A stage is free once both issuers have committed its last
+    // MMAs; the issuer of tile 1 walks (and releases) the pages of a unit without a
+    // second tile too.
     if (lane == 0) {
       constexpr uint32_t kIdS = umma_idesc_bf16(128, 64);
       constexpr uint32_t kIdO = umma_idesc_bf16_bmn(128, D);
-      int nkv = 0, nq = 0;
-      int ns[2] = {0, 0}, npv[2] = {0, 0}, no[2] = {0, 0};  // per tile: S buffers, P V, units
-      const uint32_t qa0 = smem_u32(q_tiles), ring0 = smem_u32(kv_ring), pa0 = smem_u32(p_tiles);
+      const int t = warp == 8 ? 0 : 1;
+      int nkv = 0, nq = 0, ns = 0, npv = 0, no = 0;  // stages, units, S buffers, P V, units of tile t
+      const uint32_t qa = smem_u32(q_tiles + t * C::QB), ring0 = smem_u32(kv_ring);
+      const uint32_t pa = smem_u32(p_tiles + t * C::PB);
       for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
-        const int T = w.has1() ? 2 : 1;
+        const bool mine = t == 0 || w.has1();
         const int nk = w.s.nk;
         wait_or_abort(S, &S.qfull, nq & 1, bt.err);
         tc_fence_after();
         // O_t += P_t V of page i (stage st); the unit's first overwrites O_t once the
         // softmax warps have read the previous unit's O_t out
         auto pv = [&](int i, int st) {
-          const uint32_t va = ring0 + st * C::KVB + TB;
-          for (int t = 0; t < T; ++t) {
-            wait_or_abort(S, &S.pfull[t], npv[t] & 1, bt.err);
-            if (i == 0 && no[t] >= 1) wait_or_abort(S, &S.ofree[t], (no[t] - 1) & 1, bt.err);
+          if (mine) {
+            wait_or_abort(S, &S.pfull[t], npv & 1, bt.err);
+            if (i == 0 && no >= 1) wait_or_abort(S, &S.ofree[t], (no - 1) & 1, bt.err);
             tc_fence_after();
-            const uint32_t pa = pa0 + t * C::PB;
+            const uint32_t va = ring0 + st * C::KVB + TB;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + t * D, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
                         (i > 0 || kk > 0) ? 1u : 0u);
             umma_commit(&S.pfree[t]);
-            ++npv[t];
+            ++npv;
             if (i == nk - 1) {
               umma_commit(&S.ofull[t]);
-              ++no[t];
+              ++no;
             }
           }
-          umma_commit(&S.kvempty[st]);  // every MMA that reads the stage has completed
+          umma_commit(&S.kvempty[st]);  // this issuer's MMAs that read the stage have completed
         };
         int prev_st = 0;
         for (int i = 0; i < nk; ++i, ++nkv) {
           const int st = nkv % NST;
           wait_or_abort(S, &S.kvfull[st], (nkv / NST) & 1, bt.err);
           tc_fence_after();
-          const uint32_t ka = ring0 + st * C::KVB;
-          for (int t = 0; t < T; ++t) {
-            const int bsel = ns[t] & 1;
-            if (ns[t] >= 2) wait_or_abort(S, &S.sfree[t][bsel], ((ns[t] >> 1) - 1) & 1, bt.err);
+          if (mine) {
+            const int bsel = ns & 1;
+            if (ns >= 2) wait_or_abort(S, &S.sfree[t][bsel], ((ns >> 1) - 1) & 1, bt.err);
             tc_fence_after();
-            const uint32_t qa = qa0 + t * C::QB;
+            const uint32_t ka = ring0 + st * C::KVB;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
               umma_bf16(tmem + C::kTmemS + (2 * t + bsel) * 64,
                         umma_desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32),
                         umma_desc_sw128(ka + (kk >> 2) * 8192 + (kk & 3) * 32), kIdS, kk > 0 ? 1u : 0u);
             umma_commit(&S.sfull[t][bsel]);
-            ++ns[t];
+            ++ns;
           }
           if (i == nk - 1) umma_commit(&S.qempty);  // the unit's queries are no longer read
           if (i >= 1) pv(i - 1, prev_st);
@@ -425,9 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nk >= 1) pv(nk - 1, prev_st);
         ++nq;
       }
-      // Tail: each tile's last P V commit has arrived before the CTA can exit.
-      for (int t = 0; t < 2; ++t)
-        if (npv[t] >= 1 && !mbar_wait(&S.pfree[t], (npv[t] - 1) & 1)) report_error(bt.err, kErrTimeout);
+      // Tail: the last P V commit has arrived before the CTA can exit.
+      if (npv >= 1 && !mbar_wait(&S.pfree[t], (npv - 1) & 1)) report_error(bt.err, kErrTimeout);
     }
     __syncwarp();
   } else {
@@ -464,15 +467,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.sfree[t][bsel]);
         ++ns;
-        // scale, mask the keys outside this mode's key set, this row's page max
+        // this row's page max over the keys of this mode's key set (raw scores: the scale is
+        // positive, so it is applied to the max and folded into the exponent below); a page
+        // whose keys all belong to the set takes the unmasked path (uniform per page)
         const int key0 = key_page(w.s, MODE, i) * kPage;
-        float mx4[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+        bool all_valid;
+        if (MODE == kRowsState)
+          all_valid = key0 + kPage <= nb && (key0 + kPage <= sb || key0 >= ce);
+        else if (MODE == kRowsMerge)
+          all_valid = key0 >= sb && key0 + kPage <= ce;
+        else
+          all_valid = key0 + kPage <= nb;
+        if (!all_valid) {
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) {
-          sc[cc] = key_valid<MODE>(key0 + cc, nb, sb, ce) ? sc[cc] * a.scale_log2 : neg_inf();
-          mx4[cc & 3] = fmaxf(mx4[cc & 3], sc[cc]);
+          for (int cc = 0; cc < 64; ++cc)
+            if (!key_valid<MODE>(key0 + cc, nb, sb, ce)) sc[cc] = neg_inf();
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = sc[e];
+#pragma unroll
+        for (int cc = 8; cc < 64; ++cc) mx8[cc & 7] = fmaxf(mx8[cc & 7], sc[cc]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * a.scale_log2;
         m_true = fmaxf(m_true, mx);
         // a new reference max (the unit's first page, or a rise beyond the threshold)
         float factor = 1.f;
@@ -483,13 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
         const float mu = m_ref == neg_inf() ? 0.f : m_ref;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int cc = 0; cc < 64; ++cc) {
-          sc[cc] = fast_exp2(sc[cc] - mu);
-          l4[cc & 3] += sc[cc];
+          sc[cc] = fast_exp2(fmaf(sc[cc], a.scale_log2, -mu));  // masked: 2^-inf = 0
+          l8[cc & 7] += sc[cc];
         }
-        l = l * factor + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        l = l * factor + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         // the tile's previous P V has completed: its P tile is free and O_t holds every
         // earlier page (rescaled here when the reference max rose)
         if (pw >= 1) wait_or_abort(S, &S.pfree[t], (pw - 1) & 1, bt.err);
