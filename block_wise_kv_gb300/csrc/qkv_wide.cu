@@ -72,11 +72,31 @@ constexpr int kDynSmem = kStages * kStageBytes + kStagingBytes + 1024;  // + ali
 constexpr uint32_t kTmemCols = 512;      // two chunk buffers of kTN columns
 constexpr int kColsPerThread = kTN / 2;  // two accumulator warps per lane quadrant
 constexpr int kPartialFloats = kTM * kTN;
+constexpr int kNormVec = 16;             // RMSNorm: 16-byte pieces of a row a lane holds (rows up to 4096 wide)
 
 // Stream-K: CTA c owns units [c U / G, (c + 1) U / G); the CTA that owns unit u.
 __host__ __device__ __forceinline__ long long wk_begin(long long c, long long U, long long G) { return c * U / G; }
 __host__ __device__ __forceinline__ int wk_cta_of(long long u, long long U, long long G) {
   return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+// Tile order: the weight tiles go in bands of `band` tiles (the last band may be
+// narrower); within a band, token tile by token tile, weight tile fastest.  The CTAs
+// running at one time then share one band of the weight, which stays resident in L2
+// while every token tile passes over it (with all weight tiles in one order, each wave
+// of tiles touched the whole weight and the pool writes evicted it between waves).
+__device__ __forceinline__ void tile_coords(int tile, int n_wt, int n_tt, int band, int& wt, int& tt) {
+  const int full = n_wt / band;  // bands of `band` weight tiles
+  const int in_full = full * band * n_tt;
+  if (tile < in_full) {
+    const int b = tile / (band * n_tt), r = tile % (band * n_tt);
+    tt = r / band;
+    wt = b * band + r % band;
+  } else {
+    const int rest = n_wt - full * band, r = tile - in_full;
+    tt = r / rest;
+    wt = full * band + r % rest;
+  }
 }
 
 // The walk of a CTA's work: segments (one tile, a contiguous range of its K
@@ -88,9 +108,15 @@ struct SegWalk {
   bool sk;           // stream-K (else whole tiles c, c + G, ...)
   long long sk_u, sk_hi;
   int tile, c0, c1, ch;
+  int wt, tt;  // the tile's weight tile and token tile
+  int n_wt, n_tt, band;
   bool ok;
 
-  __device__ __forceinline__ void init(int cta, int grid, int n_chunks, int tiles, bool streamk) {
+  __device__ __forceinline__ void init(int cta, int grid, int n_chunks, int tiles, bool streamk, int wtiles,
+                                       int wband) {
+    n_wt = wtiles;
+    n_tt = tiles / wtiles;
+    band = wband;
     c = cta;
     G = grid;
     nck = n_chunks;
@@ -123,6 +149,7 @@ struct SegWalk {
       c1 = nck;
     }
     ch = c0;
+    if (ok) tile_coords(tile, n_wt, n_tt, band, wt, tt);
   }
   __device__ __forceinline__ void next_chunk() {
     if (++ch == c1) next_segment();
@@ -180,7 +207,7 @@ __device__ __forceinline__ void resolve_columns(const QkvArgs& a, int tt, int at
 
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_wide_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                    const QkvArgs a, int n_wt, int n_tiles, int streamk) {
+                    const QkvArgs a, int n_wt, int band, int n_tiles, int streamk) {
   constexpr uint32_t kIdesc = umma_idesc_bf16(kTM, kTN);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -230,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npre = 0;
       if (lane == 0) {
         SegWalk w;
-        w.init(blockIdx.x, G, nck, n_tiles, sk);
+        w.init(blockIdx.x, G, nck, n_tiles, sk, n_wt, band);
         for (int k = 0; k < kStages / 2 && w.ok; ++k, w.next_chunk())
           for (int hb = 0; hb < 2; ++hb, ++npre) {
             mbar_arrive_expect_tx(&full_bar[npre], kStageBytes);
             tma_load_2d(smem + npre * kStageBytes, &tm_w, &full_bar[npre], 0,
-                        ((w.tile % n_wt) * kbp + 2 * w.ch + hb) * kTM);
+                        (w.wt * kbp + 2 * w.ch + hb) * kTM);
           }
         griddep_wait();
         const uint64_t t0 = global_timer_ns();  // bounded wait for the x^ rows
@@ -252,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier_arrive(2, 32 + kAcc);  // this CTA's producer no longer reads the claim counters
       if (lane == 0) {
         SegWalk w;
-        w.init(blockIdx.x, G, nck, n_tiles, sk);
+        w.init(blockIdx.x, G, nck, n_tiles, sk, n_wt, band);
         int q = 0;
         bool ok = true;
         for (; w.ok && ok; w.next_chunk()) {
-          const int wt = w.tile % n_wt, tt = w.tile / n_wt;
+          const int wt = w.wt, tt = w.tt;
           for (int hb = 0; hb < 2; ++hb, ++q) {
             const int s = q % kStages;
             uint8_t* st = smem + s * kStageBytes;
@@ -286,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Chunk n (K = 128: two ring stages) goes to TMEM buffer n % 2.
       if (lane == 0) {
         SegWalk w;
-        w.init(blockIdx.x, G, nck, n_tiles, sk);
+        w.init(blockIdx.x, G, nck, n_tiles, sk, n_wt, band);
         int q = 0, nc = 0;
         bool ok = true;
         for (; w.ok && ok; w.next_chunk(), ++nc) {
@@ -388,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur_tt = -1;  // the token tile tok_* describe
     bool ok = true;   // after a timed-out wait the walk goes on (same barriers) without waiting
     SegWalk w;
-    w.init(blockIdx.x, G, nck, n_tiles, sk);
+    w.init(blockIdx.x, G, nck, n_tiles, sk, n_wt, band);
     for (int nc = 0; w.ok; w.next_chunk(), ++nc) {
       const int b = nc & 1;
       if (ok && !mbar_wait(&tfull_bar[b], (nc >> 1) & 1)) {
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- epilogue of the tile: rotate q/k, round to bf16, write 16-byte runs
-      const int wt = tile % n_wt, tt = tile / n_wt;
+      const int wt = w.wt, tt = w.tt;
       if (tt != cur_tt) {
         named_barrier(1, kAcc);  // the previous tile's columns are no longer read
         resolve_columns(a, tt, at, tok_kv, tok_q, tok_pos);
@@ -454,9 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grow0 = wt * kTM;
       const int which = grow0 / HD;  // 0: q, 1: k, 2: v
       const int head0 = (grow0 % HD) / d;
+      constexpr int kPassesPerHalf = kColsPerThread / kStagingCols;
 #pragma unroll
       for (int pass = 0; pass < (kTN / kStagingCols); ++pass) {
-        constexpr int kPassesPerHalf = kColsPerThread / kStagingCols;
         const int ph = pass / kPassesPerHalf, pc = pass % kPassesPerHalf;
         if (half == ph) {
 #pragma unroll
@@ -605,7 +632,11 @@ cudaError_t launch_qkv_wide(const void* w_packed, const QkvArgs& a, const QkvPla
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qkv_wide_kernel, tm_w, tm_x, a, n_wt, plan.n_tiles, plan.streamk ? 1 : 0);
+  // weight band: about 48 MB of weight tiles (a third of L2), at least one tile
+  const long long tile_bytes = static_cast<long long>(kTM) * qkv_boxes_per_tile(a.d_model) * kBK * 2;
+  int band = static_cast<int>((48LL << 20) / tile_bytes);
+  band = band < 1 ? 1 : (band > n_wt ? n_wt : band);
+  return cudaLaunchKernelEx(&cfg, qkv_wide_kernel, tm_w, tm_x, a, n_wt, band, plan.n_tiles, plan.streamk ? 1 : 0);
 }
 
 }  // namespace dllm
