@@ -1,19 +1,34 @@
 // attn_rows.cu — attention of 128-row query tiles on the 5th-generation tensor
-// cores (sm_103a), in three modes that share one persistent kernel:
+// cores (sm_103a), in the modes of one persistent kernel.  Each mode gives,
+// per sequence, the query rows (up to two position ranges) and the keys, in
+// up to two phases:
 //
-//   kRowsState   the FACache build of a block boundary: every row r of U
-//                over the keys of U only, the online-softmax state
-//                (m, l, O~) into m_pool / l_pool / o_pool (LaCache §3.3.3;
-//                Algorithm 1 with GenStep = True).
-//   kRowsBlock   the block attention of blocks longer than one page: the
-//                block rows (from q_block) over every key of the sequence,
-//                O = O~ / l and L = m + ln l (Fast-dLLM DualCache "Inner step
-//                on block k", LaCache Eq. (2)-(6)).  This is the prefix-only
-//                cache mode of the Fast-dLLM page, where the block is the
-//                whole region after the prefix.
-//   kRowsMerge   the FACache merge for such blocks: every row of U over the
-//                block keys, merged exactly with its cached state (LaCache
-//                §3.3.3, Algorithm 1 with GenStep = False).
+//   kRowsState     the FACache build of a block boundary: every row r of U
+//                  over the keys of U only, the online-softmax state
+//                  (m, l, O~) into m_pool / l_pool / o_pool (LaCache §3.3.3;
+//                  Algorithm 1 with GenStep = True).
+//   kRowsBlock     the block attention of blocks longer than one page: the
+//                  block rows (from q_block) over every key of the sequence,
+//                  O = O~ / l and L = m + ln l (Fast-dLLM DualCache "Inner step
+//                  on block k", LaCache Eq. (2)-(6)).  This is the prefix-only
+//                  cache mode of the Fast-dLLM page, where the block is the
+//                  whole region after the prefix.
+//   kRowsMerge     the FACache merge for such blocks: every row of U over the
+//                  block keys, merged exactly with its cached state (LaCache
+//                  §3.3.3, Algorithm 1 with GenStep = False).
+//   kRowsStatePre  kRowsState, with the state of each row over the keys before
+//                  the block (phase 1) also kept in the pre pools.
+//   kRowsAdvOld,   the incremental block boundary (only the just-decoded
+//   kRowsAdvNew    block's rows changed since the last one): the rows kept
+//                  from the last boundary extend their pre state by the
+//                  decoded block's keys (phase 1); the decoded rows build it
+//                  over every key before the new block (phase 1); both then
+//                  add the suffix keys (phase 2) for the state over U.
+//
+// In the modes with a pre state, the state after phase 1 (merged with the
+// pre state read in, for kRowsAdvOld) is written to the pre pools, phase 2
+// starts from an empty accumulator, and the final state is the exact merge
+// (LaCache §3.3.3) of the pre state just written with phase 2's.
 //
 // A unit of work is (sequence b, head h, a pair of query tiles): two tiles of
 // 128 query rows that share every K/V page the unit streams.  Warp 9 streams
@@ -21,14 +36,13 @@
 // ring; warps 8 (tile 0) and 10 (tile 1) issue, per page, S_t = Q_t K^T into
 // one of two score buffers of tile t and then O_t += P_t V of the previous
 // page (P_t from shared memory, V as an MN-major operand), with S, O in
-// tensor memory; warps 0-3
-// (tile 0) and 4-7 (tile 1) run the softmax, one thread per query row (TMEM
-// lane = row).  The reference max of a row is raised (its O row and sum
-// rescaled) only when a page's max exceeds it by more than 2^8, so every P
-// stays <= 2^8; the exact max is tracked beside it for the state build's m.
-// Units are split over the CTAs by their K/V pages (every unit of a sequence
-// streams the same pages), and a CTA walks its units in order, loading the
-// next unit's query tiles while the current one finishes.
+// tensor memory; warps 0-3 (tile 0) and 4-7 (tile 1) run the softmax, one
+// thread per query row (TMEM lane = row).  The reference max of a row is
+// raised (its O row and sum rescaled) only when a page's max exceeds it by
+// more than 2^8, so every P stays <= 2^8; the exact max is tracked beside it
+// for the states' m.  Units are split over the CTAs by their K/V pages (every
+// unit of a sequence streams the same pages), and a CTA walks its units in
+// order, loading the next unit's query tiles while the current one finishes.
 #include <math.h>
 
 #include "attn_common.cuh"
@@ -66,15 +80,16 @@ struct RowsShared {
   long long cu_cost[kMaxSeqs + 1];   // K/V page prefix (the cost of the units)
 };
 
-// Per-sequence shape of the work of one mode: which query tiles (of 128 rows)
-// and which K/V pages (of 64 keys) a unit of the sequence covers.
+// Per-sequence shape of the work of one mode: the query rows, the query tiles
+// (of 128 rows) that hold them, and the K/V pages (of 64 keys) of the two key
+// phases.
 struct RowsSeq {
   SeqMeta sm;
-  int np;        // pages of the sequence
-  int nq;        // query tiles
-  int lo_t, hi_t;  // query tile k -> tile index: k < lo_t ? k : hi_t + (k - lo_t)
-  int lo_p, hi_p, end_p;  // K/V pages [0, lo_p) and [hi_p, end_p) (kRowsMerge: [lo_p, hi_p) only)
-  int nk;        // K/V pages per unit
+  int np;                  // pages of the sequence
+  int r0, r1, r2, r3;      // query rows [r0, r1) u [r2, r3) (kRowsBlock: block rows, relative)
+  int k0, k1, k2, k3;      // keys: phase 1 [k0, k1), phase 2 [k2, k3)
+  int nq, ta0, na, tb0;    // query tiles: tile k -> k < na ? ta0 + k : tb0 + (k - na)
+  int p1, n1, p2, n2, nk;  // key pages: p1 .. p1 + n1 - 1, then p2 .. p2 + n2 - 1
 };
 
 __device__ __forceinline__ SeqMeta load_meta_rows(const BatchArgs& bt, int b) {
@@ -90,57 +105,69 @@ __device__ __forceinline__ SeqMeta load_meta_rows(const BatchArgs& bt, int b) {
   return m;
 }
 
-__device__ __forceinline__ RowsSeq rows_seq(const BatchArgs& bt, int b, int mode) {
+__device__ __forceinline__ RowsSeq rows_seq(const AttnArgs& a, int b, int mode) {
   RowsSeq s;
-  s.sm = load_meta_rows(bt, b);
-  s.nq = 0;
-  s.nk = 0;
-  s.lo_t = s.hi_t = s.lo_p = s.hi_p = s.end_p = 0;
-  s.np = 0;
+  s.sm = load_meta_rows(a.bt, b);
+  s.np = s.nq = s.na = s.ta0 = s.tb0 = s.nk = s.n1 = s.n2 = s.p1 = s.p2 = 0;
+  s.r0 = s.r1 = s.r2 = s.r3 = s.k0 = s.k1 = s.k2 = s.k3 = 0;
   if (!s.sm.ok) return s;
   const int nb = s.sm.nb, sb = s.sm.sb, ce = s.sm.sb + s.sm.bb;  // C = [sb, ce)
+  int ps = 0;  // the decoded block [ps, sb)
+  if (mode == kRowsAdvOld || mode == kRowsAdvNew) {
+    ps = __ldg(a.prev_start + b);
+    if (ps < 0 || ps >= sb) {
+      s.sm.ok = false;
+      return s;
+    }
+  }
   s.np = (nb + kPage - 1) / kPage;
-  if (mode == kRowsBlock) {
-    s.nq = (s.sm.bb + 127) / 128;
-    s.lo_t = s.nq;
-    s.hi_t = 0;
-  } else {
-    // the tiles that hold rows of U = [0, sb) u [ce, nb)
-    s.lo_t = (sb + 127) / 128;
-    s.hi_t = s.lo_t;
-    int hi_end = s.lo_t;
-    if (ce < nb) {
-      s.hi_t = max(ce / 128, s.lo_t);
-      hi_end = (nb + 127) / 128;
-    }
-    s.nq = s.lo_t + (hi_end - s.hi_t);
+  switch (mode) {
+    case kRowsBlock:  // the block rows over every key
+      s.r0 = 0, s.r1 = s.sm.bb, s.k0 = 0, s.k1 = nb;
+      break;
+    case kRowsMerge:  // U over the keys of C
+      s.r0 = 0, s.r1 = sb, s.r2 = ce, s.r3 = nb, s.k0 = sb, s.k1 = ce;
+      break;
+    case kRowsAdvOld:  // the rows kept: the decoded block's keys, then the suffix
+      s.r0 = 0, s.r1 = ps, s.r2 = ce, s.r3 = nb, s.k0 = ps, s.k1 = sb, s.k2 = ce, s.k3 = nb;
+      break;
+    case kRowsAdvNew:  // the decoded rows: every key before the block, then the suffix
+      s.r0 = ps, s.r1 = sb, s.k0 = 0, s.k1 = sb, s.k2 = ce, s.k3 = nb;
+      break;
+    default:  // kRowsState, kRowsStatePre: U over the prefix, then the suffix
+      s.r0 = 0, s.r1 = sb, s.r2 = ce, s.r3 = nb, s.k0 = 0, s.k1 = sb, s.k2 = ce, s.k3 = nb;
+      break;
   }
-  if (mode == kRowsState) {  // the pages that hold keys of U
-    s.lo_p = (sb + kPage - 1) / kPage;
-    s.hi_p = s.lo_p;
-    s.end_p = s.lo_p;
-    if (ce < nb) {
-      s.hi_p = max(ce / kPage, s.lo_p);
-      s.end_p = s.np;
-    }
-    s.nk = s.lo_p + (s.end_p - s.hi_p);
-  } else if (mode == kRowsMerge) {  // the pages that hold keys of C
-    s.lo_p = sb / kPage;
-    s.hi_p = (ce - 1) / kPage + 1;
-    s.nk = s.hi_p - s.lo_p;
+  // query tiles over the row ranges (kRowsBlock: tiles of the block rows)
+  int ta1 = s.r1 > s.r0 ? (s.r1 + 127) / 128 : s.r0 / 128;
+  int tb1 = s.r3 > s.r2 ? (s.r3 + 127) / 128 : s.r2 / 128;
+  s.ta0 = s.r0 / 128;
+  s.tb0 = s.r2 / 128;
+  if (ta1 == s.ta0) {  // first range empty
+    s.ta0 = s.tb0;
+    ta1 = tb1;
+    s.tb0 = tb1;
   } else {
-    s.lo_p = s.np;
-    s.hi_p = s.end_p = s.np;
-    s.nk = s.np;
+    s.tb0 = max(s.tb0, ta1);
+    tb1 = max(tb1, s.tb0);
   }
+  s.na = ta1 - s.ta0;
+  s.nq = s.na + (tb1 - s.tb0);
+  // key pages of the two phases (a page may hold keys of both: it is streamed twice)
+  if (s.k1 > s.k0) {
+    s.p1 = s.k0 / kPage;
+    s.n1 = (s.k1 + kPage - 1) / kPage - s.p1;
+  }
+  if (s.k3 > s.k2) {
+    s.p2 = s.k2 / kPage;
+    s.n2 = (s.k3 + kPage - 1) / kPage - s.p2;
+  }
+  s.nk = s.n1 + s.n2;
   return s;
 }
 
-// The i-th K/V page of a unit of sequence s.
-__device__ __forceinline__ int key_page(const RowsSeq& s, int mode, int i) {
-  if (mode == kRowsMerge) return s.lo_p + i;
-  return i < s.lo_p ? i : s.hi_p + (i - s.lo_p);
-}
+// The i-th K/V page of a unit of sequence s, and the key range of its phase.
+__device__ __forceinline__ int key_page(const RowsSeq& s, int i) { return i < s.n1 ? s.p1 + i : s.p2 + (i - s.n1); }
 
 // The first unit, in unit order, whose first page is at or after page x of the launch's
 // cost (K/V pages): CTA c owns the units that start in [c W / G, (c + 1) W / G).  Every
@@ -164,7 +191,7 @@ struct RWalk {
   long long u, u1;
   int b, h, pr, npairs;
   RowsSeq s;
-  __device__ __forceinline__ void seek(const RowsShared& S, const BatchArgs& bt, int mode, int b_begin, int nseq,
+  __device__ __forceinline__ void seek(const RowsShared& S, const AttnArgs& a, int mode, int b_begin, int nseq,
                                        int H) {
     int lo = 0, hi = nseq - 1;  // the largest b with cu_units[b] <= u: skips sequences without units
     while (lo < hi) {
@@ -175,26 +202,26 @@ struct RWalk {
         hi = mid - 1;
     }
     b = lo;
-    s = rows_seq(bt, b_begin + b, mode);
+    s = rows_seq(a, b_begin + b, mode);
     npairs = static_cast<int>((S.cu_units[b + 1] - S.cu_units[b]) / H);
     const int r = static_cast<int>(u - S.cu_units[b]);
     h = r / npairs;
     pr = r % npairs;
   }
   __device__ __forceinline__ bool valid() const { return u < u1; }
-  __device__ __forceinline__ void next(const RowsShared& S, const BatchArgs& bt, int mode, int b_begin, int nseq,
+  __device__ __forceinline__ void next(const RowsShared& S, const AttnArgs& a, int mode, int b_begin, int nseq,
                                        int H) {
     if (++u >= u1) return;
     if (++pr == npairs) {
       pr = 0;
-      if (++h == H) seek(S, bt, mode, b_begin, nseq, H);
+      if (++h == H) seek(S, a, mode, b_begin, nseq, H);
     }
   }
   __device__ __forceinline__ bool has1() const { return 2 * pr + 1 < s.nq; }
   // tile index (of 128 rows) of query tile t of the unit
   __device__ __forceinline__ int tile(int t) const {
     const int k = 2 * pr + t;
-    return k < s.lo_t ? k : s.hi_t + (k - s.lo_t);
+    return k < s.na ? s.ta0 + k : s.tb0 + (k - s.na);
   }
 };
 
@@ -207,12 +234,48 @@ __device__ __forceinline__ void wait_or_abort(RowsShared& S, uint64_t* bar, uint
   }
 }
 
-// Is key position kp (of page key0 + c) a key of this mode?
-template <int MODE>
-__device__ __forceinline__ bool key_valid(int kp, int nb, int sb, int ce) {
-  if (MODE == kRowsState) return kp < nb && (kp < sb || kp >= ce);
-  if (MODE == kRowsMerge) return kp >= sb && kp < ce;
-  return kp < nb;
+// Write row srow of a state (m in natural units, l, O~) to the pools (mo, lo, oo):
+// the exact merge (LaCache §3.3.3) of the state read from (mi, li, oi) when
+// has_init with the accumulator's (reference max m_ref, exact max m_true, sum l,
+// O_t's row at o_row when have_o), both taken relative to their common max.
+// The O_t row is read by the whole warp (tcgen05.ld), the pools only for
+// row_out; init and output may be the same pools (read before written).
+template <int D>
+__device__ __forceinline__ void store_state(uint32_t o_row, bool have_o, float m_ref, float m_true, float l,
+                                            bool has_init, const float* mi_p, const float* li_p, const float* oi_p,
+                                            float* mo_p, float* lo_p, float* oo_p, size_t srow, bool row_out) {
+  float mi = neg_inf(), li = 0.f;
+  if (has_init && row_out) {
+    mi = mi_p[srow] * 1.4426950408889634f;  // base-2 units
+    li = li_p[srow];
+  }
+  const float M = fmaxf(mi, m_true);
+  const float wi = mi == neg_inf() ? 0.f : fast_exp2(mi - M);
+  const float wf = (!have_o || m_ref == neg_inf()) ? 0.f : fast_exp2(m_ref - M);
+  if (row_out) {
+    mo_p[srow] = M * kLn2;  // -inf stays -inf
+    lo_p[srow] = wi * li + wf * l;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    float ov[32];
+    if (have_o) {
+      tmem_ld_32x32b_x32(o_row + c0, ov);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ov[e] = 0.f;
+    }
+    if (row_out) {
+      const float4* src = reinterpret_cast<const float4*>(oi_p + srow * D + c0);
+      float4* dst = reinterpret_cast<float4*>(oo_p + srow * D + c0);
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) {
+        const float4 v = has_init ? src[qq] : make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[qq] = make_float4(wi * v.x + wf * ov[4 * qq], wi * v.y + wf * ov[4 * qq + 1],
+                              wi * v.z + wf * ov[4 * qq + 2], wi * v.w + wf * ov[4 * qq + 3]);
+      }
+    }
+  }
 }
 
 template <int D, int MODE>
@@ -223,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = RowsCfg<D>;
   constexpr int TB = C::TB;
   constexpr int NST = C::kStages;
+  // modes with a pre state: phase 2 starts from an empty accumulator
+  constexpr bool kPre = MODE == kRowsStatePre || MODE == kRowsAdvOld || MODE == kRowsAdvNew;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -256,9 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Units and their cost (K/V pages) per sequence, then their prefix sums (warp 0).
   for (int i = threadIdx.x; i < nseq; i += kThreads) {
-    const RowsSeq s = rows_seq(bt, b_begin + i, MODE);
+    const RowsSeq s = rows_seq(a, b_begin + i, MODE);
     if (!s.sm.ok) report_error(bt.err, kErrBadShape);
-    const long long units = s.nk > 0 ? static_cast<long long>(H) * ((s.nq + 1) / 2) : 0;
+    const long long units = s.nk > 0 && s.nq > 0 ? static_cast<long long>(H) * ((s.nq + 1) / 2) : 0;
     S.cu_units[i + 1] = units;
     S.cu_cost[i + 1] = units * s.nk;
   }
@@ -306,13 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   RWalk w0;
   w0.u = first_unit_at(S, nseq, c * W / G);
   w0.u1 = first_unit_at(S, nseq, (c + 1) * W / G);
-  if (w0.u < w0.u1) w0.seek(S, bt, MODE, b_begin, nseq, H);
+  if (w0.u < w0.u1) w0.seek(S, a, MODE, b_begin, nseq, H);
 
   if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int nkv = 0, nq = 0;
-      for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+      for (RWalk w = w0; w.valid(); w.next(S, a, MODE, b_begin, nseq, H)) {
         if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
         const int gb = b_begin + w.b;
         const int T = w.has1() ? 2 : 1;
@@ -343,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < w.s.nk; ++i, ++nkv) {
           const int st = nkv % NST;
           if (nkv >= NST) wait_or_abort(S, &S.kvempty[st], (nkv / NST - 1) & 1, bt.err);
-          const int y = (page_of(bt, gb, key_page(w.s, MODE, i)) * H + w.h) * kPage;
+          const int y = (page_of(bt, gb, key_page(w.s, i)) * H + w.h) * kPage;
           uint8_t* kt = kv_ring + st * C::KVB;
           mbar_arrive_expect_tx(&S.kvfull[st], C::KVB);
 #pragma unroll
@@ -378,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nkv = 0, nq = 0, ns = 0, npv = 0, no = 0;  // stages, units, S buffers, P V, units of tile t
       const uint32_t qa = smem_u32(q_tiles + t * C::QB), ring0 = smem_u32(kv_ring);
       const uint32_t pa = smem_u32(p_tiles + t * C::PB);
-      for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+      for (RWalk w = w0; w.valid(); w.next(S, a, MODE, b_begin, nseq, H)) {
         const bool mine = t == 0 || w.has1();
         const int nk = w.s.nk;
         wait_or_abort(S, &S.qfull, nq & 1, bt.err);
@@ -394,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + t * D, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+                        ((i > 0 && !(kPre && i == w.s.n1)) || kk > 0) ? 1u : 0u);
             umma_commit(&S.pfree[t]);
             ++npv;
             if (i == nk - 1) {
@@ -438,26 +503,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2, wq = warp & 3;  // query tile, warp of the tile (= TMEM lane quadrant)
     const int r = wq * 32 + lane;            // query row of the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t o_row = lane_base + t * D;  // this thread's row of O_t
     uint8_t* p_own = p_tiles + t * C::PB;
     int ns = 0, pw = 0, no = 0;  // S buffers read, P tiles written, units finished
-    for (RWalk w = w0; w.valid(); w.next(S, bt, MODE, b_begin, nseq, H)) {
+    for (RWalk w = w0; w.valid(); w.next(S, a, MODE, b_begin, nseq, H)) {
       if (t == 1 && !w.has1()) continue;
+      const RowsSeq& q = w.s;
       const int gb = b_begin + w.b;
-      const int nb = w.s.sm.nb, sb = w.s.sm.sb, ce = w.s.sm.sb + w.s.sm.bb;
       const int tq = w.tile(t);
-      // the position of this thread's query row, and whether it is written out
+      // the position of this thread's query row, whether it is written out, and its slot
+      // in the pools
       int pos;
       bool row_out;
       if (MODE == kRowsBlock) {
         const int i = 128 * tq + r;
-        pos = sb + i;
-        row_out = i < w.s.sm.bb;
+        pos = q.sm.sb + i;
+        row_out = i < q.sm.bb;
       } else {
         pos = 128 * tq + r;
-        row_out = pos < nb && (pos < sb || pos >= ce);
+        row_out = (pos >= q.r0 && pos < q.r1) || (pos >= q.r2 && pos < q.r3);
       }
+      size_t srow = 0;
+      if (MODE != kRowsBlock && row_out)
+        srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
       float m_ref = neg_inf(), m_true = neg_inf(), l = 0.f;
-      for (int i = 0; i < w.s.nk; ++i) {
+      if (kPre && q.n1 == 0)  // no phase 1: the pre state is the one read in (or empty)
+        store_state<D>(o_row, false, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pre,
+                       a.l_pre, a.o_pre, srow, row_out);
+      for (int i = 0; i < q.nk; ++i) {
         const int bsel = ns & 1;
         wait_or_abort(S, &S.sfull[t][bsel], (ns >> 1) & 1, bt.err);
         tc_fence_after();
@@ -467,21 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.sfree[t][bsel]);
         ++ns;
-        // this row's page max over the keys of this mode's key set (raw scores: the scale is
+        // this row's page max over the keys of the page's phase (raw scores: the scale is
         // positive, so it is applied to the max and folded into the exponent below); a page
-        // whose keys all belong to the set takes the unmasked path (uniform per page)
-        const int key0 = key_page(w.s, MODE, i) * kPage;
-        bool all_valid;
-        if (MODE == kRowsState)
-          all_valid = key0 + kPage <= nb && (key0 + kPage <= sb || key0 >= ce);
-        else if (MODE == kRowsMerge)
-          all_valid = key0 >= sb && key0 + kPage <= ce;
-        else
-          all_valid = key0 + kPage <= nb;
-        if (!all_valid) {
+        // whose keys all belong to the phase takes the unmasked path (uniform per page)
+        const bool ph2 = i >= q.n1;
+        const int key0 = key_page(q, i) * kPage;
+        const int klo = ph2 ? q.k2 : q.k0, khi = ph2 ? q.k3 : q.k1;
+        if (!(key0 >= klo && key0 + kPage <= khi)) {
 #pragma unroll
           for (int cc = 0; cc < 64; ++cc)
-            if (!key_valid<MODE>(key0 + cc, nb, sb, ce)) sc[cc] = neg_inf();
+            if (key0 + cc < klo || key0 + cc >= khi) sc[cc] = neg_inf();
         }
         float mx8[8];
 #pragma unroll
@@ -490,10 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 8; cc < 64; ++cc) mx8[cc & 7] = fmaxf(mx8[cc & 7], sc[cc]);
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * a.scale_log2;
+        // pre modes: phase 2 starts from an empty accumulator; phase 1's state is kept for
+        // the pre pools
+        const bool snap = kPre && i == q.n1 && i > 0;
+        const float s_mref = m_ref, s_mtrue = m_true, s_l = l;
+        if (snap) {
+          m_true = neg_inf();
+          l = 0.f;
+        }
         m_true = fmaxf(m_true, mx);
-        // a new reference max (the unit's first page, or a rise beyond the threshold)
+        // a new reference max (the accumulator's first page, or a rise beyond the threshold)
         float factor = 1.f;
-        if (i == 0) {
+        if (i == 0 || snap) {
           m_ref = mx;
         } else if (mx > m_ref + kRescale) {
           factor = fast_exp2(m_ref - mx);
@@ -511,14 +587,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // earlier page (rescaled here when the reference max rose)
         if (pw >= 1) wait_or_abort(S, &S.pfree[t], (pw - 1) & 1, bt.err);
         tc_fence_after();
+        if (snap)  // O_t holds phase 1: the pre state, before this page's P V overwrites O_t
+          store_state<D>(o_row, true, s_mref, s_mtrue, s_l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre,
+                         a.m_pre, a.l_pre, a.o_pre, srow, row_out);
         if (__any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             float ov[32];
-            tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
+            tmem_ld_32x32b_x32(o_row + c0, ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] *= factor;
-            tmem_st_32x32b_x32(lane_base + t * D + c0, ov);
+            tmem_st_32x32b_x32(o_row + c0, ov);
           }
           tmem_st_wait();
         }
@@ -542,32 +621,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_or_abort(S, &S.ofull[t], no & 1, bt.err);
       tc_fence_after();
       if (MODE == kRowsState) {
-        // state relative to the exact max over the row's keys of U
-        size_t srow = 0;
-        float corr = 0.f;
-        if (row_out) {
-          srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
-          corr = fast_exp2(m_ref - m_true);
-          a.m_pool[srow] = m_true * kLn2;  // natural units
-          a.l_pool[srow] = l * corr;
-        }
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float ov[32];
-          tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
-          if (row_out) {
-            float4* dst = reinterpret_cast<float4*>(a.o_pool + srow * D + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(ov[4 * q] * corr, ov[4 * q + 1] * corr, ov[4 * q + 2] * corr, ov[4 * q + 3] * corr);
-          }
+        store_state<D>(o_row, true, m_ref, m_true, l, false, nullptr, nullptr, nullptr, a.m_pool, a.l_pool, a.o_pool,
+                       srow, row_out);
+      } else if (kPre) {
+        if (q.n2 == 0) {  // phase 1 only: the state over U is the pre state (read in first)
+          store_state<D>(o_row, true, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pool,
+                         a.l_pool, a.o_pool, srow, row_out);
+          store_state<D>(o_row, true, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pre,
+                         a.l_pre, a.o_pre, srow, row_out);
+        } else {  // the pre state written above, merged with phase 2's
+          store_state<D>(o_row, true, m_ref, m_true, l, true, a.m_pre, a.l_pre, a.o_pre, a.m_pool, a.l_pool,
+                         a.o_pool, srow, row_out);
         }
       } else {
         // O = (w_c O~_c + w_f O_t) / L with the cached state (merge) or O_t / l (block rows)
         float wc = 0.f, wf = 1.f, M = m_ref, L = l;
-        size_t srow = 0;
         if (MODE == kRowsMerge && row_out) {
-          srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
           const float mc = __ldg(a.m_pool + srow) * 1.4426950408889634f;  // base-2 units
           const float lc = __ldg(a.l_pool + srow);
           M = fmaxf(mc, m_ref);
@@ -578,22 +647,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = row_out ? 1.f / L : 0.f;
         wc *= inv;
         wf *= inv;
-        const size_t orow = static_cast<size_t>(w.s.sm.cus + pos) * H + w.h;
+        const size_t orow = static_cast<size_t>(q.sm.cus + pos) * H + w.h;
         __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           float ov[32];
-          tmem_ld_32x32b_x32(lane_base + t * D + c0, ov);
+          tmem_ld_32x32b_x32(o_row + c0, ov);
           if (row_out) {
             if (MODE == kRowsMerge) {
               const float4* oc = reinterpret_cast<const float4*>(a.o_pool + srow * D + c0);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                const float4 v = __ldg(oc + q);
-                ov[4 * q] = wc * v.x + wf * ov[4 * q];
-                ov[4 * q + 1] = wc * v.y + wf * ov[4 * q + 1];
-                ov[4 * q + 2] = wc * v.z + wf * ov[4 * q + 2];
-                ov[4 * q + 3] = wc * v.w + wf * ov[4 * q + 3];
+              for (int qq = 0; qq < 8; ++qq) {
+                const float4 v = __ldg(oc + qq);
+                ov[4 * qq] = wc * v.x + wf * ov[4 * qq];
+                ov[4 * qq + 1] = wc * v.y + wf * ov[4 * qq + 1];
+                ov[4 * qq + 2] = wc * v.z + wf * ov[4 * qq + 2];
+                ov[4 * qq + 3] = wc * v.w + wf * ov[4 * qq + 3];
               }
             } else {
 #pragma unroll
@@ -601,13 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint4* dst = reinterpret_cast<uint4*>(of + orow * D + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int qq = 0; qq < 4; ++qq) {
               uint4 u;
-              u.x = pack_bf16x2(ov[8 * q], ov[8 * q + 1]);
-              u.y = pack_bf16x2(ov[8 * q + 2], ov[8 * q + 3]);
-              u.z = pack_bf16x2(ov[8 * q + 4], ov[8 * q + 5]);
-              u.w = pack_bf16x2(ov[8 * q + 6], ov[8 * q + 7]);
-              dst[q] = u;
+              u.x = pack_bf16x2(ov[8 * qq], ov[8 * qq + 1]);
+              u.y = pack_bf16x2(ov[8 * qq + 2], ov[8 * qq + 3]);
+              u.z = pack_bf16x2(ov[8 * qq + 4], ov[8 * qq + 5]);
+              u.w = pack_bf16x2(ov[8 * qq + 6], ov[8 * qq + 7]);
+              dst[qq] = u;
             }
           }
         }
@@ -657,9 +726,20 @@ cudaError_t launch_rows_dm(const AttnArgs& a, int num_sms, cudaStream_t stream) 
 
 template <int D>
 cudaError_t launch_rows_d(const AttnArgs& a, int mode, int num_sms, cudaStream_t stream) {
-  if (mode == kRowsState) return launch_rows_dm<D, kRowsState>(a, num_sms, stream);
-  if (mode == kRowsBlock) return launch_rows_dm<D, kRowsBlock>(a, num_sms, stream);
-  return launch_rows_dm<D, kRowsMerge>(a, num_sms, stream);
+  switch (mode) {
+    case kRowsState:
+      return launch_rows_dm<D, kRowsState>(a, num_sms, stream);
+    case kRowsBlock:
+      return launch_rows_dm<D, kRowsBlock>(a, num_sms, stream);
+    case kRowsMerge:
+      return launch_rows_dm<D, kRowsMerge>(a, num_sms, stream);
+    case kRowsStatePre:
+      return launch_rows_dm<D, kRowsStatePre>(a, num_sms, stream);
+    case kRowsAdvOld:
+      return launch_rows_dm<D, kRowsAdvOld>(a, num_sms, stream);
+    default:
+      return launch_rows_dm<D, kRowsAdvNew>(a, num_sms, stream);
+  }
 }
 
 }  // namespace

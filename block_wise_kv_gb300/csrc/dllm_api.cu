@@ -60,6 +60,13 @@ dllm_status check_cache(const dllm_cache* c, const dllm_layer_desc* d, bool need
   return DLLM_OK;
 }
 
+// The prefix state pools: all unset (0), all set and aligned (1), else invalid (-1).
+int pre_pools(const dllm_cache* c) {
+  if (c->m_pre == nullptr && c->l_pre == nullptr && c->o_pre == nullptr) return 0;
+  if (!aligned(c->m_pre, 16) || !aligned(c->l_pre, 16) || !aligned(c->o_pre, 16)) return -1;
+  return 1;
+}
+
 int device_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -105,6 +112,10 @@ AttnArgs attn_args(const dllm_layer_desc* d, const dllm_batch* b, const dllm_cac
   a.n_heads = d->n_heads;
   a.head_dim = d->head_dim;
   a.scale_log2 = softmax_scale(d) * 1.4426950408889634f;
+  a.m_pre = nullptr;
+  a.l_pre = nullptr;
+  a.o_pre = nullptr;
+  a.prev_start = nullptr;
   return a;
 }
 
@@ -200,6 +211,12 @@ dllm_status dllm_workspace_size(const dllm_layer_desc* desc, const dllm_batch* b
     case DLLM_OP_STATE_MERGE:
       *bytes = 0;
       return DLLM_OK;
+    case DLLM_OP_CACHE_ADVANCE:  // `batch` is the decoded blocks': the projection of their rows
+      *bytes = batch->batch > 0 && batch->total_block_rows > 0
+                   ? qkv_plan(batch->total_block_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms())
+                         .total_bytes
+                   : 0;
+      return DLLM_OK;
     default:
       return DLLM_ERR_INVALID_ARGUMENT;
   }
@@ -239,6 +256,8 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   DLLM_TRY(check_batch(batch));
   if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
   DLLM_TRY(check_cache(cache, desc, true, true));
+  const int pre = pre_pools(cache);
+  if (pre < 0) return DLLM_ERR_INVALID_ARGUMENT;
   if (!aligned(x_full, 16) || !aligned(rms_gain, 16) || !aligned(w_packed, 16) || !aligned(rope_table, 8))
     return DLLM_ERR_INVALID_ARGUMENT;
   if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
@@ -256,8 +275,59 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
   bind_workspace(&qa, plan, ws);
   DLLM_CUDA_TRY(launch_zero_tails(bt, cache->k_pool, cache->v_pool, cache->q_pool, desc->n_heads, desc->head_dim, s));
   DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, qa, plan, s));
-  const AttnArgs aa = attn_args(desc, batch, cache);
-  DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsState, device_sms(), s));
+  AttnArgs aa = attn_args(desc, batch, cache);
+  if (pre) {
+    aa.m_pre = cache->m_pre;
+    aa.l_pre = cache->l_pre;
+    aa.o_pre = cache->o_pre;
+  }
+  DLLM_CUDA_TRY(launch_rows_attention(aa, pre ? kRowsStatePre : kRowsState, device_sms(), s));
+  return DLLM_OK;
+}
+
+dllm_status dllm_cache_advance(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_batch* decoded,
+                               const void* x_decoded, const void* rms_gain, const void* w_packed,
+                               const float* rope_table, int32_t rope_max_pos, const dllm_cache* cache, void* ws,
+                               size_t ws_bytes, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  DLLM_TRY(check_batch(decoded));
+  // the decoded blocks describe the same sequences, through the same metadata
+  if (decoded->batch != batch->batch || decoded->block_table != batch->block_table ||
+      decoded->seq_len != batch->seq_len || decoded->cu_seq != batch->cu_seq ||
+      decoded->max_pages_per_seq != batch->max_pages_per_seq || decoded->total_seq_rows != batch->total_seq_rows ||
+      decoded->max_seq_len != batch->max_seq_len)
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (batch->batch == 0 || batch->total_seq_rows == 0) return DLLM_OK;
+  DLLM_TRY(check_cache(cache, desc, true, true));
+  if (pre_pools(cache) != 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (!aligned(x_decoded, 16) || !aligned(rms_gain, 16) || !aligned(w_packed, 16) || !aligned(rope_table, 8))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (rope_max_pos < batch->max_seq_len) return DLLM_ERR_INVALID_ARGUMENT;
+  size_t need = 0;
+  DLLM_TRY(dllm_workspace_size(desc, decoded, DLLM_OP_CACHE_ADVANCE, &need));
+  if (ws_bytes < need) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // the decoded rows: q, k, v into the pools
+  if (decoded->total_block_rows > 0) {
+    const QkvPlan plan =
+        qkv_plan(decoded->total_block_rows, desc->d_model, desc->n_heads, desc->head_dim, device_sms());
+    QkvArgs qa = qkv_args(desc, decoded, cache, rope_table, rope_max_pos, kModeRows, decoded->total_block_rows);
+    qa.x = x_decoded;
+    qa.gain = rms_gain;
+    bind_workspace(&qa, plan, ws);
+    DLLM_CUDA_TRY(launch_qkv_gemm(w_packed, qa, plan, s));
+  }
+  // the prefix state extended (rows kept) or rebuilt (decoded rows), then the state over U
+  AttnArgs aa = attn_args(desc, batch, cache);
+  aa.m_pre = cache->m_pre;
+  aa.l_pre = cache->l_pre;
+  aa.o_pre = cache->o_pre;
+  aa.prev_start = decoded->block_start;
+  DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsAdvOld, device_sms(), s));
+  DLLM_CUDA_TRY(launch_rows_attention(aa, kRowsAdvNew, device_sms(), s));
   return DLLM_OK;
 }
 

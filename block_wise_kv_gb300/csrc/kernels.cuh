@@ -42,7 +42,7 @@ struct QkvArgs {
   int32_t head_dim;
   int32_t d_model;
   int32_t n_tok;               // rows of x
-  int32_t mode;                // kModeBlock or kModeBoundary
+  int32_t mode;                // kModeBlock, kModeBoundary or kModeRows
   // RMSNorm: input rows, gain, epsilon; in the workspace the normalised rows
   // x^, the per-row scale pairs and the counters of the row claims (claimed,
   // published, CTAs done)
@@ -94,6 +94,8 @@ void qkv_wide_schedule(int n_tok, int d_model, int n_heads, int head_dim, int nu
 cudaError_t launch_qkv_wide(const void* w_packed, const QkvArgs& a, const QkvPlan& plan, cudaStream_t stream);
 constexpr int kModeBlock = 0;     // tokens are the packed block rows (cu_block)
 constexpr int kModeBoundary = 1;  // tokens are all rows of every sequence (cu_seq)
+constexpr int kModeRows = 2;      // tokens are the rows [block_start, block_start + block_len) of each
+                                  // sequence (cu_block), q written to q_pool like k and v
 
 struct AttnArgs {
   BatchArgs bt;
@@ -109,6 +111,13 @@ struct AttnArgs {
   int32_t n_heads;
   int32_t head_dim;
   float scale_log2;     // softmax_scale * log2(e)
+  // incremental boundary: the state of every row over the keys before its sequence's
+  // current block (same layout as m_pool, l_pool, o_pool), and where the block decoded
+  // last began (device int32 [batch]; the new block starts where it ended)
+  float* m_pre;
+  float* l_pre;
+  float* o_pre;
+  const int32_t* prev_start;
 };
 
 // One attention launch: a persistent grid of block-role and merge-role CTAs,
@@ -134,9 +143,17 @@ cudaError_t launch_step_attention(const AttnArgs& a, const AttnPlan& plan, cudaS
 //   kRowsState  every row of U over the keys of U: (m, l, O~) into the pools (the cache build)
 //   kRowsBlock  the block rows over every key: O and L (blocks of more than 64 rows)
 //   kRowsMerge  every row of U over the block keys, merged with its cached state: O and L
+//   kRowsStatePre  as kRowsState, and the state over the keys before the block into the pre pools
+//   kRowsAdvOld    incremental boundary, rows kept from the last one: pre extended by the decoded
+//                  block's keys, then the state over U from it and the suffix keys
+//   kRowsAdvNew    incremental boundary, the decoded rows: pre over the keys before the new
+//                  block, then the state over U from it and the suffix keys
 constexpr int kRowsState = 0;
 constexpr int kRowsBlock = 1;
 constexpr int kRowsMerge = 2;
+constexpr int kRowsStatePre = 3;
+constexpr int kRowsAdvOld = 4;
+constexpr int kRowsAdvNew = 5;
 cudaError_t launch_rows_attention(const AttnArgs& a, int mode, int num_sms, cudaStream_t stream);
 
 }  // namespace dllm

@@ -438,13 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pos = 0;
       const int j = nt * BN + c;
       if (j < a.n_tok) {
-        const int32_t* cu = a.mode == kModeBlock ? bt.cu_block : bt.cu_seq;
+        const int32_t* cu = a.mode == kModeBoundary ? bt.cu_seq : bt.cu_block;
         const int b = find_seq(cu, bt.batch, j);
         const int off = j - __ldg(cu + b);
         const int nb = __ldg(bt.seq_len + b), sb = __ldg(bt.block_start + b), lb = __ldg(bt.block_len + b);
-        pos = a.mode == kModeBlock ? sb + off : off;
+        pos = a.mode == kModeBoundary ? off : sb + off;
         const bool shape_ok = nb >= 1 && nb <= bt.max_seq_len && lb >= 1 && lb <= bt.max_block_len && sb >= 0 &&
-                              sb + lb <= nb && (a.mode == kModeBlock ? off < lb : off < nb) && pos >= 0 &&
+                              sb + lb <= nb && (a.mode == kModeBoundary ? off < nb : off < lb) && pos >= 0 &&
                               pos < nb && pos < a.rope_max_pos && pos / kPage < bt.max_pages;
         if (!shape_ok) {
           report_error(bt.err, kErrBadShape);
@@ -456,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             kv = (static_cast<long long>(pg) * H * kPage + (pos % kPage)) * d;
             if (a.mode == kModeBlock)
               qd = static_cast<long long>(j) * H * d;
-            else if (pos < sb || pos >= sb + lb)
-              qd = kv;  // queries are cached for the invariant rows only
+            else if (a.mode == kModeRows || pos < sb || pos >= sb + lb)
+              qd = kv;  // queries are cached for the invariant rows (and the rows of a range) only
           }
         }
       }

@@ -169,7 +169,7 @@ __device__ __forceinline__ void resolve_columns(const QkvArgs& a, int tt, int at
   int pos = 0;
   const int j = tt * kTN + at;
   if (j < a.n_tok) {
-    const int32_t* cu = a.mode == kModeBlock ? bt.cu_block : bt.cu_seq;
+    const int32_t* cu = a.mode == kModeBoundary ? bt.cu_seq : bt.cu_block;
     int lo = 0, hi = bt.batch - 1;  // the sequence of token j: the largest b with cu[b] <= j
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -181,9 +181,9 @@ __device__ __forceinline__ void resolve_columns(const QkvArgs& a, int tt, int at
     const int b = lo;
     const int off = j - __ldg(cu + b);
     const int nb = __ldg(bt.seq_len + b), sb = __ldg(bt.block_start + b), lb = __ldg(bt.block_len + b);
-    pos = a.mode == kModeBlock ? sb + off : off;
+    pos = a.mode == kModeBoundary ? off : sb + off;
     const bool shape_ok = nb >= 1 && nb <= bt.max_seq_len && lb >= 1 && lb <= bt.max_block_len && sb >= 0 &&
-                          sb + lb <= nb && (a.mode == kModeBlock ? off < lb : off < nb) && pos >= 0 && pos < nb &&
+                          sb + lb <= nb && (a.mode == kModeBoundary ? off < nb : off < lb) && pos >= 0 && pos < nb &&
                           pos < a.rope_max_pos && pos / kPage < bt.max_pages;
     if (!shape_ok) {
       report_error(bt.err, kErrBadShape);
@@ -195,8 +195,8 @@ __device__ __forceinline__ void resolve_columns(const QkvArgs& a, int tt, int at
         kv = (static_cast<long long>(pg) * H * kPage + (pos % kPage)) * d;
         if (a.mode == kModeBlock)
           qd = static_cast<long long>(j) * H * d;
-        else if (pos < sb || pos >= sb + lb)
-          qd = kv;  // queries are cached for the invariant rows only
+        else if (a.mode == kModeRows || pos < sb || pos >= sb + lb)
+          qd = kv;  // queries are cached for the invariant rows (and the rows of a range) only
       }
     }
   }

@@ -38,12 +38,13 @@ DLLM_OP_BLOCK_QKV_ROPE_WRITE = 1
 DLLM_OP_BLOCK_ATTENTION = 2
 DLLM_OP_STATE_MERGE = 3
 DLLM_OP_STEP_ATTENTION = 4
+DLLM_OP_CACHE_ADVANCE = 5
 
 PAGE = 64
 
 # Every symbol include/dllm.h declares.
 EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_qkv_weight_packed_bytes", "dllm_qkv_weight_pack",
-           "dllm_cache_build", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
+           "dllm_cache_build", "dllm_cache_advance", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
            "dllm_block_attention", "dllm_state_merge", "dllm_step_attention", "dllm_status_string")
 
 
@@ -62,7 +63,8 @@ class LayerDescC(ctypes.Structure):
 class CacheC(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("q_pool", ctypes.c_void_p),
                 ("m_pool", ctypes.c_void_p), ("l_pool", ctypes.c_void_p), ("o_pool", ctypes.c_void_p),
-                ("num_pages", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32),
+                ("m_pre", ctypes.c_void_p), ("l_pre", ctypes.c_void_p), ("o_pre", ctypes.c_void_p)]
 
 
 class BatchC(ctypes.Structure):
@@ -96,6 +98,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                 "dllm_qkv_weight_packed_bytes": [P(LayerDescC), P(sz)],
                 "dllm_qkv_weight_pack": [P(LayerDescC), vp, vp, vp],
                 "dllm_cache_build": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, sz, vp],
+                "dllm_cache_advance": [P(LayerDescC), P(BatchC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, sz,
+                                       vp],
                 "dllm_block_qkv_rope_write": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp, vp, sz,
                                               vp],
                 "dllm_block_qkv_rope_write_noalloc": [P(LayerDescC), P(BatchC), vp, vp, vp, vp, i32, P(CacheC), vp,
@@ -182,6 +186,14 @@ def dllm_cache_build(desc, batch, x_full, rms_gain, w_packed, rope_table, rope_m
         int(rope_max_pos), ctypes.byref(cache), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
+def dllm_cache_advance(desc, batch, decoded, x_decoded, rms_gain, w_packed, rope_table, rope_max_pos, cache, ws,
+                       stream=None):
+    _check("dllm_cache_advance", load().dllm_cache_advance(
+        ctypes.byref(desc), ctypes.byref(batch), ctypes.byref(decoded), _ptr(x_decoded), _ptr(rms_gain),
+        _ptr(w_packed), _ptr(rope_table), int(rope_max_pos), ctypes.byref(cache), _ptr(ws), _nbytes(ws),
+        _stream(stream)))
+
+
 def dllm_block_qkv_rope_write(desc, batch, x_block, rms_gain, w_packed, rope_table, rope_max_pos, cache, q_block,
                               ws, stream=None):
     _check("dllm_block_qkv_rope_write", load().dllm_block_qkv_rope_write(
@@ -249,12 +261,38 @@ class BatchLayout:
     def error_bits(self) -> int:
         return 0 if self.error is None else int(self.error.item())
 
+    def with_blocks(self, block_start, block_len) -> "BlockRange":
+        """The same sequences with other block ranges (for dllm_cache_advance's
+        decoded blocks): the struct shares this layout's block table, seq_len,
+        cu_seq and error flag."""
+        return BlockRange(self, block_start, block_len)
+
+
+class BlockRange:
+    """A dllm_batch that shares a BatchLayout's sequences and points at its own
+    block_start / block_len / cu_block."""
+
+    def __init__(self, base: BatchLayout, block_start, block_len):
+        bs = np.asarray(block_start, np.int32)
+        bl = np.asarray(block_len, np.int32)
+        cu = np.concatenate([[0], np.cumsum(bl)]).astype(np.int32)
+        dev = base.dev["seq_len"].device
+        self.host = dict(block_start=bs, block_len=bl, cu_block=cu)
+        self.dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in self.host.items()}
+        self.total_block_rows = int(cu[-1])
+        self.max_block_len = int(bl.max()) if bl.size else 1
+        d, bd = self.dev, base.dev
+        self.c = BatchC(base.batch, base.max_pages, self.total_block_rows, base.total_seq_rows, self.max_block_len,
+                        base.max_seq_len, _ptr(bd["block_table"]), _ptr(bd["seq_len"]), _ptr(d["block_start"]),
+                        _ptr(d["block_len"]), _ptr(d["cu_block"]), _ptr(bd["cu_seq"]), _ptr(base.error))
+
 
 class PagedCache:
     """The paged pools of one layer, allocated by torch (zero-filled, or
     filled with `fill` to act as a sentinel)."""
 
-    def __init__(self, num_pages: int, n_heads: int, head_dim: int, device="cuda", fill: float | None = None):
+    def __init__(self, num_pages: int, n_heads: int, head_dim: int, device="cuda", fill: float | None = None,
+                 pre: bool = False):
         shp = (num_pages, n_heads, PAGE, head_dim)
 
         def mk(shape, dtype):
@@ -270,8 +308,12 @@ class PagedCache:
         self.l = mk(shp[:3], torch.float32)
         self.o = mk(shp, torch.float32)
         self.num_pages = num_pages
+        # the prefix state (for incremental boundaries), when asked for
+        self.m_pre = mk(shp[:3], torch.float32) if pre else None
+        self.l_pre = mk(shp[:3], torch.float32) if pre else None
+        self.o_pre = mk(shp, torch.float32) if pre else None
         self.c = CacheC(_ptr(self.k), _ptr(self.v), _ptr(self.q), _ptr(self.m), _ptr(self.l), _ptr(self.o),
-                        num_pages)
+                        num_pages, _ptr(self.m_pre), _ptr(self.l_pre), _ptr(self.o_pre))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

@@ -19,7 +19,7 @@ class LayerStep:
     for the batch layout of `cfg` (block k_b of each sequence)."""
 
     def __init__(self, cfg: Config, layer: int = 0, blocks=None, device: str = "cuda", cache_fill=None,
-                 weights=None, rope_max_pos: int | None = None):
+                 weights=None, rope_max_pos: int | None = None, pre: bool = False):
         self.cfg = cfg
         self.device = device
         wl = Workload(cfg)
@@ -35,24 +35,54 @@ class LayerStep:
         self.rope_max_pos = int(rope_max_pos or self.batch.max_seq_len)
         self.rope = torch.empty(self.rope_max_pos, cfg.head_dim // 2, 2, dtype=torch.float32, device=device)
         dllm.dllm_rope_table_build(self.desc, self.rope_max_pos, self.rope)
-        self.cache = dllm.PagedCache(lay["num_pages"], cfg.n_heads, cfg.head_dim, device=device, fill=cache_fill)
+        self.cache = dllm.PagedCache(lay["num_pages"], cfg.n_heads, cfg.head_dim, device=device, fill=cache_fill,
+                                     pre=pre)
         self.ws_build = dllm.workspace(dllm.dllm_workspace_size(self.desc, self.batch.c, dllm.DLLM_OP_CACHE_BUILD),
                                        device)
+        self._block_buffers()
+        H, d = cfg.n_heads, cfg.head_dim
+        self.o_full = torch.zeros(self.batch.total_seq_rows, H, d, dtype=torch.bfloat16, device=device)
+        self.lse = torch.zeros(self.batch.total_seq_rows, H, dtype=torch.float32, device=device)
+
+    def _block_buffers(self) -> None:
+        """q_block and the step workspaces, sized for the current blocks."""
+        cfg, device = self.cfg, self.device
         self.ws_step = dllm.workspace(
             dllm.dllm_workspace_size(self.desc, self.batch.c, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE), device)
         # the attention calls of a step run in order, so one workspace serves all three
         self.ws_attn = dllm.workspace(max(
             dllm.dllm_workspace_size(self.desc, self.batch.c, op)
             for op in (dllm.DLLM_OP_BLOCK_ATTENTION, dllm.DLLM_OP_STATE_MERGE, dllm.DLLM_OP_STEP_ATTENTION)), device)
-        H, d = cfg.n_heads, cfg.head_dim
-        self.q_block = torch.zeros(self.batch.total_block_rows, H, d, dtype=torch.bfloat16, device=device)
-        self.o_full = torch.zeros(self.batch.total_seq_rows, H, d, dtype=torch.bfloat16, device=device)
-        self.lse = torch.zeros(self.batch.total_seq_rows, H, dtype=torch.float32, device=device)
+        self.q_block = torch.zeros(self.batch.total_block_rows, cfg.n_heads, cfg.head_dim, dtype=torch.bfloat16,
+                                   device=device)
 
     # ------------------------------------------------------------ the calls
     def boundary(self, x_full: torch.Tensor, stream=None) -> None:
         dllm.dllm_cache_build(self.desc, self.batch.c, x_full, self.gain, self.w_qkv, self.rope, self.rope_max_pos,
                               self.cache.c, self.ws_build, stream)
+
+    def advance(self, blocks, x_decoded: torch.Tensor, stream=None) -> None:
+        """Incremental boundary to the blocks `blocks` (one block index per
+        sequence, each starting where the current block ends): the current
+        blocks are the decoded ones, x_decoded their final rows.  Needs the
+        prefix state pools (pre=True) and a cache built by boundary() and
+        advance() calls only."""
+        old = self.batch.host
+        lay = layout(self.cfg, blocks)
+        dec_start = old["block_start"]
+        dec_len = lay["block_start"] - dec_start
+        if (dec_len <= 0).any():
+            raise ValueError("each new block must start after the current one's start")
+        new = dllm.BatchLayout(lay["block_table"], lay["seq_len"], lay["block_start"], lay["block_len"],
+                               device=self.device)
+        dec = new.with_blocks(dec_start, dec_len)
+        ws = dllm.workspace(dllm.dllm_workspace_size(self.desc, dec.c, dllm.DLLM_OP_CACHE_ADVANCE), self.device)
+        dllm.dllm_cache_advance(self.desc, new.c, dec.c, x_decoded, self.gain, self.w_qkv, self.rope,
+                                self.rope_max_pos, self.cache.c, ws, stream)
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+        self._advanced = (new, dec, ws)  # alive until the next advance
+        self.batch, self.host_layout = new, lay
+        self._block_buffers()
 
     def qkv(self, x_block: torch.Tensor, stream=None) -> None:
         dllm.dllm_block_qkv_rope_write(self.desc, self.batch.c, x_block, self.gain, self.w_qkv, self.rope,

@@ -129,6 +129,13 @@ typedef struct dllm_cache {
   float* l_pool;     /* fp32 [num_pages][H][64]: cached sum of exp(S - m) over U keys */
   float* o_pool;     /* fp32 [num_pages][H][64][d]: cached unnormalised sum of exp(S - m) v over U keys */
   int32_t num_pages; /* pages in each pool; num_pages*H*64 < 2^31 */
+  /* Optional (all NULL, or all set): the prefix state of each row, the same
+   * (m, l, O~) over only the keys before its sequence's current block, in the
+   * layouts of m_pool, l_pool, o_pool.  dllm_cache_build fills it when set;
+   * dllm_cache_advance needs it. */
+  float* m_pre;
+  float* l_pre;
+  float* o_pre;
 } dllm_cache;
 
 /* A ragged batch.  Host scalars bound the device arrays and size the grids. */
@@ -154,6 +161,7 @@ typedef struct dllm_batch {
 #define DLLM_OP_BLOCK_ATTENTION 2
 #define DLLM_OP_STATE_MERGE 3
 #define DLLM_OP_STEP_ATTENTION 4
+#define DLLM_OP_CACHE_ADVANCE 5 /* pass the decoded blocks' dllm_batch */
 
 /* Bytes of device workspace `op` needs for this layer and batch (0 if none).
  * The workspace is scratch owned by the caller, 256-byte aligned, and may be
@@ -188,7 +196,9 @@ dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv,
  *   m = max_{j in U} S_rj, l = sum_{j in U} exp(S_rj - m),
  *   O~ = sum_{j in U} exp(S_rj - m) v_j,   S_rj = scale * q_r . k_j,
  * written to m_pool, l_pool, o_pool at row r's slot.  If U_b is empty for a
- * row's keys, m = -inf, l = 0, O~ = 0.
+ * row's keys, m = -inf, l = 0, O~ = 0.  When the cache's prefix state pools
+ * are set, the same state over only the keys [0, s_b) is written there too
+ * (what dllm_cache_advance extends).
  *   x_full: device bf16 [R][d_model]; rms_gain: device bf16 [d_model];
  *   w_packed: device, from dllm_qkv_weight_pack; rope_table: device fp32, rope_max_pos
  *   >= max_seq_len positions; ws: device scratch of
@@ -196,6 +206,37 @@ dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv,
 dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batch, const void* x_full,
                              const void* rms_gain, const void* w_packed, const float* rope_table, int32_t rope_max_pos,
                              const dllm_cache* cache, void* ws, size_t ws_bytes, void* stream);
+
+/* Incremental block boundary: the cache of dllm_cache_build for the next
+ * blocks, when only the just-decoded blocks' rows changed since the last
+ * boundary (the state of every other row is rebuilt from cached pieces, per
+ * KV block: LaCache §3.3.3, the exact merge of partial states; Fast-dLLM
+ * "Block-wise Generation": blocks are decoded left to right, each new block
+ * starting where the decoded one ended).
+ *   batch:   the new blocks (block_start s_b', block_len B_b').
+ *   decoded: the blocks just decoded: the same sequences, block_table,
+ *            seq_len and cu_seq pointers and host bounds as batch, with
+ *            block_start s_b, block_len = s_b' - s_b, cu_block over those
+ *            lengths (0 <= s_b < s_b').
+ *   x_decoded: device bf16 [decoded->total_block_rows][d_model], the final
+ *            rows of the decoded blocks, packed like x_block.
+ *   cache:   written by dllm_cache_build (with the prefix state pools set)
+ *            and any number of dllm_cache_advance calls since; every row
+ *            outside the decoded blocks must be the one the cache was built
+ *            from.
+ * In order: the decoded rows' q, k, v (RMSNorm, projection, RoPE) into the
+ * pools; for every row r of U' = [0, s_b') u [s_b' + B_b', N_b):
+ *   pre'(r)   = pre(r) merged with r's partial state over the decoded keys
+ *               [s_b, s_b') (rows kept from the last boundary), or r's state
+ *               over [0, s_b') (the decoded rows);
+ *   state'(r) = pre'(r) merged with r's partial state over [s_b' + B_b', N_b)
+ * written to m_pre/l_pre/o_pre and m_pool/l_pool/o_pool.  The result equals
+ * dllm_cache_build on the same rows up to the rounding order of the sums.
+ *   ws: dllm_workspace_size(desc, decoded, DLLM_OP_CACHE_ADVANCE) bytes. */
+dllm_status dllm_cache_advance(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_batch* decoded,
+                               const void* x_decoded, const void* rms_gain, const void* w_packed,
+                               const float* rope_table, int32_t rope_max_pos, const dllm_cache* cache, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /* Inner step, part 1 (LaCache §3.3.2 Eq. (1); Flash-dLLM Flash-Cache): for
  * the B_b rows of each current block only, in one kernel: x^ = RMSNorm(x_block)

@@ -138,3 +138,27 @@ def test_status_strings(lib):
     assert dllm.dllm_status_string(dllm.DLLM_OK) == "ok"
     assert "workspace" in dllm.dllm_status_string(dllm.DLLM_ERR_WORKSPACE_TOO_SMALL)
     assert dllm.dllm_status_string(99) == "unknown status"
+
+
+def test_cache_advance_rejects_before_launch(lib):
+    d = _desc()
+    b = _batch()
+    fake = 0x10000
+    no_pre = dllm.CacheC(fake, fake, fake, fake, fake, fake, 24)
+    with_pre = dllm.CacheC(fake, fake, fake, fake, fake, fake, 24, fake, fake, fake)
+    # the decoded blocks must describe the same sequences through the same metadata
+    other = dllm.BatchC(2, 12, 64, 1536, 32, 768, fake + 256, fake, fake, fake, fake, fake, None)
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_cache_advance(d, b, other, fake, fake, fake, fake, 1024, with_pre, fake, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+    # the prefix state pools are required (all three)
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_cache_advance(d, b, b, fake, fake, fake, fake, 1024, no_pre, fake, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+    half = dllm.CacheC(fake, fake, fake, fake, fake, fake, 24, fake, None, fake)
+    with pytest.raises(dllm.DllmError) as e:
+        dllm.dllm_cache_build(d, b, fake, fake, fake, fake, 1024, half, fake, 0)
+    assert e.value.status == dllm.DLLM_ERR_INVALID_ARGUMENT
+    # its workspace is the projection of the decoded rows
+    assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_ADVANCE) == \
+        dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE)
