@@ -410,10 +410,65 @@ def measure(cfg, L, K, W, P, sample_every, dev, rank, ws, extras=True, e2e_steps
     for st, _, _ in items:
         assert st.batch.error_bits() == 0, "device-side error in the block boundary"
 
+    if extras:
+        adv = time_advances(cfg, dev, ws)
+        if adv is not None:
+            res["advance_ms"], res["advances"] = adv
+
     if e2e_steps > 0:
         res["e2e"] = e2e(items, min(K, e2e_steps), W, ws)
     del g_round, g_pass, g_step, g_qkv, g_att
     return res
+
+
+def time_advances(cfg, dev, ws, max_adv: int = 8):
+    """Mean time of the incremental block boundary (dllm_cache_advance) over a
+    sweep of up to max_adv consecutive blocks on one layer instance (prefix
+    state pools on), every call timed with events on its stream; None when a
+    sequence has no block left to advance to.  Layouts, workspaces and the
+    decoded rows are prepared before the timed calls."""
+    from block_wise_kv_gb300 import dllm
+    from block_wise_kv_gb300.inputs import Workload, layout
+    from block_wise_kv_gb300.step import LayerStep
+
+    n_adv = min([max_adv] + [cfg.num_blocks(b) - 1 - cfg.block_index[b] for b in range(cfg.batch)])
+    if n_adv < 1:
+        return None
+    wl = Workload(cfg)
+    W, g = wl.weights_device(0, dev)
+    st = LayerStep(cfg, layer=0, weights=(W, g), device=dev, pre=True)
+    del W
+    x_full, _ = wl.batch_rows_device(0, 1, cfg.block_index, dev)
+    plan = []
+    k_of = list(cfg.block_index)
+    prev = st.batch
+    for _ in range(n_adv):
+        k_of = [k + 1 for k in k_of]
+        lay = layout(cfg, k_of)
+        new = dllm.BatchLayout(lay["block_table"], lay["seq_len"], lay["block_start"], lay["block_len"], device=dev)
+        dec_start = prev.host["block_start"]
+        dec = new.with_blocks(dec_start, lay["block_start"] - dec_start)
+        wsb = dllm.workspace(dllm.dllm_workspace_size(st.desc, dec.c, dllm.DLLM_OP_CACHE_ADVANCE), dev)
+        x_dec = torch.randn(dec.total_block_rows, cfg.d_model, device=dev).to(torch.bfloat16)
+        plan.append((new, dec, wsb, x_dec))
+        prev = new
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(2):  # the second sweep is timed (the first warms up)
+        st.boundary(x_full)
+        torch.cuda.synchronize()
+        times = []
+        for new, dec, wsb, x_dec in plan:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dllm.dllm_cache_advance(st.desc, new.c, dec.c, x_dec, st.gain, st.w_qkv, st.rope, st.rope_max_pos,
+                                    st.cache.c, wsb, stream)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+    assert all(new.error_bits() == 0 for new, _, _, _ in plan), "device-side error in the incremental boundary"
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    return _max_over_ranks(ms, ws), n_adv
 
 
 def e2e(items, Ke, W, ws):
@@ -525,6 +580,14 @@ def summarize(res, hbm, tf_burst, ws, tf_sus=None):
                                               "how": "projection of every row (6 R D HD) + FACache state of U over "
                                                      "U (4 |U|^2 HD per sequence) over the event-timed boundary "
                                                      "(back-to-back boundaries: sustained peak)"}}
+        if "advance_ms" in res:
+            out["cache_build_us"]["advance"] = {
+                "per_boundary": round(res["advance_ms"] * 1e3, 1),
+                "vs_full_build": round(res["build_ms"] / res["advance_ms"], 2),
+                "advances": res["advances"],
+                "how": "dllm_cache_advance (only the decoded blocks' rows changed): their projection, the prefix "
+                       "state extended by their keys, the state over U rebuilt from it and the suffix keys; mean "
+                       "over a sweep of consecutive blocks on one layer instance"}
     return out
 
 

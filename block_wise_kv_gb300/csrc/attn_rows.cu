@@ -25,10 +25,12 @@
 //                  over every key before the new block (phase 1); both then
 //                  add the suffix keys (phase 2) for the state over U.
 //
-// In the modes with a pre state, the state after phase 1 (merged with the
-// pre state read in, for kRowsAdvOld) is written to the pre pools, phase 2
-// starts from an empty accumulator, and the final state is the exact merge
-// (LaCache §3.3.3) of the pre state just written with phase 2's.
+// In the modes with a pre state, the accumulator's state after phase 1 is
+// written to the pre pools and accumulation goes on through phase 2; the kept
+// rows of kRowsAdvOld start from their pre state, loaded into the accumulator
+// (O_t, reference max, sum) before the first page, so that the exact merge
+// (LaCache §3.3.3) of the pre state with the new keys' partial state is the
+// online softmax itself.
 //
 // A unit of work is (sequence b, head h, a pair of query tiles): two tiles of
 // 128 query rows that share every K/V page the unit streams.  Warp 9 streams
@@ -234,27 +236,17 @@ __device__ __forceinline__ void wait_or_abort(RowsShared& S, uint64_t* bar, uint
   }
 }
 
-// Write row srow of a state (m in natural units, l, O~) to the pools (mo, lo, oo):
-// the exact merge (LaCache §3.3.3) of the state read from (mi, li, oi) when
-// has_init with the accumulator's (reference max m_ref, exact max m_true, sum l,
-// O_t's row at o_row when have_o), both taken relative to their common max.
-// The O_t row is read by the whole warp (tcgen05.ld), the pools only for
-// row_out; init and output may be the same pools (read before written).
+// Write row srow of the accumulator's state to the pools (mo, lo, oo): m in
+// natural units is the exact max m_true, l and O~ (O_t's row at o_row, when
+// have_o, else zero) taken from the reference max m_ref to m_true.  The O_t
+// row is read by the whole warp (tcgen05.ld), the pools only for row_out.
 template <int D>
 __device__ __forceinline__ void store_state(uint32_t o_row, bool have_o, float m_ref, float m_true, float l,
-                                            bool has_init, const float* mi_p, const float* li_p, const float* oi_p,
                                             float* mo_p, float* lo_p, float* oo_p, size_t srow, bool row_out) {
-  float mi = neg_inf(), li = 0.f;
-  if (has_init && row_out) {
-    mi = mi_p[srow] * 1.4426950408889634f;  // base-2 units
-    li = li_p[srow];
-  }
-  const float M = fmaxf(mi, m_true);
-  const float wi = mi == neg_inf() ? 0.f : fast_exp2(mi - M);
-  const float wf = (!have_o || m_ref == neg_inf()) ? 0.f : fast_exp2(m_ref - M);
+  const float c = (!have_o || m_ref == neg_inf()) ? 0.f : fast_exp2(m_ref - m_true);
   if (row_out) {
-    mo_p[srow] = M * kLn2;  // -inf stays -inf
-    lo_p[srow] = wi * li + wf * l;
+    mo_p[srow] = m_true * kLn2;  // -inf stays -inf
+    lo_p[srow] = l * c;
   }
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
@@ -266,14 +258,10 @@ __device__ __forceinline__ void store_state(uint32_t o_row, bool have_o, float m
       for (int e = 0; e < 32; ++e) ov[e] = 0.f;
     }
     if (row_out) {
-      const float4* src = reinterpret_cast<const float4*>(oi_p + srow * D + c0);
       float4* dst = reinterpret_cast<float4*>(oo_p + srow * D + c0);
 #pragma unroll
-      for (int qq = 0; qq < 8; ++qq) {
-        const float4 v = has_init ? src[qq] : make_float4(0.f, 0.f, 0.f, 0.f);
-        dst[qq] = make_float4(wi * v.x + wf * ov[4 * qq], wi * v.y + wf * ov[4 * qq + 1],
-                              wi * v.z + wf * ov[4 * qq + 2], wi * v.w + wf * ov[4 * qq + 3]);
-      }
+      for (int qq = 0; qq < 8; ++qq)
+        dst[qq] = make_float4(ov[4 * qq] * c, ov[4 * qq + 1] * c, ov[4 * qq + 2] * c, ov[4 * qq + 3] * c);
     }
   }
 }
@@ -286,8 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = RowsCfg<D>;
   constexpr int TB = C::TB;
   constexpr int NST = C::kStages;
-  // modes with a pre state: phase 2 starts from an empty accumulator
+  // modes that keep the state after phase 1 in the pre pools
   constexpr bool kPre = MODE == kRowsStatePre || MODE == kRowsAdvOld || MODE == kRowsAdvNew;
+  // the kept rows of an incremental boundary start from their pre state (loaded into O_t)
+  constexpr bool kInit = MODE == kRowsAdvOld;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -448,8 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nk = w.s.nk;
         wait_or_abort(S, &S.qfull, nq & 1, bt.err);
         tc_fence_after();
-        // O_t += P_t V of page i (stage st); the unit's first overwrites O_t once the
-        // softmax warps have read the previous unit's O_t out
+        // O_t += P_t V of page i (stage st); the unit's first overwrites O_t (adds to the pre
+        // state loaded there, for the kept rows of an incremental boundary) once the softmax
+        // warps have read the previous unit's O_t out
         auto pv = [&](int i, int st) {
           if (mine) {
             wait_or_abort(S, &S.pfull[t], npv & 1, bt.err);
@@ -459,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + t * D, umma_desc_sw128(pa + kk * 32), umma_desc_sw128_mn(va + kk * 2048, 8192), kIdO,
-                        ((i > 0 && !(kPre && i == w.s.n1)) || kk > 0) ? 1u : 0u);
+                        (i > 0 || kInit || kk > 0) ? 1u : 0u);
             umma_commit(&S.pfree[t]);
             ++npv;
             if (i == nk - 1) {
@@ -527,9 +518,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE != kRowsBlock && row_out)
         srow = (static_cast<size_t>(page_of(bt, gb, pos / kPage)) * H + w.h) * kPage + pos % kPage;
       float m_ref = neg_inf(), m_true = neg_inf(), l = 0.f;
-      if (kPre && q.n1 == 0)  // no phase 1: the pre state is the one read in (or empty)
-        store_state<D>(o_row, false, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pre,
-                       a.l_pre, a.o_pre, srow, row_out);
+      if (kInit) {
+        // the kept row's pre state becomes the accumulator: O_t's row (the previous unit's
+        // O_t is read out and its last P V complete), the reference max and the sum
+        float mi = neg_inf(), li = 0.f;
+        if (row_out) {
+          mi = a.m_pre[srow] * 1.4426950408889634f;  // base-2 units
+          li = a.l_pre[srow];
+        }
+        const bool have = mi != neg_inf();
+#pragma unroll
+        for (int h0 = 0; h0 < D; h0 += 64) {  // two batches of loads in flight
+          float4 v[16];
+#pragma unroll
+          for (int qq = 0; qq < 16; ++qq)
+            v[qq] = have ? reinterpret_cast<const float4*>(a.o_pre + srow * D + h0)[qq] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            float ov[32];
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq) {
+              ov[4 * qq] = v[c0 / 4 + qq].x;
+              ov[4 * qq + 1] = v[c0 / 4 + qq].y;
+              ov[4 * qq + 2] = v[c0 / 4 + qq].z;
+              ov[4 * qq + 3] = v[c0 / 4 + qq].w;
+            }
+            tmem_st_32x32b_x32(o_row + h0 + c0, ov);
+          }
+        }
+        tmem_st_wait();
+        if (have) {
+          m_ref = mi;
+          m_true = mi;
+          l = li;
+        }
+      }
+      if (kPre && q.n1 == 0)  // no phase 1: an empty pre state
+        store_state<D>(o_row, false, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
       for (int i = 0; i < q.nk; ++i) {
         const int bsel = ns & 1;
         wait_or_abort(S, &S.sfull[t][bsel], (ns >> 1) & 1, bt.err);
@@ -558,18 +583,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 8; cc < 64; ++cc) mx8[cc & 7] = fmaxf(mx8[cc & 7], sc[cc]);
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * a.scale_log2;
-        // pre modes: phase 2 starts from an empty accumulator; phase 1's state is kept for
-        // the pre pools
+        // pre modes: the state after phase 1 (before this page) goes to the pre pools
         const bool snap = kPre && i == q.n1 && i > 0;
         const float s_mref = m_ref, s_mtrue = m_true, s_l = l;
-        if (snap) {
-          m_true = neg_inf();
-          l = 0.f;
-        }
         m_true = fmaxf(m_true, mx);
-        // a new reference max (the accumulator's first page, or a rise beyond the threshold)
+        // a new reference max (the accumulator's first keys, or a rise beyond the threshold)
         float factor = 1.f;
-        if (i == 0 || snap) {
+        if (m_ref == neg_inf()) {
           m_ref = mx;
         } else if (mx > m_ref + kRescale) {
           factor = fast_exp2(m_ref - mx);
@@ -587,9 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // earlier page (rescaled here when the reference max rose)
         if (pw >= 1) wait_or_abort(S, &S.pfree[t], (pw - 1) & 1, bt.err);
         tc_fence_after();
-        if (snap)  // O_t holds phase 1: the pre state, before this page's P V overwrites O_t
-          store_state<D>(o_row, true, s_mref, s_mtrue, s_l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre,
-                         a.m_pre, a.l_pre, a.o_pre, srow, row_out);
+        if (snap)  // O_t holds phase 1 (relative to the reference max before this page)
+          store_state<D>(o_row, true, s_mref, s_mtrue, s_l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
         if (__any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -620,19 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- the unit is complete for this tile: O_t out, then released for the next unit
       wait_or_abort(S, &S.ofull[t], no & 1, bt.err);
       tc_fence_after();
-      if (MODE == kRowsState) {
-        store_state<D>(o_row, true, m_ref, m_true, l, false, nullptr, nullptr, nullptr, a.m_pool, a.l_pool, a.o_pool,
-                       srow, row_out);
-      } else if (kPre) {
-        if (q.n2 == 0) {  // phase 1 only: the state over U is the pre state (read in first)
-          store_state<D>(o_row, true, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pool,
-                         a.l_pool, a.o_pool, srow, row_out);
-          store_state<D>(o_row, true, m_ref, m_true, l, MODE == kRowsAdvOld, a.m_pre, a.l_pre, a.o_pre, a.m_pre,
-                         a.l_pre, a.o_pre, srow, row_out);
-        } else {  // the pre state written above, merged with phase 2's
-          store_state<D>(o_row, true, m_ref, m_true, l, true, a.m_pre, a.l_pre, a.o_pre, a.m_pool, a.l_pool,
-                         a.o_pool, srow, row_out);
-        }
+      if (MODE == kRowsState || kPre) {
+        store_state<D>(o_row, true, m_ref, m_true, l, a.m_pool, a.l_pool, a.o_pool, srow, row_out);
+        if (kPre && q.n2 == 0)  // phase 1 only: the pre state is the same
+          store_state<D>(o_row, true, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
       } else {
         // O = (w_c O~_c + w_f O_t) / L with the cached state (merge) or O_t / l (block rows)
         float wc = 0.f, wf = 1.f, M = m_ref, L = l;
