@@ -165,7 +165,7 @@ class ClockSampler:
 # with the hash of the kernel's sources at capture time: the figure is
 # reported only while the sources still hash the same (else null).
 KERNEL_SOURCES = {
-    "qkv": ("qkv_gemm.cu", "norm.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
+    "qkv": ("qkv_gemm.cu", "qkv_wide.cu", "norm.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
     "attention": ("attn_stream.cu", "attn_common.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
 }
 TRAFFIC = {
