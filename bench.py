@@ -169,10 +169,10 @@ KERNEL_SOURCES = {
     "attention": ("attn_stream.cu", "attn_common.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
 }
 TRAFFIC = {
-    # (workload, kernel): (bytes per launch, sources hash); profiles/attn_stream_stack.md,
-    # profiles/qkv_gemm_stack.md
-    ("stack", "attention"): (1_176_412_392, "75a391b53b9afa55"),
-    ("stack", "qkv"): (108_459_776, "272b0963be33b34b"),
+    # (workload, kernel): (DRAM bytes per launch, sources hash); profiles/attn_stream_stack.md,
+    # profiles/qkv_wide_stack.md
+    ("stack", "attention"): (1_176_540_672, "9801264b857656ca"),
+    ("stack", "qkv"): (135_720_960, "eac74e05f86e5bcb"),
 }
 
 
