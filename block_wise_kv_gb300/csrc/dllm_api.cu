@@ -413,6 +413,52 @@ dllm_status dllm_step_attention(const dllm_layer_desc* desc, const dllm_batch* b
   return attention_call(desc, batch, q_block, cache, o_full, lse, ws, ws_bytes, stream, true, true);
 }
 
+dllm_status dllm_lm_head_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t vocab,
+                                        size_t* bytes) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (bytes == nullptr || vocab < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  *bytes = batch->batch > 0 && batch->total_block_rows > 0
+               ? lm_head_workspace_bytes(batch->total_block_rows, desc->d_model, vocab)
+               : 0;
+  return DLLM_OK;
+}
+
+dllm_status dllm_block_lm_head(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t vocab,
+                               const void* h_full, const void* final_gain, const void* w_lm, void* logits,
+                               float* lse, int32_t* argmax, float* p_max, void* ws, size_t ws_bytes, void* stream) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (vocab < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (desc->d_model % 128 != 0 || vocab % 8 != 0) return DLLM_ERR_UNSUPPORTED;
+  if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
+  if (!aligned(h_full, 16) || !aligned(final_gain, 16) || !aligned(w_lm, 16) || !aligned(lse, 4) ||
+      !aligned(argmax, 4) || !aligned(p_max, 4))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (logits != nullptr && !aligned(logits, 16)) return DLLM_ERR_INVALID_ARGUMENT;
+  size_t need = 0;
+  DLLM_TRY(dllm_lm_head_workspace_size(desc, batch, vocab, &need));
+  if (ws_bytes < need) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
+  LmArgs a;
+  dllm_cache none = {};
+  none.num_pages = 1;
+  a.bt = batch_args(batch, &none);
+  a.h = h_full;
+  a.gain = final_gain;
+  a.logits = logits;
+  a.lse = lse;
+  a.argmax = argmax;
+  a.p_max = p_max;
+  a.n_rows = batch->total_block_rows;
+  a.d_model = desc->d_model;
+  a.vocab = vocab;
+  a.rms_eps = desc->rms_eps;
+  lm_bind_workspace(&a, ws);
+  DLLM_CUDA_TRY(launch_lm_head(w_lm, a, device_sms(), static_cast<cudaStream_t>(stream)));
+  return DLLM_OK;
+}
+
 const char* dllm_status_string(dllm_status status) {
   switch (status) {
     case DLLM_OK:

@@ -139,6 +139,27 @@ cudaError_t launch_qkv_gemm(const void* w_packed, const QkvArgs& a, const QkvPla
 // The block attention (LaCache Eq. (2)-(6) over all keys of each block row)
 // and/or the FACache merge of every invariant row, as planned by attn_plan.
 cudaError_t launch_step_attention(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+// The block-only epilogue (lm_head.cu): the block rows of the final hidden states, the
+// final RMSNorm, the LM head and the softmax over the vocabulary.
+struct LmArgs {
+  BatchArgs bt;
+  const void* h;     // bf16 [R][d_model]: every row's final hidden state (packed by cu_seq)
+  const void* gain;  // bf16 [d_model]: the final RMSNorm gain
+  void* xhat;        // workspace: bf16 [n_rows][d_model]
+  float* pmax;       // workspace: [2 * vocab tiles][n_rows] per-half-tile max, sum of exp, argmax
+  float* psum;
+  int32_t* parg;
+  void* logits;      // bf16 [n_rows][vocab], nullable
+  float* lse;        // [n_rows]
+  int32_t* argmax;   // [n_rows]
+  float* p_max;      // [n_rows]
+  int32_t n_rows, d_model, vocab;
+  float rms_eps;
+};
+size_t lm_head_workspace_bytes(int n_rows, int d_model, int vocab);
+void lm_bind_workspace(LmArgs* a, void* ws);
+cudaError_t launch_lm_head(const void* w_lm, const LmArgs& a, int num_sms, cudaStream_t stream);
+
 // Attention of 128-row query tiles on the tensor cores (attn_rows.cu):
 //   kRowsState  every row of U over the keys of U: (m, l, O~) into the pools (the cache build)
 //   kRowsBlock  the block rows over every key: O and L (blocks of more than 64 rows)

@@ -45,7 +45,8 @@ PAGE = 64
 # Every symbol include/dllm.h declares.
 EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_qkv_weight_packed_bytes", "dllm_qkv_weight_pack",
            "dllm_cache_build", "dllm_cache_advance", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
-           "dllm_block_attention", "dllm_state_merge", "dllm_step_attention", "dllm_status_string")
+           "dllm_block_attention", "dllm_state_merge", "dllm_step_attention", "dllm_lm_head_workspace_size",
+           "dllm_block_lm_head", "dllm_status_string")
 
 
 class DllmError(RuntimeError):
@@ -107,6 +108,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                 "dllm_block_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
                 "dllm_state_merge": [P(LayerDescC), P(BatchC), P(CacheC), vp, vp, vp, sz, vp],
                 "dllm_step_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
+                "dllm_lm_head_workspace_size": [P(LayerDescC), P(BatchC), i32, P(sz)],
+                "dllm_block_lm_head": [P(LayerDescC), P(BatchC), i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             }
             for name, argt in sig.items():
                 fn = getattr(lib, name)
@@ -226,6 +229,19 @@ def dllm_step_attention(desc, batch, q_block, cache, o_full, lse=None, ws=None, 
     _check("dllm_step_attention", load().dllm_step_attention(
         ctypes.byref(desc), ctypes.byref(batch), _ptr(q_block), ctypes.byref(cache), _ptr(o_full), _ptr(lse),
         _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def dllm_lm_head_workspace_size(desc, batch, vocab: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("dllm_lm_head_workspace_size", load().dllm_lm_head_workspace_size(ctypes.byref(desc), ctypes.byref(batch),
+                                                                             int(vocab), ctypes.byref(out)))
+    return int(out.value)
+
+
+def dllm_block_lm_head(desc, batch, vocab, h_full, final_gain, w_lm, logits, lse, argmax, p_max, ws, stream=None):
+    _check("dllm_block_lm_head", load().dllm_block_lm_head(
+        ctypes.byref(desc), ctypes.byref(batch), int(vocab), _ptr(h_full), _ptr(final_gain), _ptr(w_lm),
+        _ptr(logits), _ptr(lse), _ptr(argmax), _ptr(p_max), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 # ---------------------------------------------------- memory / structs ----

@@ -40,7 +40,7 @@ PAGE = 64
 
 # role ids folded into seeds
 (_R_WEIGHT, _R_PROMPT, _R_BLOCK, _R_MASK, _R_EMBED, _R_IDS_PROMPT, _R_IDS_BLOCK, _R_SHAPE, _R_PAGES,
- _R_SUFFIX) = range(1, 11)
+ _R_SUFFIX, _R_HIDDEN, _R_LM) = range(1, 13)
 
 
 def splitmix64(x: int) -> int:
@@ -264,6 +264,21 @@ class Workload:
             full.append(torch.cat([head, mask.expand(n_suffix, c.d_model)], 0))
             blk.append(full[-1][s0:] if c.prefix_only else head[s0:])
         return torch.cat(full, 0).contiguous(), torch.cat(blk, 0).contiguous()
+
+    # ------------------------------------------------- block-only epilogue
+    def lm_inputs(self, vocab: int, gain_spread: float = 0.0):
+        """(h_full [R, D] ~ N(0, 1) bf16: the final hidden states of every row, packed in
+        sequence order; final RMSNorm gain bf16 [D] (1, or uniform in 1 +- gain_spread);
+        W_lm [vocab, D] ~ N(0, 0.02) bf16: a synthetic LM head)."""
+        c = self.cfg
+        R = sum(c.seq_len(b) for b in range(c.batch))
+        h = randn_bf16((R, c.d_model), derive_seed(c.seed, _R_HIDDEN))
+        g = torch.ones(c.d_model)
+        if gain_spread > 0:
+            u = torch.rand(c.d_model, generator=_gen(derive_seed(c.seed, _R_HIDDEN, 1)))
+            g = 1.0 + gain_spread * (2 * u - 1)
+        W = randn_bf16((vocab, c.d_model), derive_seed(c.seed, _R_LM, vocab), std=0.02)
+        return h, g.to(torch.bfloat16), W
 
     # ---------------------------------------------------------------- layout
     def page_lists(self):

@@ -322,6 +322,27 @@ dllm_status dllm_step_attention(const dllm_layer_desc* desc, const dllm_batch* b
                                 const dllm_cache* cache, void* o_full, float* lse, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/* Block-only epilogue after the layer stack (LaCache §3.4, the sampling
+ * stage: the output is cut to the tokens of the current generation block;
+ * Fast-dLLM "Block-wise Generation").  For the B_b rows of each current block
+ * only (block row i of sequence b is row cu_seq[b] + s_b + i of h_full):
+ *   x^ = RMSNorm(h) with gain final_gain (correctly rounded to bf16),
+ *   logits = x^ W_lm^T (fp32 accumulation, W_lm bf16 [vocab][d_model]),
+ *   and the softmax over the vocabulary, summarised per row as
+ *   lse = log sum_v exp(logit_v), argmax = the lowest v with the largest
+ *   logit, p_max = exp(logit_argmax - lse) (the confidence the sampler
+ *   compares with its threshold),
+ * written to lse, argmax, p_max (device [M] each, M = batch->total_block_rows,
+ * packed by cu_block) and, when logits is non-NULL, the bf16 logits
+ * [M][vocab].  d_model must be a multiple of 128 and vocab of 8.
+ *   ws: dllm_lm_head_workspace_size bytes (the x^ rows and per-tile partial
+ *   softmax statistics). */
+dllm_status dllm_lm_head_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t vocab,
+                                        size_t* bytes);
+dllm_status dllm_block_lm_head(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t vocab,
+                               const void* h_full, const void* final_gain, const void* w_lm, void* logits,
+                               float* lse, int32_t* argmax, float* p_max, void* ws, size_t ws_bytes, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* dllm_status_string(dllm_status status);
 

@@ -87,6 +87,7 @@ def _load():
                     [_D, _i64, _D, _D, _i64, _i64, _i64, _f64, _i64, _i64, _i64, _D, _D, _D, _D, _D],
                     None,
                 ),
+                "orc_softmax_stats": ([_D, _i64, _i64, _D, _I64, _D], None),
                 "orc_alg1": (
                     [_D, _D, _D, _i64, _i64, _i64, _f64, _i64, _i64, _i64, _i64, ctypes.c_int, _D, _D, _D, _D, _D],
                     None,
@@ -224,6 +225,30 @@ def project(x: np.ndarray, W: np.ndarray) -> np.ndarray:
     """x [rows, D] times W^T: the projection of the step, `orc_linear`'s plain
     sums in oracle.cpp (pinned against numpy's matmul)."""
     return linear(x, W)
+
+
+def softmax_stats(z):
+    """Per row of logits z [rows, V]: (lse, argmax (lowest index of the max), p_max)."""
+    z = _c(z)
+    rows, V = z.shape
+    lse = np.empty(rows)
+    am = np.empty(rows, dtype=np.int64)
+    pm = np.empty(rows)
+    _load().orc_softmax_stats(_p(z), rows, V, _p(lse), am.ctypes.data_as(_I64), _p(pm))
+    return lse, am, pm
+
+
+def lm_head(h, g, W_lm, eps: float, mirror: bool = True):
+    """The block-only epilogue for the given rows (the block rows of the final hidden
+    states; LaCache §3.4, the sampling stage): x^ = RMSNorm(h) (rounded to bf16 when
+    `mirror`: the GEMM operand), logits = x^ W_lm^T, and the softmax summary.
+    Returns dict(logits, lse, argmax, p_max)."""
+    xh = rmsnorm(h, g, eps)
+    if mirror:
+        xh = bf16_round(xh)
+    z = linear(xh, W_lm)
+    lse, am, pm = softmax_stats(z)
+    return dict(logits=z, lse=lse, argmax=am, p_max=pm)
 
 
 # ---------------------------------------------------------------- the step

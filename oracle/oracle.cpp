@@ -332,4 +332,26 @@ void orc_alg1(const double* q, const double* k, const double* v, int64_t N, int6
   }
 }
 
+// The softmax over a row of logits, summarised (LaCache §3.4, the sampling stage; the
+// quantities a confidence sampler reads): lse = m + log sum_v exp(z_v - m) with m the row
+// max, argmax = the lowest v with z_v = m, p_max = exp(m - lse).  Two passes, fp64.
+void orc_softmax_stats(const double* z, int64_t rows, int64_t V, double* lse, int64_t* argmax, double* pmax) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* zr = z + r * V;
+    double m = zr[0];
+    int64_t am = 0;
+    for (int64_t v = 1; v < V; ++v)
+      if (zr[v] > m) {
+        m = zr[v];
+        am = v;
+      }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) s += exp(zr[v] - m);
+    lse[r] = m + log(s);
+    argmax[r] = am;
+    pmax[r] = exp(m - lse[r]);
+  }
+}
+
 }  // extern "C"

@@ -162,3 +162,19 @@ def test_cache_advance_rejects_before_launch(lib):
     # its workspace is the projection of the decoded rows
     assert dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_CACHE_ADVANCE) == \
         dllm.dllm_workspace_size(d, b, dllm.DLLM_OP_BLOCK_QKV_ROPE_WRITE)
+
+
+def test_lm_head_rejects_before_launch(lib):
+    d = _desc()
+    b = _batch()
+    fake = 0x10000
+    # 2 * ceil(V / 256) half-tile partials (max, sum, argmax) per row and the x^ rows, 256-byte aligned
+    n = dllm.dllm_lm_head_workspace_size(d, b, 126464)
+    assert n == 64 * 4096 * 2 + 3 * ((2 * 494 * 64 * 4 + 255) // 256 * 256)
+    for vocab, kw, status in ((100, {}, dllm.DLLM_ERR_UNSUPPORTED),           # vocab not a multiple of 8
+                              (1024, dict(d_model=4032), dllm.DLLM_ERR_UNSUPPORTED),  # d_model not of 128
+                              (0, {}, dllm.DLLM_ERR_INVALID_ARGUMENT),
+                              (1024, {}, dllm.DLLM_ERR_WORKSPACE_TOO_SMALL)):
+        with pytest.raises(dllm.DllmError) as e:
+            dllm.dllm_block_lm_head(_desc(**kw), b, vocab, fake, fake, fake, None, fake, fake, fake, None, 0)
+        assert e.value.status == status, (vocab, kw)

@@ -34,6 +34,9 @@ MUTANTS = {
     "alg1_skip_overlapping_q": ("if (!genstep && !q_overlap && !k_overlap) continue;",
                                 "if (!genstep && !k_overlap) continue;"),
     "bf16_ties_away": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
+    "softmax_argmax_last_of_ties": ("      if (zr[v] > m) {\n        m = zr[v];\n        am = v;",
+                                    "      if (zr[v] >= m) {\n        m = zr[v];\n        am = v;"),
+    "softmax_lse_without_max": ("lse[r] = m + log(s);", "lse[r] = log(s);"),
 }
 
 

@@ -323,3 +323,48 @@ def test_layer_step_matches_library_composition():
     np.testing.assert_allclose(ref["O"], O.numpy(), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(ref["k"], k.numpy(), rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(ref["q"], q.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------------ the block-only epilogue (softmax summary)
+def test_softmax_stats_against_library_and_closed_forms():
+    """LaCache §3.4 (the sampling stage): per row, lse, the argmax and its
+    probability.  Pinned to scipy's logsumexp and numpy's argmax, and to
+    closed forms: equal logits give lse = log V, argmax 0 (the lowest index
+    among ties) and p_max = 1 / V; a shift by c moves lse by c only."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(11)
+    z = rng.normal(scale=3.0, size=(7, 300))
+    lse, am, pm = orc.softmax_stats(z)
+    assert np.allclose(lse, logsumexp(z, axis=1), rtol=0, atol=1e-12)
+    assert np.array_equal(am, z.argmax(axis=1))
+    assert np.allclose(pm, np.exp(z.max(axis=1) - lse), rtol=1e-13, atol=0)
+    V = 256
+    lse, am, pm = orc.softmax_stats(np.full((2, V), 1.5))
+    assert np.allclose(lse, 1.5 + np.log(V), atol=1e-13) and np.array_equal(am, [0, 0])
+    assert np.allclose(pm, 1.0 / V, rtol=1e-13)
+    t = np.zeros((1, 10))
+    t[0, [3, 7]] = 5.0  # a tie between 3 and 7: the lowest index
+    assert orc.softmax_stats(t)[1][0] == 3
+    lse2, am2, pm2 = orc.softmax_stats(z + 4.25)
+    lse0, am0, pm0 = orc.softmax_stats(z)
+    assert np.allclose(lse2, lse0 + 4.25, atol=1e-12) and np.array_equal(am2, am0) and np.allclose(pm2, pm0)
+
+
+def test_lm_head_against_torch_composition():
+    """RMSNorm (torch's rms_norm), the bf16 operand, the LM head (torch matmul)
+    and torch's logsumexp / argmax / softmax reproduce the oracle's block-only
+    epilogue."""
+    import torch
+    rng = np.random.default_rng(12)
+    h = rng.normal(size=(5, 64)).astype(np.float64)
+    g = rng.uniform(0.5, 1.5, size=64)
+    W = rng.normal(scale=0.1, size=(96, 64))
+    ref = orc.lm_head(h, g, W, 1e-5)
+    th = torch.from_numpy(h)
+    xh = torch.nn.functional.rms_norm(th, (64,), torch.from_numpy(g), eps=1e-5)
+    xh = xh.to(torch.bfloat16).to(torch.float64)
+    z = xh @ torch.from_numpy(W).T
+    assert np.allclose(ref["logits"], z.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(ref["lse"], torch.logsumexp(z, 1).numpy(), atol=1e-12)
+    assert np.array_equal(ref["argmax"], z.argmax(1).numpy())
+    assert np.allclose(ref["p_max"], torch.softmax(z, 1).max(1).values.numpy(), rtol=1e-12)
