@@ -167,6 +167,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "qkv": ("qkv_gemm.cu", "qkv_wide.cu", "norm.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
     "attention": ("attn_stream.cu", "attn_common.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
+    "lm_head": ("lm_head.cu", "norm.cuh", "sm103.cuh", "kernels.cuh", "tmap.cuh"),
 }
 TRAFFIC = {
     # (workload, kernel): (DRAM bytes per launch, sources hash); profiles/attn_stream_stack.md,
@@ -414,6 +415,7 @@ def measure(cfg, L, K, W, P, sample_every, dev, rank, ws, extras=True, e2e_steps
         adv = time_advances(cfg, dev, ws)
         if adv is not None:
             res["advance_ms"], res["advances"] = adv
+        res["lm_head_ms"] = time_lm_head(cfg, items[0][0], dev, ws)
 
     if e2e_steps > 0:
         res["e2e"] = e2e(items, min(K, e2e_steps), W, ws)
@@ -469,6 +471,44 @@ def time_advances(cfg, dev, ws, max_adv: int = 8):
     assert all(new.error_bits() == 0 for new, _, _, _ in plan), "device-side error in the incremental boundary"
     ms = statistics.mean(a.elapsed_time(b) for a, b in times)
     return _max_over_ranks(ms, ws), n_adv
+
+
+LM_VOCAB = 126464  # the LLaDA-8B vocabulary size (the LM head's weights are synthetic)
+
+
+def time_lm_head(cfg, st, dev, ws, reps: int = 10):
+    """Event-timed dllm_block_lm_head (the block-only epilogue after the layer stack) on the
+    workload's block rows with a synthetic LM head of LM_VOCAB entries: mean of `reps`
+    calls after a warm-up call, each call timed with events on its stream."""
+    from block_wise_kv_gb300 import dllm
+
+    R, D = st.batch.total_seq_rows, cfg.d_model
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    h = torch.randn(R, D, generator=g, device=dev).to(torch.bfloat16)
+    W = (torch.randn(LM_VOCAB, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    gain = torch.ones(D, dtype=torch.bfloat16, device=dev)
+    M = st.batch.total_block_rows
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    pm = torch.empty(M, dtype=torch.float32, device=dev)
+    wsb = dllm.workspace(dllm.dllm_lm_head_workspace_size(st.desc, st.batch.c, LM_VOCAB), dev)
+    stream = torch.cuda.current_stream()
+    call = lambda: dllm.dllm_block_lm_head(st.desc, st.batch.c, LM_VOCAB, h, gain, W, None, lse, am, pm, wsb, stream)
+    call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() == 0, "device-side error in the LM head"
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del W, h
+    return _max_over_ranks(ms, ws)
 
 
 def e2e(items, Ke, W, ws):
@@ -580,6 +620,13 @@ def summarize(res, hbm, tf_burst, ws, tf_sus=None):
                                               "how": "projection of every row (6 R D HD) + FACache state of U over "
                                                      "U (4 |U|^2 HD per sequence) over the event-timed boundary "
                                                      "(back-to-back boundaries: sustained peak)"}}
+        if "lm_head_ms" in res:
+            M, D = int(st.batch.total_block_rows), cfg.d_model
+            lm_bytes = LM_VOCAB * D * 2 + M * D * 2
+            out["block_lm_head"] = kernel_roofline(
+                f"dllm_block_lm_head (block rows only: gather + RMSNorm, tcgen05 LM head of {LM_VOCAB} entries with "
+                "the softmax summary in its epilogue, ordered merge)", lm_bytes, 2 * M * LM_VOCAB * D,
+                res["lm_head_ms"] * 1e-3, hbm, tf_burst, cfg.name, "lm_head")
         if "advance_ms" in res:
             out["cache_build_us"]["advance"] = {
                 "per_boundary": round(res["advance_ms"] * 1e3, 1),
@@ -654,6 +701,7 @@ def run_ours(args, rank, ws, local):
         "steady_state_frac": head["steady_state_frac"],
         "block_rows_only": head["block_rows_only"],
         "cache_build_us": head["cache_build_us"],
+        "block_lm_head": head.get("block_lm_head"),
         "roofline": {k: v for k, v in dominant.items()},
         "roofline_kernels": rk,
         "peak_source": f"{peak_kind} MEASURED_PEAKS hbm_gbs / bf16_tflops (burst: each kernel timed alone)",
