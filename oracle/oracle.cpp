@@ -276,57 +276,56 @@ void orc_state_merge(const double* q, int64_t nrows, const double* k, const doub
   }
 }
 
-// LaCache Algorithm 1 at tile granularity, for one sequence of N tokens whose
-// current block is [c_lo, c_hi).  Queries are split into tiles of br rows and
-// keys into tiles of bc.  A tile "overlaps" the block if any of its tokens
-// lies in [c_lo, c_hi).
-//   genstep != 0: every query tile streams every KV tile; for query tiles that
-//     do not overlap the block, the cache state (mc, lc, Oc) is the online
-//     state over the KV tiles that do not overlap the block (§3.3.3: the cache
-//     is updated like (m, l, O~) over the KV blocks fully inside U).
-//   genstep == 0: query tiles that do not overlap the block start from the
-//     cache and skip every KV tile that does not overlap the block; other
-//     query tiles stream every KV tile from the empty state.
-// All rows produce O and L.  q, k, v [N][H][d]; cache mc, lc [N][H], Oc [N][H][d].
+// The FACache of LaCache §3.3.3 at tile granularity, for one sequence of N
+// tokens whose current block is C = [c_lo, c_hi).  Rows are grouped in tiles
+// of br and keys in tiles of bc; a tile that holds any token of C is fresh as
+// a whole.  Written as sets: R_f / K_f = the rows / keys of fresh tiles, and
+// K_u = every other key.
+//   genstep != 0 (building the cache): every row's output is its attention
+//     over all N keys; every row outside R_f also stores, in (mc, lc, Oc), its
+//     online-softmax state over K_u.
+//   genstep == 0 (reusing it): a row outside R_f outputs the exact merge of its
+//     stored state with its state over K_f; a row of R_f attends over all keys.
+// Every row produces O and L.  q, k, v [N][H][d]; mc, lc [N][H], Oc [N][H][d].
 void orc_alg1(const double* q, const double* k, const double* v, int64_t N, int64_t H, int64_t d, double scale,
               int64_t c_lo, int64_t c_hi, int64_t br, int64_t bc, int genstep, double* mc, double* lc, double* Oc,
               double* O, double* L) {
-  const int64_t tr = (N + br - 1) / br, tc = (N + bc - 1) / bc;
-  auto overlaps = [&](int64_t lo, int64_t hi) { return lo < c_hi && c_lo < hi; };
+  // the tile-granular sets
+  std::vector<char> row_fresh(N, 0);
+  std::vector<int64_t> keys_all, keys_fresh, keys_kept;
+  auto tile_holds_block = [&](int64_t t, int64_t size) {
+    const int64_t lo = t * size, hi = (lo + size < N) ? lo + size : N;
+    return lo < c_hi && c_lo < hi;
+  };
+  for (int64_t r = 0; r < N; ++r) row_fresh[r] = tile_holds_block(r / br, br) ? 1 : 0;
+  for (int64_t j = 0; j < N; ++j) {
+    keys_all.push_back(j);
+    (tile_holds_block(j / bc, bc) ? keys_fresh : keys_kept).push_back(j);
+  }
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
-  for (int64_t i = 0; i < tr; ++i) {
+  for (int64_t r = 0; r < N; ++r) {
     for (int64_t h = 0; h < H; ++h) {
-      const int64_t r0 = i * br, r1 = (r0 + br < N) ? r0 + br : N;
-      const bool q_overlap = overlaps(r0, r1);
-      std::vector<int64_t> keys;
-      for (int64_t r = r0; r < r1; ++r) {
-        const double* qr = q + (r * H + h) * d;
-        double m = -INFINITY, l = 0.0;
-        std::vector<double> Ot(d, 0.0);
+      const double* qr = q + (r * H + h) * d;
+      const int64_t rh = r * H + h;
+      double m = -INFINITY, l = 0.0;
+      std::vector<double> Ot(d, 0.0);
+      if (genstep || row_fresh[r]) {  // attention over every key
+        online_update(qr, k, v, H, h, d, scale, keys_all.data(), (int64_t)keys_all.size(), &m, &l, Ot.data());
+      } else {  // the stored state, merged with the fresh keys
+        m = mc[rh];
+        l = lc[rh];
+        for (int64_t c = 0; c < d; ++c) Ot[c] = Oc[rh * d + c];
+        online_update(qr, k, v, H, h, d, scale, keys_fresh.data(), (int64_t)keys_fresh.size(), &m, &l, Ot.data());
+      }
+      for (int64_t c = 0; c < d; ++c) O[rh * d + c] = Ot[c] / l;
+      L[rh] = m + log(l);
+      if (genstep && !row_fresh[r]) {  // store the state over the kept keys
         double cm = -INFINITY, cl = 0.0;
         std::vector<double> cO(d, 0.0);
-        if (!genstep && !q_overlap) {  // initialise with the cache
-          m = mc[r * H + h];
-          l = lc[r * H + h];
-          for (int64_t c = 0; c < d; ++c) Ot[c] = Oc[(r * H + h) * d + c];
-        }
-        for (int64_t j = 0; j < tc; ++j) {
-          const int64_t k0 = j * bc, k1 = (k0 + bc < N) ? k0 + bc : N;
-          const bool k_overlap = overlaps(k0, k1);
-          if (!genstep && !q_overlap && !k_overlap) continue;  // already in the cache
-          keys.clear();
-          for (int64_t t = k0; t < k1; ++t) keys.push_back(t);
-          online_update(qr, k, v, H, h, d, scale, keys.data(), (int64_t)keys.size(), &m, &l, Ot.data());
-          if (genstep && !q_overlap && !k_overlap)
-            online_update(qr, k, v, H, h, d, scale, keys.data(), (int64_t)keys.size(), &cm, &cl, cO.data());
-        }
-        for (int64_t c = 0; c < d; ++c) O[(r * H + h) * d + c] = Ot[c] / l;
-        L[r * H + h] = m + log(l);
-        if (genstep && !q_overlap) {  // store the cache
-          mc[r * H + h] = cm;
-          lc[r * H + h] = cl;
-          for (int64_t c = 0; c < d; ++c) Oc[(r * H + h) * d + c] = cO[c];
-        }
+        online_update(qr, k, v, H, h, d, scale, keys_kept.data(), (int64_t)keys_kept.size(), &cm, &cl, cO.data());
+        mc[rh] = cm;
+        lc[rh] = cl;
+        for (int64_t c = 0; c < d; ++c) Oc[rh * d + c] = cO[c];
       }
     }
   }

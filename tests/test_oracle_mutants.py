@@ -31,8 +31,8 @@ MUTANTS = {
     "build_includes_block_keys": ("if (j < c_lo || j >= c_hi) keys.push_back(j);", "keys.push_back(j);"),
     "merge_block_off_by_one": ("for (int64_t j = t0; j < c_hi && j < t0 + bc; ++j)",
                                "for (int64_t j = t0 + 1; j < c_hi && j < t0 + bc; ++j)"),
-    "alg1_skip_overlapping_q": ("if (!genstep && !q_overlap && !k_overlap) continue;",
-                                "if (!genstep && !k_overlap) continue;"),
+    "alg1_fresh_rows_from_cache": ("if (genstep || row_fresh[r]) {  // attention over every key",
+                                   "if (genstep) {  // attention over every key"),
     "bf16_ties_away": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
     "softmax_argmax_last_of_ties": ("      if (zr[v] > m) {\n        m = zr[v];\n        am = v;",
                                     "      if (zr[v] >= m) {\n        m = zr[v];\n        am = v;"),
