@@ -20,7 +20,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIBPATH = os.path.join(LIBDIR, "libdllm.so")
 
-SOURCES = ["dllm_api.cu", "qkv_gemm.cu", "qkv_wide.cu", "attn_rows.cu", "attn_stream.cu", "misc.cu", "noalloc.cu", "lm_head.cu"]
+SOURCES = ["dllm_api.cu", "qkv_gemm.cu", "qkv_wide.cu", "attn_rows.cu", "attn_stream.cu", "misc.cu", "noalloc.cu", "lm_head.cu", "ffn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I",
          CSRC]

@@ -459,6 +459,55 @@ dllm_status dllm_block_lm_head(const dllm_layer_desc* desc, const dllm_batch* ba
   return DLLM_OK;
 }
 
+dllm_status dllm_ffn_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t d_ff,
+                                    size_t* bytes) {
+  DLLM_TRY(check_desc(desc));
+  DLLM_TRY(check_batch(batch));
+  if (bytes == nullptr || d_ff < 1) return DLLM_ERR_INVALID_ARGUMENT;
+  if (desc->d_model % 128 != 0 || d_ff % 128 != 0) return DLLM_ERR_UNSUPPORTED;
+  *bytes = batch->batch > 0 && batch->total_block_rows > 0
+               ? ffn_workspace_bytes(batch->total_block_rows, desc->d_model, desc->n_heads * desc->head_dim, d_ff,
+                                     device_sms())
+               : 0;
+  return DLLM_OK;
+}
+
+dllm_status dllm_block_ffn(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t d_ff, const void* o_full,
+                           const void* x_block, const void* w_o, const void* ffn_gain, const void* w_gate_up,
+                           const float* w_gate_up_scale, const void* w_down, const float* w_down_scale,
+                           void* y_block, void* ws, size_t ws_bytes, void* stream) {
+  size_t need = 0;
+  DLLM_TRY(dllm_ffn_workspace_size(desc, batch, d_ff, &need));
+  if (batch->batch == 0 || batch->total_block_rows == 0) return DLLM_OK;
+  if (!aligned(o_full, 16) || !aligned(x_block, 16) || !aligned(w_o, 16) || !aligned(ffn_gain, 16) ||
+      !aligned(w_gate_up, 16) || !aligned(w_gate_up_scale, 4) || !aligned(w_down, 16) || !aligned(w_down_scale, 4) ||
+      !aligned(y_block, 16))
+    return DLLM_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < need) return DLLM_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return DLLM_ERR_INVALID_ARGUMENT;
+  FfnArgs a = {};
+  dllm_cache none = {};
+  none.num_pages = 1;
+  a.bt = batch_args(batch, &none);
+  a.o_full = o_full;
+  a.x_block = x_block;
+  a.gain2 = ffn_gain;
+  a.y = y_block;
+  a.n_rows = batch->total_block_rows;
+  a.d_model = desc->d_model;
+  a.hd = desc->n_heads * desc->head_dim;
+  a.d_ff = d_ff;
+  a.rms_eps = desc->rms_eps;
+  FfnWeights w;
+  w.w_o = w_o;
+  w.w_gu = w_gate_up;
+  w.gu_scale = w_gate_up_scale;
+  w.w_down = w_down;
+  w.down_scale = w_down_scale;
+  DLLM_CUDA_TRY(launch_ffn(a, w, ws, device_sms(), static_cast<cudaStream_t>(stream)));
+  return DLLM_OK;
+}
+
 const char* dllm_status_string(dllm_status status) {
   switch (status) {
     case DLLM_OK:

@@ -160,6 +160,42 @@ size_t lm_head_workspace_bytes(int n_rows, int d_model, int vocab);
 void lm_bind_workspace(LmArgs* a, void* ws);
 cudaError_t launch_lm_head(const void* w_lm, const LmArgs& a, int num_sms, cudaStream_t stream);
 
+// The rest of the layer for the block rows (ffn.cu): output projection + residual, AddNorm
+// with per-group e4m3 quantisation, the FP8 gate-up GEMM with SwiGLU and requantisation, the
+// FP8 down GEMM + residual.
+struct FfnArgs {
+  BatchArgs bt;
+  const void* o_full;   // bf16 [R][H d]: the attention output of every row
+  const void* x_block;  // bf16 [M][d_model]: the layer input of the block rows (first residual)
+  const void* gain2;    // bf16 [d_model]: the FFN's RMSNorm gain
+  void* y;              // bf16 [M][d_model]: the layer output of the block rows
+  void* o_block;        // workspace: bf16 [M][H d]
+  void* h1;             // workspace: bf16 [M][d_model]
+  void* x2;             // workspace: e4m3 [M][d_model]
+  float* x2_scale;      // workspace: [M][d_model / 128]
+  int32_t n_rows, d_model, hd, d_ff;
+  float rms_eps;
+};
+struct FfnWeights {
+  const void* w_o;         // bf16 [d_model][H d]
+  const void* w_gu;        // e4m3 [2 d_ff][d_model]: row 2j gate j, row 2j + 1 up j
+  const float* gu_scale;   // [2 d_ff / 128][d_model / 128]
+  const void* w_down;      // e4m3 [d_model][d_ff]
+  const float* down_scale; // [d_model / 128][d_ff / 128]
+};
+// One token-major GEMM of ffn.cu.
+struct DenseArgs {
+  int32_t M, N, K, splits;
+  const float* sa;   // e4m3 A: [M][K / 128] row group scales
+  const float* sb;   // e4m3 B: [N / 128][K / 128] block scales
+  float* part;       // [splits][M][N] fp32 partial sums
+  void* out8;        // SwiGLU: e4m3 [M][N / 2]
+  float* out_scale;  // SwiGLU: [M][N / 2 / 128]
+  int32_t* err;
+};
+size_t ffn_workspace_bytes(int n_rows, int d_model, int hd, int d_ff, int num_sms);
+cudaError_t launch_ffn(const FfnArgs& a, const FfnWeights& w, void* ws, int num_sms, cudaStream_t stream);
+
 // Attention of 128-row query tiles on the tensor cores (attn_rows.cu):
 //   kRowsState  every row of U over the keys of U: (m, l, O~) into the pools (the cache build)
 //   kRowsBlock  the block rows over every key: O and L (blocks of more than 64 rows)

@@ -46,7 +46,7 @@ PAGE = 64
 EXPORTS = ("dllm_workspace_size", "dllm_rope_table_build", "dllm_qkv_weight_packed_bytes", "dllm_qkv_weight_pack",
            "dllm_cache_build", "dllm_cache_advance", "dllm_block_qkv_rope_write", "dllm_block_qkv_rope_write_noalloc",
            "dllm_block_attention", "dllm_state_merge", "dllm_step_attention", "dllm_lm_head_workspace_size",
-           "dllm_block_lm_head", "dllm_status_string")
+           "dllm_block_lm_head", "dllm_ffn_workspace_size", "dllm_block_ffn", "dllm_status_string")
 
 
 class DllmError(RuntimeError):
@@ -110,6 +110,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                 "dllm_step_attention": [P(LayerDescC), P(BatchC), vp, P(CacheC), vp, vp, vp, sz, vp],
                 "dllm_lm_head_workspace_size": [P(LayerDescC), P(BatchC), i32, P(sz)],
                 "dllm_block_lm_head": [P(LayerDescC), P(BatchC), i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                "dllm_ffn_workspace_size": [P(LayerDescC), P(BatchC), i32, P(sz)],
+                "dllm_block_ffn": [P(LayerDescC), P(BatchC), i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             }
             for name, argt in sig.items():
                 fn = getattr(lib, name)
@@ -242,6 +244,21 @@ def dllm_block_lm_head(desc, batch, vocab, h_full, final_gain, w_lm, logits, lse
     _check("dllm_block_lm_head", load().dllm_block_lm_head(
         ctypes.byref(desc), ctypes.byref(batch), int(vocab), _ptr(h_full), _ptr(final_gain), _ptr(w_lm),
         _ptr(logits), _ptr(lse), _ptr(argmax), _ptr(p_max), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def dllm_ffn_workspace_size(desc, batch, d_ff: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("dllm_ffn_workspace_size", load().dllm_ffn_workspace_size(ctypes.byref(desc), ctypes.byref(batch),
+                                                                     int(d_ff), ctypes.byref(out)))
+    return int(out.value)
+
+
+def dllm_block_ffn(desc, batch, d_ff, o_full, x_block, w_o, ffn_gain, w_gate_up, w_gate_up_scale, w_down,
+                   w_down_scale, y_block, ws, stream=None):
+    _check("dllm_block_ffn", load().dllm_block_ffn(
+        ctypes.byref(desc), ctypes.byref(batch), int(d_ff), _ptr(o_full), _ptr(x_block), _ptr(w_o), _ptr(ffn_gain),
+        _ptr(w_gate_up), _ptr(w_gate_up_scale), _ptr(w_down), _ptr(w_down_scale), _ptr(y_block), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
 
 
 # ---------------------------------------------------- memory / structs ----

@@ -40,7 +40,7 @@ PAGE = 64
 
 # role ids folded into seeds
 (_R_WEIGHT, _R_PROMPT, _R_BLOCK, _R_MASK, _R_EMBED, _R_IDS_PROMPT, _R_IDS_BLOCK, _R_SHAPE, _R_PAGES,
- _R_SUFFIX, _R_HIDDEN, _R_LM) = range(1, 13)
+ _R_SUFFIX, _R_HIDDEN, _R_LM, _R_FFN) = range(1, 14)
 
 
 def splitmix64(x: int) -> int:
@@ -279,6 +279,39 @@ class Workload:
             g = 1.0 + gain_spread * (2 * u - 1)
         W = randn_bf16((vocab, c.d_model), derive_seed(c.seed, _R_LM, vocab), std=0.02)
         return h, g.to(torch.bfloat16), W
+
+    # ------------------------------------------------- rest of the layer (FFN)
+    def ffn_inputs(self, d_ff: int):
+        """Inputs of the rest of the layer for the current blocks' rows: o_full [R, H d]
+        bf16 ~ N(0, 0.25) (the attention output of every row), x_block [M, D] bf16 ~ N(0, 1)
+        (the layer input of the block rows, packed by cu_block), W_o [D, H d] ~ N(0, 0.02)
+        bf16, the FFN gain (ones), and the e4m3 weights: W_gate_up codes [2 d_ff, D] (rows
+        2j gate, 2j + 1 up) with fp32 scales [2 d_ff / 128, D / 128], W_down codes [D, d_ff]
+        with scales [D / 128, d_ff / 128].  Codes are random bytes: random sign, exponent
+        field uniform in 1..14 (no NaN code), mantissa uniform; scales uniform in
+        [1e-4, 3e-4]."""
+        c = self.cfg
+        R = sum(c.seq_len(b) for b in range(c.batch))
+        M = sum(c.c_len(b) for b in range(c.batch))
+        HD, D = c.n_heads * c.head_dim, c.d_model
+        o = randn_bf16((R, HD), derive_seed(c.seed, _R_FFN, 1), std=0.5)
+        x = randn_bf16((M, D), derive_seed(c.seed, _R_FFN, 2))
+        Wo = randn_bf16((D, HD), derive_seed(c.seed, _R_FFN, 3), std=0.02)
+        g2 = torch.ones(D, dtype=torch.bfloat16)
+
+        def codes(rows, cols, key):
+            gen = _gen(derive_seed(c.seed, _R_FFN, key))
+            sign = torch.randint(0, 2, (rows, cols), generator=gen, dtype=torch.int32)
+            expo = torch.randint(1, 15, (rows, cols), generator=gen, dtype=torch.int32)
+            mant = torch.randint(0, 8, (rows, cols), generator=gen, dtype=torch.int32)
+            return ((sign << 7) | (expo << 3) | mant).to(torch.uint8)
+
+        def scales(rows, cols, key):
+            return torch.empty(rows // 128, cols // 128).uniform_(1e-4, 3e-4,
+                                                                   generator=_gen(derive_seed(c.seed, _R_FFN, key)))
+
+        return dict(o_full=o, x_block=x, w_o=Wo, gain2=g2, w_gu=codes(2 * d_ff, D, 4), gu_scale=scales(2 * d_ff, D, 5),
+                    w_down=codes(D, d_ff, 6), down_scale=scales(D, d_ff, 7))
 
     # ---------------------------------------------------------------- layout
     def page_lists(self):

@@ -343,6 +343,35 @@ dllm_status dllm_block_lm_head(const dllm_layer_desc* desc, const dllm_batch* ba
                                const void* h_full, const void* final_gain, const void* w_lm, void* logits,
                                float* lse, int32_t* argmax, float* p_max, void* ws, size_t ws_bytes, void* stream);
 
+/* The rest of the layer for the current blocks' rows, with the FFN in
+ * per-group FP8 (LaCache §3.4 Mixed precision strategy, Eq. (7)-(8): a tensor
+ * split into groups g is quantised as x' = clip(x / scale_g, -448, 448),
+ * scale_g = max_g |x| / 448 (e4m3, round to nearest even), the quantisation
+ * fused into the AddNorm before the gate-up linear and into the SwiGLU
+ * before the down linear).  For the B_b rows of each current block
+ * (block row i of sequence b: attention output row cu_seq[b] + s_b + i):
+ *   h1 = x_block + O W_o^T                               (bf16 in, fp32 sum, bf16 h1)
+ *   x2 = RMSNorm(h1) ffn_gain, quantised per row and 128 columns
+ *   a  = SiLU(x2 W_gate^T) * (x2 W_up^T), quantised per row and 128 units
+ *   y_block = h1 + a W_down^T                           (bf16)
+ * where every e4m3 GEMM sums each group of 128 products in fp32 times the
+ * product of its two scales.  Layouts (row-major):
+ *   o_full:      bf16 [R][n_heads * head_dim] (dllm_block_attention's output)
+ *   x_block:     bf16 [M][d_model], packed by cu_block (the layer's input rows)
+ *   w_o:         bf16 [d_model][n_heads * head_dim]
+ *   ffn_gain:    bf16 [d_model]
+ *   w_gate_up:   e4m3 [2 d_ff][d_model]: row 2j is gate unit j, row 2j + 1 up unit j;
+ *   w_gate_up_scale: fp32 [2 d_ff / 128][d_model / 128], one scale per 128 x 128 block
+ *   w_down:      e4m3 [d_model][d_ff]; w_down_scale fp32 [d_model / 128][d_ff / 128]
+ *   y_block:     bf16 [M][d_model], packed by cu_block
+ * d_model and d_ff must be multiples of 128.
+ *   ws: dllm_ffn_workspace_size bytes. */
+dllm_status dllm_ffn_workspace_size(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t d_ff, size_t* bytes);
+dllm_status dllm_block_ffn(const dllm_layer_desc* desc, const dllm_batch* batch, int32_t d_ff, const void* o_full,
+                           const void* x_block, const void* w_o, const void* ffn_gain, const void* w_gate_up,
+                           const float* w_gate_up_scale, const void* w_down, const float* w_down_scale,
+                           void* y_block, void* ws, size_t ws_bytes, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* dllm_status_string(dllm_status status);
 

@@ -88,6 +88,11 @@ def _load():
                     None,
                 ),
                 "orc_softmax_stats": ([_D, _i64, _i64, _D, _I64, _D], None),
+                "orc_e4m3_decode": ([ctypes.c_int], _f64),
+                "orc_e4m3_round": ([_f64], _f64),
+                "orc_quant_groups": ([_D, _i64, _i64, _i64, _D, _D], None),
+                "orc_dequant_blocks": ([ctypes.c_void_p, _i64, _i64, _i64, _i64, ctypes.c_void_p, _D], None),
+                "orc_rmsnorm_f32": ([_D, _i64, _i64, _D, _f64, _D], None),
                 "orc_alg1": (
                     [_D, _D, _D, _i64, _i64, _i64, _f64, _i64, _i64, _i64, _i64, ctypes.c_int, _D, _D, _D, _D, _D],
                     None,
@@ -249,6 +254,64 @@ def lm_head(h, g, W_lm, eps: float, mirror: bool = True):
     z = linear(xh, W_lm)
     lse, am, pm = softmax_stats(z)
     return dict(logits=z, lse=lse, argmax=am, p_max=pm)
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().orc_e4m3_decode(int(code))
+
+
+def e4m3_round(x: float) -> float:
+    return _load().orc_e4m3_round(float(x))
+
+
+def quant_groups(x, group: int = 128):
+    """LaCache Eq. (7)-(8) per row and group of columns: (dequantised values, scales)."""
+    x = _c(x)
+    rows, cols = x.shape
+    deq = np.empty_like(x)
+    sc = np.empty((rows, cols // group))
+    _load().orc_quant_groups(_p(x), rows, cols, int(group), _p(deq), _p(sc))
+    return deq, sc
+
+
+def rmsnorm_f32(h, g, eps: float):
+    """RMSNorm(h) g as the quantisation's input, in fp32: 1 / rms correctly rounded to fp32,
+    then (h * inv) * g with fp32 products (returned as fp64 values)."""
+    h, g = _c(h), _c(g)
+    rows, D = h.shape
+    out = np.empty_like(h)
+    _load().orc_rmsnorm_f32(_p(h), rows, D, _p(g), float(eps), _p(out))
+    return out
+
+
+def dequant_blocks(codes, scales, block: int = 128):
+    """e4m3 codes [rows][cols] (uint8) times one fp32 scale per block x block."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols))
+    _load().orc_dequant_blocks(codes.ctypes.data, rows, cols, int(block), int(block), scales.ctypes.data, _p(out))
+    return out
+
+
+def ffn(o_rows, x_rows, W_o, g2, wgu_codes, wgu_scale, wd_codes, wd_scale, eps: float, mirror: bool = True):
+    """The rest of the layer for the given rows (LaCache §3.4 Mixed precision
+    strategy): h1 = x + O W_o^T (rounded to bf16: the residual stream's storage
+    point), x2 = RMSNorm(h1) g2 quantised per row and 128 columns (Eq. (7)-(8);
+    a quantised code is an integer decided by floating point, so x2 is formed in
+    the kernels' fp32 before the decision, see `rmsnorm_f32`), gate / up from the
+    e4m3 weights (rows 2j, 2j + 1), a = SiLU(gate) * up quantised the same way,
+    y = h1 + a W_down^T.  Returns dict(h1, y)."""
+    h1 = x_rows + linear(o_rows, W_o)
+    if mirror:
+        h1 = bf16_round(h1)
+    x2, _ = quant_groups(rmsnorm_f32(h1, g2, eps))
+    gu = linear(x2, dequant_blocks(wgu_codes, wgu_scale))
+    gate, up = gu[:, 0::2], gu[:, 1::2]
+    a = gate / (1.0 + np.exp(-gate)) * up
+    aq, _ = quant_groups(a)
+    y = h1 + linear(aq, dequant_blocks(wd_codes, wd_scale))
+    return dict(h1=h1, y=y)
 
 
 # ---------------------------------------------------------------- the step

@@ -353,4 +353,77 @@ void orc_softmax_stats(const double* z, int64_t rows, int64_t V, double* lse, in
   }
 }
 
+// ---- FP8 (e4m3) for the FFN's per-group quantisation (LaCache §3.4, Eq. (7)-(8)).
+// e4m3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0 holds the
+// subnormals m/8 * 2^-6; the largest finite magnitude is 1.75 * 2^8 = 448; no infinities.
+
+// The value of an e4m3 code (the two NaN codes give NaN).
+double orc_e4m3_decode(int code) {
+  const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+// Round to the nearest e4m3 value, ties to the even mantissa, magnitudes beyond 448
+// saturated to 448 (the clip of Eq. (7) with Q_max = 448).
+double orc_e4m3_round(double x) {
+  const double a = fabs(x);
+  if (a == 0.0) return x;
+  int e;
+  frexp(a, &e);       // a = f * 2^e, f in [0.5, 1)
+  int ex = e - 1;     // a in [2^ex, 2^(ex+1))
+  if (ex < -6) ex = -6;  // the subnormal spacing below 2^-6
+  const double step = ldexp(1.0, ex - 3);
+  double r = nearbyint(a / step) * step;  // the default rounding mode: to nearest even
+  if (r > 448.0) r = 448.0;
+  return x < 0 ? -r : r;
+}
+
+// Eq. (7)-(8) for rows of x [rows][cols] in groups of `group` columns: scale_g =
+// max_g |x| / 448 and q = e4m3(x / scale_g), each decision taken in fp32 (x rounded to
+// fp32 first, the division correctly rounded), as the kernels take it.  Writes the
+// dequantised values q * scale_g and the scales [rows][cols / group].
+void orc_quant_groups(const double* x, int64_t rows, int64_t cols, int64_t group, double* deq, double* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t g0 = 0; g0 < cols; g0 += group) {
+      float amax = 0.f;
+      for (int64_t c = g0; c < g0 + group; ++c) amax = fmaxf(amax, fabsf((float)x[r * cols + c]));
+      const float sc = amax / 448.f;
+      scales[r * (cols / group) + g0 / group] = sc;
+      for (int64_t c = g0; c < g0 + group; ++c) {
+        const float t = sc > 0.f ? (float)x[r * cols + c] / sc : 0.f;
+        deq[r * cols + c] = orc_e4m3_round((double)t) * (double)sc;
+      }
+    }
+  }
+}
+
+// The input of the AddNorm's quantisation, in the precision the quantisation decides in:
+// x2 = RMSNorm(h) g taken as the kernels take it in fp32, with 1 / rms correctly rounded to
+// fp32 (from the exact fp64 mean) and the two products rounded to fp32 in the order (h *
+// inv) * g.  Returns the fp32 values as doubles.
+void orc_rmsnorm_f32(const double* h, int64_t rows, int64_t D, const double* g, double eps, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t c = 0; c < D; ++c) ss += h[r * D + c] * h[r * D + c];
+    const float inv = (float)(1.0 / sqrt(ss / (double)D + eps));
+    for (int64_t c = 0; c < D; ++c) {
+      const float t = (float)h[r * D + c] * inv;
+      out[r * D + c] = (double)(t * (float)g[c]);
+    }
+  }
+}
+
+// Dequantise e4m3 codes [rows][cols] with one scale per block of br x bc: [rows / br][cols / bc].
+void orc_dequant_blocks(const uint8_t* codes, int64_t rows, int64_t cols, int64_t br, int64_t bc,
+                        const float* scales, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c)
+      out[r * cols + c] = orc_e4m3_decode(codes[r * cols + c]) * (double)scales[(r / br) * (cols / bc) + c / bc];
+}
+
 }  // extern "C"

@@ -37,6 +37,9 @@ MUTANTS = {
     "softmax_argmax_last_of_ties": ("      if (zr[v] > m) {\n        m = zr[v];\n        am = v;",
                                     "      if (zr[v] >= m) {\n        m = zr[v];\n        am = v;"),
     "softmax_lse_without_max": ("lse[r] = m + log(s);", "lse[r] = log(s);"),
+    "e4m3_ties_away": ("double r = nearbyint(a / step) * step;", "double r = round(a / step) * step;"),
+    "quant_scale_without_qmax": ("const float sc = amax / 448.f;", "const float sc = amax;"),
+    "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
 }
 
 

@@ -368,3 +368,108 @@ def test_lm_head_against_torch_composition():
     assert np.allclose(ref["lse"], torch.logsumexp(z, 1).numpy(), atol=1e-12)
     assert np.array_equal(ref["argmax"], z.argmax(1).numpy())
     assert np.allclose(ref["p_max"], torch.softmax(z, 1).max(1).values.numpy(), rtol=1e-12)
+
+
+# ------------------------------------------------ FP8 (e4m3) of the FFN (LaCache §3.4)
+def _golden_e4m3():
+    codes, rounds = [], []
+    for line in open(os.path.join(GOLDEN, "e4m3.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b = line.split()
+        (codes if a.startswith("0x") else rounds).append((a, float(b)))
+    return codes, rounds
+
+
+def test_e4m3_golden_values_and_library():
+    """Hand-derived codes and roundings (tests/golden/e4m3.txt), torch's
+    float8_e4m3fn for every finite code and for in-range rounding."""
+    import torch
+    codes, rounds = _golden_e4m3()
+    for c, v in codes:
+        assert orc.e4m3_decode(int(c, 16)) == v, c
+    for x, r in rounds:
+        assert orc.e4m3_round(float(x)) == r, x
+    all_codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = all_codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = orc.e4m3_decode(c)
+        if np.isnan(lib[c]):
+            assert np.isnan(v), c
+        else:
+            assert v == lib[c], c
+            assert orc.e4m3_round(v) == v  # every finite value rounds to itself
+    rng = np.random.default_rng(21)
+    xs = rng.uniform(-448, 448, size=4000) * np.exp(rng.uniform(-12, 0, size=4000))
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.array([orc.e4m3_round(x) for x in xs]), ref)
+
+
+def test_quant_groups_eq7_eq8():
+    """Eq. (7)-(8): the group max maps to +-448 exactly, every value within half
+    a step (2^-4 relative for the normal range) of its group's grid, a group of
+    zeros has scale 0, and a group of equal values comes back unchanged."""
+    rng = np.random.default_rng(22)
+    x = rng.normal(size=(5, 256)) * np.exp(rng.uniform(-3, 3, size=(5, 1)))
+    deq, sc = orc.quant_groups(x)
+    x32 = x.astype(np.float32).astype(np.float64)
+    for r in range(5):
+        for g in range(2):
+            blk, d = x32[r, 128 * g:128 * g + 128], deq[r, 128 * g:128 * g + 128]
+            s = np.float32(np.abs(blk).max()) / np.float32(448)
+            assert sc[r, g] == s
+            k = np.abs(blk).argmax()
+            assert abs(d[k]) == 448.0 * float(s)
+            big = np.abs(blk) > 2.0 ** -6 * s  # normal range of the codes
+            assert np.all(np.abs(d - blk)[big] <= np.abs(blk)[big] * 2.0 ** -4 * (1 + 1e-6))
+    z = np.zeros((1, 128))
+    dz, sz = orc.quant_groups(z)
+    assert sz[0, 0] == 0.0 and not dz.any()
+    e = np.full((1, 128), 0.37)
+    de, _ = orc.quant_groups(e)
+    assert np.allclose(de, np.float32(0.37), rtol=1e-6)
+
+
+def test_ffn_against_torch_composition():
+    """The FFN with per-group FP8 reproduced by torch: bf16 residual stream,
+    rms_norm, the fp32 quantisation decisions with torch's float8_e4m3fn cast,
+    dequantised block-scaled weights, SiLU."""
+    import torch
+    rng = np.random.default_rng(23)
+    M, D, HD, F = 3, 256, 128, 256
+    o = rng.normal(size=(M, HD))
+    x = rng.normal(size=(M, D))
+    Wo = rng.normal(scale=0.05, size=(D, HD))
+    g2 = rng.uniform(0.5, 1.5, size=D)
+    gu_codes = rng.integers(0, 256, size=(2 * F, D), dtype=np.uint8)
+    gu_codes[(gu_codes & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    gu_scale = rng.uniform(1e-4, 3e-4, size=(2 * F // 128, D // 128)).astype(np.float32)
+    d_codes = rng.integers(0, 256, size=(D, F), dtype=np.uint8)
+    d_codes[(d_codes & 0x7F) == 0x7F] = 0x38
+    d_scale = rng.uniform(1e-4, 3e-4, size=(D // 128, F // 128)).astype(np.float32)
+    ref = orc.ffn(o, x, Wo, g2, gu_codes, gu_scale, d_codes, d_scale, 1e-5)
+
+    def q(t):  # Eq. (7)-(8), decisions in fp32
+        t32 = t.to(torch.float32).reshape(t.shape[0], -1, 128)
+        s = t32.abs().amax(-1, keepdim=True) / 448.0
+        qq = torch.where(s > 0, t32 / s, torch.zeros_like(t32)).to(torch.float8_e4m3fn).to(torch.float64)
+        return (qq * s.to(torch.float64)).reshape(t.shape)
+
+    def deq(codes, scale):
+        v = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64)
+        s = torch.from_numpy(scale).to(torch.float64).repeat_interleave(128, 0).repeat_interleave(128, 1)
+        return v * s
+
+    h1 = (torch.from_numpy(x) + torch.from_numpy(o) @ torch.from_numpy(Wo).T).to(torch.bfloat16).to(torch.float64)
+    # the quantisation's input in fp32: 1 / rms rounded to fp32, then (h1 * inv) * g2 in fp32
+    inv = (1.0 / torch.sqrt(h1.pow(2).mean(1, keepdim=True) + 1e-5)).to(torch.float32)
+    x2 = q((h1.to(torch.float32) * inv) * torch.from_numpy(g2).to(torch.float32))
+    # and it is RMSNorm: the fp32 values are within fp32 rounding of torch's rms_norm
+    assert torch.allclose((h1.to(torch.float32) * inv * torch.from_numpy(g2).to(torch.float32)).double(),
+                          torch.nn.functional.rms_norm(h1, (D,), torch.from_numpy(g2), eps=1e-5), rtol=1e-6)
+    gu = x2 @ deq(gu_codes, gu_scale).T
+    a = q(torch.nn.functional.silu(gu[:, 0::2]) * gu[:, 1::2])
+    y = h1 + a @ deq(d_codes, d_scale).T
+    assert np.array_equal(ref["h1"], h1.numpy())
+    assert np.allclose(ref["y"], y.numpy(), rtol=1e-9, atol=1e-9)
