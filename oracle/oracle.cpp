@@ -409,7 +409,8 @@ void orc_rmsnorm_f32(const double* h, int64_t rows, int64_t D, const double* g, 
   for (int64_t r = 0; r < rows; ++r) {
     double ss = 0.0;
     for (int64_t c = 0; c < D; ++c) ss += h[r * D + c] * h[r * D + c];
-    const float inv = (float)(1.0 / sqrt(ss / (double)D + eps));
+    const double ms = ss / (double)D;  // the mean square
+    const float inv = (float)(1.0 / sqrt(ms + eps));
     for (int64_t c = 0; c < D; ++c) {
       const float t = (float)h[r * D + c] * inv;
       out[r * D + c] = (double)(t * (float)g[c]);

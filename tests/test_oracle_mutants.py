@@ -39,6 +39,8 @@ MUTANTS = {
     "softmax_lse_without_max": ("lse[r] = m + log(s);", "lse[r] = log(s);"),
     "e4m3_ties_away": ("double r = nearbyint(a / step) * step;", "double r = round(a / step) * step;"),
     "quant_scale_without_qmax": ("const float sc = amax / 448.f;", "const float sc = amax;"),
+    "rms_f32_no_eps": ("const float inv = (float)(1.0 / sqrt(ms + eps));",
+                       "const float inv = (float)(1.0 / sqrt(ms));"),
     "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
 }
 

@@ -473,3 +473,17 @@ def test_ffn_against_torch_composition():
     y = h1 + a @ deq(d_codes, d_scale).T
     assert np.array_equal(ref["h1"], h1.numpy())
     assert np.allclose(ref["y"], y.numpy(), rtol=1e-9, atol=1e-9)
+
+
+def test_rmsnorm_f32_is_rmsnorm_in_fp32():
+    """The quantisation's input (RMSNorm formed in fp32 as the kernels form it) is
+    torch's rms_norm up to fp32 rounding (three roundings: 2^-22 relative), for
+    rows whose mean square is comparable to eps (so eps counts)."""
+    import torch
+    rng = np.random.default_rng(24)
+    h = rng.normal(size=(6, 256)) * np.array([1.0, 1e-1, 1e-2, 3e-3, 1e-3, 10.0])[:, None]
+    g = rng.uniform(0.5, 1.5, size=256)
+    got = orc.rmsnorm_f32(h, g, 1e-5)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(h), (256,), torch.from_numpy(g), eps=1e-5).numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -22 * np.abs(ref) + 1e-30)
+    assert np.array_equal(got, got.astype(np.float32).astype(np.float64))  # fp32 values
