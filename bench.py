@@ -416,6 +416,7 @@ def measure(cfg, L, K, W, P, sample_every, dev, rank, ws, extras=True, e2e_steps
         if adv is not None:
             res["advance_ms"], res["advances"] = adv
         res["lm_head_ms"] = time_lm_head(cfg, items[0][0], dev, ws)
+        res["ffn_ms"] = time_ffn(cfg, items[0][0], dev, ws)
 
     if e2e_steps > 0:
         res["e2e"] = e2e(items, min(K, e2e_steps), W, ws)
@@ -508,6 +509,50 @@ def time_lm_head(cfg, st, dev, ws, reps: int = 10):
     assert st.batch.error_bits() == 0, "device-side error in the LM head"
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     del W, h
+    return _max_over_ranks(ms, ws)
+
+
+FFN_DFF = 12288  # the LLaDA-8B FFN width (the weights are synthetic)
+
+
+def time_ffn(cfg, st, dev, ws, reps: int = 10):
+    """Event-timed dllm_block_ffn (the rest of the layer for the block rows: output
+    projection + residual, AddNorm with e4m3 quantisation, FP8 gate-up with SwiGLU,
+    FP8 down + residual) with random e4m3 weights of the FFN_DFF-wide FFN."""
+    from block_wise_kv_gb300 import dllm
+
+    D, HD = cfg.d_model, cfg.n_heads * cfg.head_dim
+    R, M = st.batch.total_seq_rows, st.batch.total_block_rows
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    o = (torch.randn(R, HD, generator=g, device=dev) * 0.5).to(torch.bfloat16)
+    x = torch.randn(M, D, generator=g, device=dev).to(torch.bfloat16)
+    Wo = (torch.randn(D, HD, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    gain = torch.ones(D, dtype=torch.bfloat16, device=dev)
+
+    def codes(rows, cols):  # random e4m3 codes without the NaN pattern
+        c = torch.randint(0, 256, (rows, cols), generator=g, device=dev, dtype=torch.int32)
+        return torch.where((c & 0x7F) == 0x7F, c & 0x78, c).to(torch.uint8)
+
+    wgu, wd = codes(2 * FFN_DFF, D), codes(D, FFN_DFF)
+    sgu = torch.full((2 * FFN_DFF // 128, D // 128), 2e-4, device=dev)
+    sd = torch.full((D // 128, FFN_DFF // 128), 2e-4, device=dev)
+    y = torch.empty(M, D, dtype=torch.bfloat16, device=dev)
+    wsb = dllm.workspace(dllm.dllm_ffn_workspace_size(st.desc, st.batch.c, FFN_DFF), dev)
+    stream = torch.cuda.current_stream()
+    call = lambda: dllm.dllm_block_ffn(st.desc, st.batch.c, FFN_DFF, o, x, Wo, gain, wgu, sgu, wd, sd, y, wsb, stream)
+    call()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    assert st.batch.error_bits() == 0, "device-side error in the FFN"
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     return _max_over_ranks(ms, ws)
 
 
@@ -627,6 +672,22 @@ def summarize(res, hbm, tf_burst, ws, tf_sus=None):
                 f"dllm_block_lm_head (block rows only: gather + RMSNorm, tcgen05 LM head of {LM_VOCAB} entries with "
                 "the softmax summary in its epilogue, ordered merge)", lm_bytes, 2 * M * LM_VOCAB * D,
                 res["lm_head_ms"] * 1e-3, hbm, tf_burst, cfg.name, "lm_head")
+        if "ffn_ms" in res:
+            M, D, HD, F = int(st.batch.total_block_rows), cfg.d_model, cfg.n_heads * cfg.head_dim, FFN_DFF
+            fl_bf16, fl_fp8 = 2 * M * D * HD, 2 * M * 2 * F * D + 2 * M * D * F
+            by = D * HD * 2 + 2 * F * D + D * F + M * (HD + 2 * D) * 2  # weights, O rows, x, y
+            t = res["ffn_ms"] * 1e-3
+            t_tc = fl_bf16 / (tf_burst * 1e12) + fl_fp8 / (2 * tf_burst * 1e12)  # e4m3 at twice the bf16 rate
+            t_hbm = by / (hbm * 1e9)
+            bound = "tensor" if t_tc > t_hbm else "hbm"
+            out["block_ffn"] = {
+                "kernel": f"dllm_block_ffn (O-projection + residual, AddNorm + e4m3 quantisation, FP8 gate-up + "
+                          f"SwiGLU, FP8 down + residual; d_ff {F})",
+                "bound": bound, "duration_us": round(t * 1e6, 2), "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2),
+                "frac": round(max(t_tc, t_hbm) / t, 4), "algorithmic_flops": fl_bf16 + fl_fp8,
+                "algorithmic_bytes": by, "traffic": None,
+                "peak": f"bf16 {tf_burst} TFLOP/s (measured burst), e4m3 twice that (nominal ratio), "
+                        f"HBM {hbm} GB/s"}
         if "advance_ms" in res:
             out["cache_build_us"]["advance"] = {
                 "per_boundary": round(res["advance_ms"] * 1e3, 1),
@@ -702,6 +763,7 @@ def run_ours(args, rank, ws, local):
         "block_rows_only": head["block_rows_only"],
         "cache_build_us": head["cache_build_us"],
         "block_lm_head": head.get("block_lm_head"),
+        "block_ffn": head.get("block_ffn"),
         "roofline": {k: v for k, v in dominant.items()},
         "roofline_kernels": rk,
         "peak_source": f"{peak_kind} MEASURED_PEAKS hbm_gbs / bf16_tflops (burst: each kernel timed alone)",
