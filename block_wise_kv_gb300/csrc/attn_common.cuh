@@ -63,7 +63,8 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][4], uint32_t
 
 // One online-softmax step (LaCache Eq. (2)-(6)) of a warp's 16 rows with the
 // NK keys key0..key0+NK-1 of a K/V tile pair; key j takes part iff valid(j).
-template <int D, int NK, class Valid>
+// FRESH: st is the empty state (m = -inf, l = 0, O~ = 0), so nothing is rescaled.
+template <int D, int NK, bool FRESH = false, class Valid>
 __device__ __forceinline__ void attend(WarpAttn<D>& st, const uint32_t (&qf)[D / 16][4], uint32_t k_tile,
                                        uint32_t v_tile, int key0, float scale_log2, Valid valid, int lane) {
   float s[NK / 8][4];
@@ -99,9 +100,10 @@ __device__ __forceinline__ void attend(WarpAttn<D>& st, const uint32_t (&qf)[D /
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
   mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+  const float mn0 = FRESH ? mx0 : fmaxf(st.m[0], mx0), mn1 = FRESH ? mx1 : fmaxf(st.m[1], mx1);
   const float mu0 = mn0 == neg_inf() ? 0.f : mn0, mu1 = mn1 == neg_inf() ? 0.f : mn1;
-  const float a0 = fast_exp2(st.m[0] - mu0), a1 = fast_exp2(st.m[1] - mu1);  // Eq. (3); empty state -> 0
+  const float a0 = FRESH ? 0.f : fast_exp2(st.m[0] - mu0);  // Eq. (3); empty state -> 0
+  const float a1 = FRESH ? 0.f : fast_exp2(st.m[1] - mu1);
   st.m[0] = mn0;
   st.m[1] = mn1;
   float rs0 = 0.f, rs1 = 0.f;
@@ -114,14 +116,16 @@ __device__ __forceinline__ void attend(WarpAttn<D>& st, const uint32_t (&qf)[D /
     rs0 += s[n][0] + s[n][1];
     rs1 += s[n][2] + s[n][3];
   }
-  st.l[0] = st.l[0] * a0 + rs0;  // Eq. (5), per-thread partial
-  st.l[1] = st.l[1] * a1 + rs1;
+  st.l[0] = FRESH ? rs0 : st.l[0] * a0 + rs0;  // Eq. (5), per-thread partial
+  st.l[1] = FRESH ? rs1 : st.l[1] * a1 + rs1;
+  if (!FRESH) {
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {  // Eq. (6), first term
-    st.o[n][0] *= a0;
-    st.o[n][1] *= a0;
-    st.o[n][2] *= a1;
-    st.o[n][3] *= a1;
+    for (int n = 0; n < D / 8; ++n) {  // Eq. (6), first term
+      st.o[n][0] *= a0;
+      st.o[n][1] *= a0;
+      st.o[n][2] *= a1;
+      st.o[n][3] *= a1;
+    }
   }
   // Eq. (6), second term: O~ += P V
 #pragma unroll
@@ -135,8 +139,13 @@ __device__ __forceinline__ void attend(WarpAttn<D>& st, const uint32_t (&qf)[D /
       ldmatrix_x4_trans(b, v_tile + tile_off(key0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
                                              2 * dn + (lane >> 4)));
       const uint32_t b01[2] = {b[0], b[1]}, b23[2] = {b[2], b[3]};
-      mma_bf16_16816(st.o[2 * dn], pa, b01);
-      mma_bf16_16816(st.o[2 * dn + 1], pa, b23);
+      if (FRESH && kk == 0) {  // the first product over the empty state: C = 0
+        mma_bf16_16816_zc(st.o[2 * dn], pa, b01);
+        mma_bf16_16816_zc(st.o[2 * dn + 1], pa, b23);
+      } else {
+        mma_bf16_16816(st.o[2 * dn], pa, b01);
+        mma_bf16_16816(st.o[2 * dn + 1], pa, b23);
+      }
     }
   }
 }
@@ -220,7 +229,7 @@ inline cudaError_t encode_pool_maps(const AttnArgs& a, bool need_q, bool need_o,
   if (e == cudaSuccess && need_q)
     e = encode_2d_sw128(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q_pool, d, rows, 64, 64);
   if (e == cudaSuccess && need_o)
-    e = encode_2d_sw128(&m->o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.o_pool, d, rows, 32, 64);
+    e = encode_2d_sw128(&m->o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.o_pool, d, rows, 64, 64);
   return e;
 }
 

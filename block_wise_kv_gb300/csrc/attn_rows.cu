@@ -5,7 +5,7 @@
 //
 //   kRowsState     the FACache build of a block boundary: every row r of U
 //                  over the keys of U only, the online-softmax state
-//                  (m, l, O~) into m_pool / l_pool / o_pool (LaCache §3.3.3;
+//                  (m, l, O~ / l) into m_pool / l_pool / o_pool (LaCache §3.3.3;
 //                  Algorithm 1 with GenStep = True).
 //   kRowsBlock     the block attention of blocks longer than one page: the
 //                  block rows (from q_block) over every key of the sequence,
@@ -237,17 +237,23 @@ __device__ __forceinline__ void wait_or_abort(RowsShared& S, uint64_t* bar, uint
 }
 
 // Write row srow of the accumulator's state to the pools (mo, lo, oo): m in
-// natural units is the exact max m_true, l and O~ (O_t's row at o_row, when
-// have_o, else zero) taken from the reference max m_ref to m_true.  The O_t
-// row is read by the whole warp (tcgen05.ld), the pools only for row_out.
+// natural units is the exact max m_true, l is taken from the reference max
+// m_ref to m_true, and the state's O~ is kept normalised: oo = O~ / l (O_t's
+// row at o_row over the row's sum; zero when !have_o or l = 0), as fp16.  O~ / l
+// is a convex combination of value rows, so it stays within fp16's range unless
+// a value does; a row beyond it flags kErrRange.  The O_t row is read by the
+// whole warp (tcgen05.ld), the pools only for row_out.
 template <int D>
 __device__ __forceinline__ void store_state(uint32_t o_row, bool have_o, float m_ref, float m_true, float l,
-                                            float* mo_p, float* lo_p, float* oo_p, size_t srow, bool row_out) {
+                                            float* mo_p, float* lo_p, void* oo_p, size_t srow, bool row_out,
+                                            int* err) {
   const float c = (!have_o || m_ref == neg_inf()) ? 0.f : fast_exp2(m_ref - m_true);
+  const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;  // O~ / l: the rescale to m_true cancels
   if (row_out) {
     mo_p[srow] = m_true * kLn2;  // -inf stays -inf
     lo_p[srow] = l * c;
   }
+  float amax = 0.f;
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += 32) {
     float ov[32];
@@ -258,11 +264,29 @@ __device__ __forceinline__ void store_state(uint32_t o_row, bool have_o, float m
       for (int e = 0; e < 32; ++e) ov[e] = 0.f;
     }
     if (row_out) {
-      float4* dst = reinterpret_cast<float4*>(oo_p + srow * D + c0);
 #pragma unroll
-      for (int qq = 0; qq < 8; ++qq)
-        dst[qq] = make_float4(ov[4 * qq] * c, ov[4 * qq + 1] * c, ov[4 * qq + 2] * c, ov[4 * qq + 3] * c);
+      for (int e = 0; e < 32; ++e) {
+        ov[e] *= inv;
+        amax = fmaxf(amax, fabsf(ov[e]));
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(oo_p) + srow * D + c0);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        dst[qq] = make_uint4(pack_f16x2(ov[8 * qq], ov[8 * qq + 1]), pack_f16x2(ov[8 * qq + 2], ov[8 * qq + 3]),
+                             pack_f16x2(ov[8 * qq + 4], ov[8 * qq + 5]), pack_f16x2(ov[8 * qq + 6], ov[8 * qq + 7]));
     }
+  }
+  if (row_out && !(amax <= 65504.f)) report_error(err, kErrRange);
+}
+
+// Eight fp16 (one 16-byte load) to fp32 times k.
+__device__ __forceinline__ void f16x8_scaled(const uint4& u, float k, float* out) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    out[2 * i] = __low2float(h) * k;
+    out[2 * i + 1] = __high2float(h) * k;
   }
 }
 
@@ -528,23 +552,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool have = mi != neg_inf();
 #pragma unroll
-        for (int h0 = 0; h0 < D; h0 += 64) {  // two batches of loads in flight
-          float4 v[16];
+        for (int c0 = 0; c0 < D; c0 += 32) {  // O~ = l * (O~ / l), 32 columns at a time
+          float ov[32];
+          if (have) {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.o_pre) + srow * D + c0);
+            const uint4 u0 = src[0], u1 = src[1], u2 = src[2], u3 = src[3];
+            f16x8_scaled(u0, li, ov);
+            f16x8_scaled(u1, li, ov + 8);
+            f16x8_scaled(u2, li, ov + 16);
+            f16x8_scaled(u3, li, ov + 24);
+          } else {
 #pragma unroll
-          for (int qq = 0; qq < 16; ++qq)
-            v[qq] = have ? reinterpret_cast<const float4*>(a.o_pre + srow * D + h0)[qq] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            float ov[32];
-#pragma unroll
-            for (int qq = 0; qq < 8; ++qq) {
-              ov[4 * qq] = v[c0 / 4 + qq].x;
-              ov[4 * qq + 1] = v[c0 / 4 + qq].y;
-              ov[4 * qq + 2] = v[c0 / 4 + qq].z;
-              ov[4 * qq + 3] = v[c0 / 4 + qq].w;
-            }
-            tmem_st_32x32b_x32(o_row + h0 + c0, ov);
+            for (int e = 0; e < 32; ++e) ov[e] = 0.f;
           }
+          tmem_st_32x32b_x32(o_row + c0, ov);
         }
         tmem_st_wait();
         if (have) {
@@ -554,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (kPre && q.n1 == 0)  // no phase 1: an empty pre state
-        store_state<D>(o_row, false, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
+        store_state<D>(o_row, false, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out, bt.err);
       for (int i = 0; i < q.nk; ++i) {
         const int bsel = ns & 1;
         wait_or_abort(S, &S.sfull[t][bsel], (ns >> 1) & 1, bt.err);
@@ -608,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pw >= 1) wait_or_abort(S, &S.pfree[t], (pw - 1) & 1, bt.err);
         tc_fence_after();
         if (snap)  // O_t holds phase 1 (relative to the reference max before this page)
-          store_state<D>(o_row, true, s_mref, s_mtrue, s_l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
+          store_state<D>(o_row, true, s_mref, s_mtrue, s_l, a.m_pre, a.l_pre, a.o_pre, srow, row_out, bt.err);
         if (__any_sync(0xffffffffu, factor != 1.f)) {
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -640,15 +661,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_or_abort(S, &S.ofull[t], no & 1, bt.err);
       tc_fence_after();
       if (MODE == kRowsState || kPre) {
-        store_state<D>(o_row, true, m_ref, m_true, l, a.m_pool, a.l_pool, a.o_pool, srow, row_out);
+        store_state<D>(o_row, true, m_ref, m_true, l, a.m_pool, a.l_pool, a.o_pool, srow, row_out, bt.err);
         if (kPre && q.n2 == 0)  // phase 1 only: the pre state is the same
-          store_state<D>(o_row, true, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out);
+          store_state<D>(o_row, true, m_ref, m_true, l, a.m_pre, a.l_pre, a.o_pre, srow, row_out, bt.err);
       } else {
         // O = (w_c O~_c + w_f O_t) / L with the cached state (merge) or O_t / l (block rows)
-        float wc = 0.f, wf = 1.f, M = m_ref, L = l;
+        float wc = 0.f, wf = 1.f, M = m_ref, L = l, lc = 0.f;
         if (MODE == kRowsMerge && row_out) {
           const float mc = __ldg(a.m_pool + srow) * 1.4426950408889634f;  // base-2 units
-          const float lc = __ldg(a.l_pool + srow);
+          lc = __ldg(a.l_pool + srow);
           M = fmaxf(mc, m_ref);
           wc = mc == neg_inf() ? 0.f : fast_exp2(mc - M);
           wf = fast_exp2(m_ref - M);
@@ -657,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = row_out ? 1.f / L : 0.f;
         wc *= inv;
         wf *= inv;
+        const float wcl = wc * lc;  // the cached part's weight on O~_c / l_c
         const size_t orow = static_cast<size_t>(q.sm.cus + pos) * H + w.h;
         __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
 #pragma unroll 1
@@ -664,15 +686,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           float ov[32];
           tmem_ld_32x32b_x32(o_row + c0, ov);
           if (row_out) {
-            if (MODE == kRowsMerge) {
-              const float4* oc = reinterpret_cast<const float4*>(a.o_pool + srow * D + c0);
+            if (MODE == kRowsMerge) {  // wc l_c (O~_c / l_c) + wf O_t
+              const uint4* oc = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.o_pool) +
+                                                               srow * D + c0);
 #pragma unroll
-              for (int qq = 0; qq < 8; ++qq) {
-                const float4 v = __ldg(oc + qq);
-                ov[4 * qq] = wc * v.x + wf * ov[4 * qq];
-                ov[4 * qq + 1] = wc * v.y + wf * ov[4 * qq + 1];
-                ov[4 * qq + 2] = wc * v.z + wf * ov[4 * qq + 2];
-                ov[4 * qq + 3] = wc * v.w + wf * ov[4 * qq + 3];
+              for (int qq = 0; qq < 4; ++qq) {
+                float cv[8];
+                f16x8_scaled(__ldg(oc + qq), wcl, cv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ov[8 * qq + e] = cv[e] + wf * ov[8 * qq + e];
               }
             } else {
 #pragma unroll

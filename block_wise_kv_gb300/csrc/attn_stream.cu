@@ -28,6 +28,8 @@
 // stops waiting, flags DLLM_DEVERR_TIMEOUT and drains its own copies.
 #include <math.h>
 
+#include <algorithm>
+
 #include "attn_common.cuh"
 
 namespace dllm {
@@ -35,16 +37,17 @@ namespace {
 using namespace attn;
 
 constexpr int kThreads = 384;
-// Time of a merge-role page over that of a block-role page on GB300: measured over the
-// 32-layer stack, long-context and ragged workloads (attention time falls from the even
-// split to a minimum at 2.5 on all three: 275 -> 229, 259 -> 191, 1162 -> 870 us).
-constexpr double kMergePageCost = 2.5;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
+// Time of a merge-role page over that of a block-role page on GB300, fitted to sweeps of
+// the split over the 32-layer stack, long-context and ragged workloads with the fp16 O~ / l
+// state: at the best split of each, the block role's ceil(pairs / CTAs) pairs and the merge
+// role's share of pages take about equal time at 2.2-2.5 (attention 198, 178, 796 us).
+constexpr double kMergePageCost = 2.4;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
 constexpr int kMaxBatch = 512;
 
 template <int D>
 struct StreamCfg {
   static constexpr int TB = tile_bytes<D>();  // bf16 64 x D
-  static constexpr int OB = 64 * D * 4;       // fp32 O~ page
+  static constexpr int OB = 64 * D * 2;       // fp16 O~ / l page, laid out like a query tile
   // block role: K/V ring | 128-row query tile | two 128 x 64 score-probability tiles
   static constexpr int kKStages = 5;
   static constexpr int KStage = 2 * TB;
@@ -57,8 +60,8 @@ struct StreamCfg {
   static constexpr int PB = 128 * 128;
   static constexpr int kPOff = 8192;
   static constexpr int kBlockSmem = off_p + kPOff + PB;
-  // merge role: query page | O~ page | m | l ring, then the gathered block keys / values
-  static constexpr int kMStages = 3;
+  // merge role: query page | O~ / l page | m | l ring, then the gathered block keys / values
+  static constexpr int kMStages = 5;
   static constexpr int MStage = TB + OB + 1024;
   static constexpr int off_kc = kMStages * MStage;
   static constexpr int off_vc = off_kc + TB;
@@ -71,18 +74,19 @@ struct StreamCfg {
 };
 
 struct Shared {
-  // A ring stage alternates between the two consumer groups (pages go to the groups
-  // alternately), so each (group, stage) has its own "full" barrier: a waiter must see
-  // every phase of the barrier it waits on, since a parity wait cannot tell phase p from
-  // phase p + 2 (with one barrier per stage a group would skip the other group's phases
-  // and could take a stale stage whenever loads complete out of order).
-  uint64_t full[2][5], empty[5], qfull, qempty;
+  // A ring stage is shared by several consumer groups (pages go to the groups in turn),
+  // so each (group, stage) has its own "full" barrier: a waiter must see every phase of
+  // the barrier it waits on, since a parity wait cannot tell phase p from phase p + 2
+  // (with one barrier per stage a group would skip the other groups' phases and could
+  // take a stale stage whenever loads complete out of order).
+  uint64_t full[3][5], empty[5], qfull, qempty;  // full: [group][stage] (block role: groups 0-1)
   uint64_t sfull[2], sempty[2], pfull[2], pvdone[2], ofinal, oempty;  // block role: MMA <-> softmax warps
   uint32_t tmem_base;
   float xmax[2][2][4][32];  // block role: [group][page parity][warp of the group][lane] maxima over the warp's keys
   float xm[2][64];          // block role: [group][query row] reference max at the end of a (b, h)
   float xl[8][32];          // block role: [warp][lane] sum over the warp's keys at the end of a (b, h)
   int abort_flag;
+  int last_page[5];            // merge role: the last page issued into each stage (-1: none)
   int n_seq_units[kMaxBatch];  // H * pages of sequence b (0: invalid metadata)
   int cu[kMaxBatch + 1];       // unit prefix
 };
@@ -545,7 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     for (int s = 0; s < 5; ++s) {
       mbar_init(&S.full[0][s], 1);
       mbar_init(&S.full[1][s], 1);
-      mbar_init(&S.empty[s], block_role ? 2 : 4);  // block role: the Q K^T and P V completions; merge: 4 warps
+      mbar_init(&S.full[2][s], 1);
+      mbar_init(&S.empty[s], 2);  // block role: the Q K^T and P V completions
+      S.last_page[s] = -1;
     }
     mbar_init(&S.qfull, 1);
     mbar_init(&S.qempty, 2);  // block role: the Q K^T completions of a (b, h) (two issuers)
@@ -602,54 +608,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   w.seek(S, bt, H);
 
   // ===================================================================== merge role
+  // Three groups of four warps take the pages with invariant rows in turn, page j (in walk
+  // order) to group j % 3, through a ring of kMStages stages, page j in stage
+  // j % kMStages; (group, stage) barrier phase j / (3 kMStages) is page j.  The stage of
+  // page j is refilled with page j + kMStages by the leader of the group that consumed
+  // page j, once its four warps are done with it.  Within a stage, issue, landing and
+  // consumption therefore alternate: no barrier is armed again before its earlier phase
+  // completed, and a group waits for its next phase of a barrier only after the previous.
+  constexpr int NG = 3;
   uint8_t* ring = smem;
   uint8_t* kc_tile = smem + C::off_kc;
   uint8_t* vc_tile = smem + C::off_vc;
-  if (warp == 8) {
-    // ---------------------------------------------------- merge producer
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();  // the cached state is read once per step
-      int nm = 0;
-      for (; w.valid(); w.next(S, bt, H)) {
-        if (*reinterpret_cast<volatile int*>(&S.abort_flag)) break;
-        if (!w.has_u_rows()) continue;
-        const int s = nm % C::kMStages;
-        if (nm >= C::kMStages) wait_or_abort(S, &S.empty[s], (nm / C::kMStages - 1) & 1, bt.err);
-        const int y = (page_of(bt, w.b, w.p) * H + w.h) * kPage;
-        uint8_t* mt = ring + s * C::MStage;
-        uint64_t* fb = &S.full[nm & 1][s];  // page nm goes to group nm & 1
-        mbar_arrive_expect_tx(fb, TB + C::OB + 512);
-#pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + hf * 8192, &tm_q, fb, hf * 64, y, pol);
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) tma_load_2d_hint(mt + TB + j * 8192, &tm_o, fb, j * 32, y, pol);
-        bulk_load(mt + TB + C::OB, a.m_pool + y, 256, fb);
-        bulk_load(mt + TB + C::OB + 256, a.l_pool + y, 256, fb);
-        ++nm;
-      }
-      // every copy has landed: page i is phase i / (2 kMStages) of barrier (i & 1, i % kMStages)
-      for (int i = (nm > C::kMStages ? nm - C::kMStages : 0); i < nm; ++i)
-        if (!mbar_wait(&S.full[i & 1][i % C::kMStages], (i / (2 * C::kMStages)) & 1))
-          report_error(bt.err, kErrTimeout);
-    }
-    return;
-  }
-  if (warp >= 9) return;  // not used by the merge role
-  // ------------------------------------------------ merge compute (2 groups of 4 warps)
   const int grp = warp >> 2, mw = warp & 3;
-  const int g = lane >> 2, t = lane & 3;
+  const bool leader = mw == 0 && lane == 0;
+  const uint64_t pol = l2_evict_first_policy();  // the cached state is read once per step
+  auto next_u = [&](UWalk& x) {                  // the next page with invariant rows
+    do {
+      x.next(S, bt, H);
+    } while (x.valid() && !x.has_u_rows());
+  };
+  auto issue = [&](const UWalk& x, int j) {
+    const int s = j % C::kMStages;
+    const int y = (page_of(bt, x.b, x.p) * H + x.h) * kPage;
+    uint8_t* mt = ring + s * C::MStage;
+    uint64_t* fb = &S.full[j % NG][s];
+    S.last_page[s] = j;
+    mbar_arrive_expect_tx(fb, TB + C::OB + 512);
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + hf * 8192, &tm_q, fb, hf * 64, y, pol);
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) tma_load_2d_hint(mt + TB + hf * 8192, &tm_o, fb, hf * 64, y, pol);
+    bulk_load(mt + TB + C::OB, a.m_pool + y, 256, fb);
+    bulk_load(mt + TB + C::OB + 256, a.l_pool + y, 256, fb);
+  };
+  // The leaders' look-ahead walkers: the page each group issues next (page grp + kMStages,
+  // then every third page).  The first kMStages pages are issued here, before
+  // griddepcontrol.wait (the cached state is not written by the preceding kernel).
+  UWalk wa = w;
+  if (leader) {
+    if (!wa.has_u_rows()) next_u(wa);
+    for (int j = 0; j < C::kMStages + grp && wa.valid(); ++j) {
+      if (grp == 0) issue(wa, j);
+      next_u(wa);
+    }
+  }
   const float log2e = 1.4426950408889634f;
-  int nm = 0;  // pages with U rows seen so far (both groups count all of them)
+  int nm = 0;  // pages with invariant rows seen so far (every group counts all of them)
   int nkc = 32;
   __nv_bfloat16* of = static_cast<__nv_bfloat16*>(a.o_full);
   for (; w.valid(); w.next(S, bt, H)) {
     if (w.seg_start()) {  // gather the fresh block keys / values of (b, h) through the table
-      griddep_wait();         // they come from the preceding kernel (a no-op after the first time)
-      named_barrier(2, 256);  // both groups are done with the previous (b, h)'s
+      griddep_wait();               // they come from the preceding kernel (a no-op after the first time)
+      named_barrier(2, kThreads);   // every group is done with the previous (b, h)'s
       nkc = w.sm.bb <= 32 ? 32 : 64;  // keys the QK^T below covers; rows past bb are zero
       const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
       const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
-      for (int e = threadIdx.x; e < nkc * (D / 8); e += 256) {
+      for (int e = threadIdx.x; e < nkc * (D / 8); e += kThreads) {
         const int cc = e / (D / 8), ch = e % (D / 8);
         uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
         if (cc < w.sm.bb) {
@@ -662,15 +676,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
         *reinterpret_cast<uint4*>(kc_tile + tile_off(cc, ch)) = kv4;
         *reinterpret_cast<uint4*>(vc_tile + tile_off(cc, ch)) = vv4;
       }
-      named_barrier(2, 256);
+      named_barrier(2, kThreads);
     }
     if (!w.has_u_rows()) continue;
-    const int mine = (nm & 1) == grp;
-    const int s = nm % C::kMStages;
-    const int uses = nm / (2 * C::kMStages);  // earlier pages of this group in stage s
-    ++nm;
-    if (!mine) continue;  // the other group's page
-    wait_or_abort(S, &S.full[grp][s], uses & 1, bt.err);
+    const int j = nm++;
+    if (j % NG != grp) continue;  // another group's page
+    const int s = j % C::kMStages;
+    wait_or_abort(S, &S.full[grp][s], (j / (NG * C::kMStages)) & 1, bt.err);
     uint8_t* q_tile = ring + s * C::MStage;
     const uint8_t* o_tile = q_tile + TB;
     const float* m_s = reinterpret_cast<const float*>(q_tile + TB + C::OB);
@@ -684,30 +696,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     const int bb = w.sm.bb;
     auto valid = [bb](int key) { return key < bb; };
     if (nkc <= 32)
-      attend<D, 32>(st, qf, kt, vt, 0, a.scale_log2, valid, lane);
+      attend<D, 32, true>(st, qf, kt, vt, 0, a.scale_log2, valid, lane);
     else
-      attend<D, 64>(st, qf, kt, vt, 0, a.scale_log2, valid, lane);
+      attend<D, 64, true>(st, qf, kt, vt, 0, a.scale_log2, valid, lane);
     st.reduce_l();
-    // exact merge with the cached state, staged as bf16 rows in this warp's
-    // 16 rows of the q tile (read into registers above)
+    // exact merge with the cached state (O~_c = l_c times the stored O~_c / l_c), staged as
+    // bf16 rows in this warp's 16 rows of the q tile (read into registers above)
     const int r_lo = w.p * kPage, c_lo = w.sm.sb, c_hi = w.sm.sb + w.sm.bb;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      const int r = mw * 16 + g + 8 * hr;
+      const int r = mw * 16 + (lane >> 2) + 8 * hr;
       const float mc = m_s[r] * log2e;  // cached max, base-2 units
       const float mn = st.m[hr];
       const float M = fmaxf(mc, mn);
       const float wc = mc == neg_inf() ? 0.f : fast_exp2(mc - M);
       const float wn = mn == neg_inf() ? 0.f : fast_exp2(mn - M);
-      const float L = wc * l_s[r] + wn * st.l[hr];
+      const float lc = l_s[r];
+      const float L = wc * lc + wn * st.l[hr];
       const float inv = 1.f / L;
+      const float wcl = wc * lc * inv, wni = wn * inv;
+      const int t = lane & 3;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
         const int col = 8 * n + 2 * t;
-        const float2 oc = *reinterpret_cast<const float2*>(o_tile + (col >> 5) * 8192 +
-                                                           sw128_offset(r, (col & 31) >> 2) + (col & 3) * 4);
-        const float v0 = (wc * oc.x + wn * st.o[n][2 * hr]) * inv;
-        const float v1 = (wc * oc.y + wn * st.o[n][2 * hr + 1]) * inv;
+        const __half2 oc = *reinterpret_cast<const __half2*>(o_tile + tile_off(r, n) + (col & 7) * 2);
+        const float v0 = wcl * __low2float(oc) + wni * st.o[n][2 * hr];
+        const float v1 = wcl * __high2float(oc) + wni * st.o[n][2 * hr + 1];
         *reinterpret_cast<uint32_t*>(q_tile + tile_off(r, n) + (col & 7) * 2) = pack_bf16x2(v0, v1);
       }
       const int pos = r_lo + r;
@@ -722,9 +736,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       const uint4 v = *reinterpret_cast<const uint4*>(q_tile + tile_off(r, ch));
       *reinterpret_cast<uint4*>(of + (static_cast<size_t>(w.sm.cus + pos) * H + w.h) * D + ch * 8) = v;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
+    // the stage's generic reads and writes before the TMA that refills it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    named_barrier(3 + grp, 128);  // the group's four warps are done with stage s
+    if (leader && wa.valid() && !*reinterpret_cast<volatile int*>(&S.abort_flag)) {
+      issue(wa, j + C::kMStages);
+      for (int i = 0; i < NG && wa.valid(); ++i) next_u(wa);
+    }
   }
+  // every issued copy has landed before the CTA exits (they all have, unless a wait gave up)
+  named_barrier(2, kThreads);
+  if (threadIdx.x == 0)
+    for (int st = 0; st < C::kMStages; ++st) {
+      const int j = S.last_page[st];
+      if (j >= 0 && !mbar_wait(&S.full[j % NG][st], (j / (NG * C::kMStages)) & 1)) report_error(bt.err, kErrTimeout);
+    }
 }
 
 template <int D>
@@ -764,16 +790,26 @@ AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int ma
   const long long units = bh * max_pages;  // upper bound of the merge role's units
   const int g = static_cast<int>(units < num_sms ? (units < 1 ? 1 : units) : num_sms);
   if (block && merge) {
-    // Split the CTAs between the roles by their work: both walk every page of every
-    // (sequence, head) (the block role its keys, the merge role its invariant rows), and a
-    // merge page (query page, fp32 O~ page, row out) costs kMergePageCost block pages.
-    const double merge_frac =
-        total_seq_rows > 0 ? static_cast<double>(total_seq_rows - total_block_rows) / total_seq_rows : 0.0;
-    long long nb = llround(g / (1.0 + kMergePageCost * merge_frac));
-    if (nb < 1) nb = 1;
-    if (nb > g - 1) nb = g - 1 < 1 ? 1 : g - 1;
-    if (nb > bh) nb = bh;
-    p.n_block_ctas = static_cast<int>(nb);
+    // Split the CTAs between the roles by their work.  The block role walks every page of
+    // every (sequence, head) and owns whole pairs, so with nb CTAs its time is about
+    // ceil(pairs / nb) pairs of mean length; the merge role spreads the pages of the invariant
+    // rows evenly, a merge page (query page, fp16 O~ / l page, row out) costing
+    // kMergePageCost block pages.  Take the nb with the smallest larger of the two (in block
+    // pages x 64), the most merge CTAs among equals.
+    const double pair_rows = static_cast<double>(total_seq_rows) / batch;
+    const double merge_rows = static_cast<double>(total_seq_rows - total_block_rows) * n_heads;
+    const long long nb_max = std::min<long long>(bh, g - 1);
+    long long best_nb = 1;
+    double best = 0.0;
+    for (long long nb = 1; nb <= nb_max; ++nb) {
+      const double t = std::max(static_cast<double>((bh + nb - 1) / nb) * pair_rows,
+                                kMergePageCost * merge_rows / static_cast<double>(g - nb));
+      if (nb == 1 || t < best) {
+        best = t;
+        best_nb = nb;
+      }
+    }
+    p.n_block_ctas = static_cast<int>(best_nb);
     p.n_merge_ctas = g - p.n_block_ctas < 1 ? 1 : g - p.n_block_ctas;
   } else {
     p.n_block_ctas = block ? static_cast<int>(bh < num_sms ? bh : num_sms) : 0;

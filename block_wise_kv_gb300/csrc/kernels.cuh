@@ -105,7 +105,7 @@ struct AttnArgs {
   const void* q_pool;
   float* m_pool;        // fp32 [P][H][64]: written by the state build, read by the merge
   float* l_pool;
-  float* o_pool;        // fp32 [P][H][64][d]
+  void* o_pool;         // fp16 [P][H][64][d]: the state's O~ / l
   void* o_full;         // bf16 [R][H][d]
   float* lse;           // fp32 [R][H], nullable
   int32_t n_heads;
@@ -116,7 +116,7 @@ struct AttnArgs {
   // last began (device int32 [batch]; the new block starts where it ended)
   float* m_pre;
   float* l_pre;
-  float* o_pre;
+  void* o_pre;
   const int32_t* prev_start;
 };
 

@@ -32,6 +32,7 @@ DLLM_ERR_TIMEOUT = 5
 DLLM_DEVERR_TIMEOUT = 1
 DLLM_DEVERR_BAD_PAGE = 2
 DLLM_DEVERR_BAD_SHAPE = 4
+DLLM_DEVERR_RANGE = 8
 
 DLLM_OP_CACHE_BUILD = 0
 DLLM_OP_BLOCK_QKV_ROPE_WRITE = 1
@@ -339,12 +340,12 @@ class PagedCache:
         self.q = mk(shp, torch.bfloat16)
         self.m = mk(shp[:3], torch.float32)
         self.l = mk(shp[:3], torch.float32)
-        self.o = mk(shp, torch.float32)
+        self.o = mk(shp, torch.float16)  # the state's O~ / l
         self.num_pages = num_pages
         # the prefix state (for incremental boundaries), when asked for
         self.m_pre = mk(shp[:3], torch.float32) if pre else None
         self.l_pre = mk(shp[:3], torch.float32) if pre else None
-        self.o_pre = mk(shp, torch.float32) if pre else None
+        self.o_pre = mk(shp, torch.float16) if pre else None
         self.c = CacheC(_ptr(self.k), _ptr(self.v), _ptr(self.q), _ptr(self.m), _ptr(self.l), _ptr(self.o),
                         num_pages, _ptr(self.m_pre), _ptr(self.l_pre), _ptr(self.o_pre))
 

@@ -39,8 +39,9 @@
  *     failed validation the call returns a non-zero status and launches
  *     nothing.  A launch failure returns DLLM_ERR_CUDA.  Device-side checks
  *     (block-table entries outside [0, num_pages), per-sequence metadata that
- *     contradicts the host bounds, a bounded wait that ran out) skip the
- *     offending access and OR a DLLM_DEVERR_* bit into *batch->error_flag
+ *     contradicts the host bounds, a bounded wait that ran out, a cached state
+ *     beyond its storage range) skip the offending access and OR a
+ *     DLLM_DEVERR_* bit into *batch->error_flag
  *     when that pointer is non-NULL; outputs are then undefined.
  *   - Thread safety: calls on different streams are safe when their outputs
  *     do not overlap.
@@ -63,7 +64,7 @@
  *   page      = 64 consecutive token positions of one sequence.
  *   k_pool, v_pool, q_pool: bf16 [num_pages][n_heads][64][head_dim]
  *   m_pool, l_pool:         fp32 [num_pages][n_heads][64]
- *   o_pool:                 fp32 [num_pages][n_heads][64][head_dim]
+ *   o_pool:                 fp16 [num_pages][n_heads][64][head_dim] (the state's O~ / l)
  *   token at position p of sequence b lives at page block_table[b][p / 64],
  *   slot p % 64.
  *   w_qkv:   bf16 [3 * n_heads * head_dim][d_model]; rows are Q heads, then K
@@ -108,6 +109,7 @@ typedef enum dllm_status {
 #define DLLM_DEVERR_TIMEOUT 1   /* a bounded on-chip wait gave up */
 #define DLLM_DEVERR_BAD_PAGE 2  /* block_table entry outside [0, num_pages) */
 #define DLLM_DEVERR_BAD_SHAPE 4 /* seq_len/block_start/block_len/cu_* contradict the host bounds */
+#define DLLM_DEVERR_RANGE 8     /* a state's O~ / l beyond fp16 range (a value above 65504 in magnitude) */
 
 /* Shape of one attention layer. */
 typedef struct dllm_layer_desc {
@@ -127,15 +129,16 @@ typedef struct dllm_cache {
   void* q_pool;      /* bf16 [num_pages][H][64][d]: RoPE'd queries of U rows */
   float* m_pool;     /* fp32 [num_pages][H][64]: cached row max over U keys (natural units of scale*q.k) */
   float* l_pool;     /* fp32 [num_pages][H][64]: cached sum of exp(S - m) over U keys */
-  float* o_pool;     /* fp32 [num_pages][H][64][d]: cached unnormalised sum of exp(S - m) v over U keys */
+  void* o_pool;      /* fp16 [num_pages][H][64][d]: cached O~ / l, O~ = sum of exp(S - m) v over U keys
+                      * (the state is kept normalised: O~ = l * o_pool) */
   int32_t num_pages; /* pages in each pool; num_pages*H*64 < 2^31 */
   /* Optional (all NULL, or all set): the prefix state of each row, the same
-   * (m, l, O~) over only the keys before its sequence's current block, in the
-   * layouts of m_pool, l_pool, o_pool.  dllm_cache_build fills it when set;
+   * (m, l, O~ / l) over only the keys before its sequence's current block, in
+   * the layouts and types of m_pool, l_pool, o_pool.  dllm_cache_build fills it when set;
    * dllm_cache_advance needs it. */
   float* m_pre;
   float* l_pre;
-  float* o_pre;
+  void* o_pre;
 } dllm_cache;
 
 /* A ragged batch.  Host scalars bound the device arrays and size the grids. */
@@ -195,8 +198,8 @@ dllm_status dllm_qkv_weight_pack(const dllm_layer_desc* desc, const void* w_qkv,
  * online-softmax state over the keys of U_b only (LaCache §3.3.3):
  *   m = max_{j in U} S_rj, l = sum_{j in U} exp(S_rj - m),
  *   O~ = sum_{j in U} exp(S_rj - m) v_j,   S_rj = scale * q_r . k_j,
- * written to m_pool, l_pool, o_pool at row r's slot.  If U_b is empty for a
- * row's keys, m = -inf, l = 0, O~ = 0.  When the cache's prefix state pools
+ * written to m_pool, l_pool and (as O~ / l, rounded to fp16) o_pool at row r's
+ * slot.  If U_b is empty for a row's keys, m = -inf, l = 0, o_pool = 0.  When the cache's prefix state pools
  * are set, the same state over only the keys [0, s_b) is written there too
  * (what dllm_cache_advance extends).
  *   x_full: device bf16 [R][d_model]; rms_gain: device bf16 [d_model];
@@ -300,7 +303,8 @@ dllm_status dllm_block_attention(const dllm_layer_desc* desc, const dllm_batch* 
                                  void* stream);
 
 /* Inner step, part 3 (LaCache §3.3.3 and Algorithm 1 with GenStep = False):
- * for every row r of U_b and head h, start from the cached state (m, l, O~)
+ * for every row r of U_b and head h, start from the cached state (m, l,
+ * O~ = l o_pool)
  * of dllm_cache_build, stream only the B_b fresh block keys (read through
  * block_table at positions s_b .. s_b+B_b-1):
  *   m' = max_c S_rc, l' = sum_c exp(S_rc - m'), O' = sum_c exp(S_rc - m') v_c,
