@@ -169,14 +169,19 @@ __device__ __forceinline__ SeqMeta load_meta(const BatchArgs& bt, int b) {
   return m;
 }
 
-__device__ __forceinline__ int page_of(const BatchArgs& bt, int b, int p) {
-  int pg = __ldg(bt.block_table + static_cast<size_t>(b) * bt.max_pages + p);
+// A block-table entry in two steps, so that its load can be issued well before its use:
+// page_raw loads it, page_checked validates it.
+__device__ __forceinline__ int page_raw(const BatchArgs& bt, int b, int p) {
+  return __ldg(bt.block_table + static_cast<size_t>(b) * bt.max_pages + p);
+}
+__device__ __forceinline__ int page_checked(const BatchArgs& bt, int pg) {
   if (pg < 0 || pg >= bt.num_pages) {
     report_error(bt.err, kErrBadPage);
     pg = 0;  // load an in-bounds page; the result is flagged as invalid
   }
   return pg;
 }
+__device__ __forceinline__ int page_of(const BatchArgs& bt, int b, int p) { return page_checked(bt, page_raw(bt, b, p)); }
 
 template <int D>
 constexpr int tile_bytes() {

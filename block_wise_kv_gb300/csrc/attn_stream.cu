@@ -37,11 +37,13 @@ namespace {
 using namespace attn;
 
 constexpr int kThreads = 384;
-// Time of a merge-role page over that of a block-role page on GB300, fitted to sweeps of
-// the split over the 32-layer stack, long-context and ragged workloads with the fp16 O~ / l
-// state: at the best split of each, the block role's ceil(pairs / CTAs) pairs and the merge
-// role's share of pages take about equal time at 2.2-2.5 (attention 198, 178, 796 us).
-constexpr double kMergePageCost = 2.4;  // merge role: warps 0-7 compute, 8 streams; block role: see block_role_tc
+// Time of a merge-role page over that of a block-role page on GB300, for blocks of at most
+// 32 rows and for longer ones (the block role packs four 32-row query sets or two 64-row
+// ones into a tile; the merge attends to 32 or 64 keys), fitted to sweeps of the split:
+// 32-layer stack (blocks of 32) best over 1.6-1.8 (184 us), long-context (64) and ragged
+// (16-64) over 2.1-2.4 and at 2.3 (173, 746 us).
+constexpr double kMergePageCost32 = 1.7;
+constexpr double kMergePageCost64 = 2.3;
 constexpr int kMaxBatch = 512;
 
 template <int D>
@@ -262,10 +264,13 @@ __device__ __forceinline__ void block_role_tc(Shared& S, uint8_t* smem, const CU
                           sm.cub);
         }
         ++nq;
+        int raw_next = p < np ? page_raw(bt, b, p) : 0;  // loaded one page ahead of its use
         for (; p < np; ++p, ++nk) {
+          const int raw = raw_next;
+          if (p + 1 < np) raw_next = page_raw(bt, b, p + 1);
           const int s = nk % C::kKStages;
           if (nk >= C::kKStages) wait_or_abort(S, &S.empty[s], (nk / C::kKStages - 1) & 1, bt.err);
-          const int y = (page_of(bt, b, p) * H + h) * kPage;
+          const int y = (page_checked(bt, raw) * H + h) * kPage;
           uint8_t* kt = ring + s * C::KStage;
           uint64_t* fb = &S.full[p & 1][s];
           ++loads[(p & 1) * C::kKStages + s];
@@ -627,9 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       x.next(S, bt, H);
     } while (x.valid() && !x.has_u_rows());
   };
-  auto issue = [&](const UWalk& x, int j) {
+  auto issue = [&](const UWalk& x, int raw, int j) {  // raw: the page's block-table entry
     const int s = j % C::kMStages;
-    const int y = (page_of(bt, x.b, x.p) * H + x.h) * kPage;
+    const int y = (page_checked(bt, raw) * H + x.h) * kPage;
     uint8_t* mt = ring + s * C::MStage;
     uint64_t* fb = &S.full[j % NG][s];
     S.last_page[s] = j;
@@ -644,13 +649,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
   // The leaders' look-ahead walkers: the page each group issues next (page grp + kMStages,
   // then every third page).  The first kMStages pages are issued here, before
   // griddepcontrol.wait (the cached state is not written by the preceding kernel).
+  // Block-table entries are loaded ahead of their issue (all of the first kMStages at once,
+  // then each leader's next one right after its current issue).
   UWalk wa = w;
+  int wa_raw = 0;
   if (leader) {
     if (!wa.has_u_rows()) next_u(wa);
-    for (int j = 0; j < C::kMStages + grp && wa.valid(); ++j) {
-      if (grp == 0) issue(wa, j);
-      next_u(wa);
+    if (grp == 0) {
+      int raws[C::kMStages];
+      UWalk x = wa;
+#pragma unroll
+      for (int j = 0; j < C::kMStages; ++j) {
+        raws[j] = x.valid() ? page_raw(bt, x.b, x.p) : 0;
+        if (x.valid()) next_u(x);
+      }
+#pragma unroll
+      for (int j = 0; j < C::kMStages; ++j)
+        if (wa.valid()) {
+          issue(wa, raws[j], j);
+          next_u(wa);
+        }
+    } else {
+      for (int j = 0; j < C::kMStages + grp && wa.valid(); ++j) next_u(wa);
     }
+    if (wa.valid()) wa_raw = page_raw(bt, wa.b, wa.p);
   }
   const float log2e = 1.4426950408889634f;
   int nm = 0;  // pages with invariant rows seen so far (every group counts all of them)
@@ -700,9 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     else
       attend<D, 64, true>(st, qf, kt, vt, 0, a.scale_log2, valid, lane);
     st.reduce_l();
-    // exact merge with the cached state (O~_c = l_c times the stored O~_c / l_c), staged as
-    // bf16 rows in this warp's 16 rows of the q tile (read into registers above)
+    // exact merge with the cached state (O~_c = l_c times the stored O~_c / l_c): the weights
+    // of rows g and g + 8, then O~_c / l_c read in the accumulator layout (ldmatrix: rows g,
+    // g + 8 of the 8-column tiles 2kk, 2kk + 1) and the merged rows staged the same way
+    // (stmatrix) as bf16 in this warp's 16 rows of the q tile (read into registers above)
     const int r_lo = w.p * kPage, c_lo = w.sm.sb, c_hi = w.sm.sb + w.sm.bb;
+    float wcl[2], wni[2];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int r = mw * 16 + (lane >> 2) + 8 * hr;
@@ -714,19 +739,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
       const float lc = l_s[r];
       const float L = wc * lc + wn * st.l[hr];
       const float inv = 1.f / L;
-      const float wcl = wc * lc * inv, wni = wn * inv;
-      const int t = lane & 3;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const int col = 8 * n + 2 * t;
-        const __half2 oc = *reinterpret_cast<const __half2*>(o_tile + tile_off(r, n) + (col & 7) * 2);
-        const float v0 = wcl * __low2float(oc) + wni * st.o[n][2 * hr];
-        const float v1 = wcl * __high2float(oc) + wni * st.o[n][2 * hr + 1];
-        *reinterpret_cast<uint32_t*>(q_tile + tile_off(r, n) + (col & 7) * 2) = pack_bf16x2(v0, v1);
-      }
+      wcl[hr] = wc * lc * inv;
+      wni[hr] = wn * inv;
       const int pos = r_lo + r;
-      if (a.lse != nullptr && t == 0 && pos < w.sm.nb && (pos < c_lo || pos >= c_hi))
-        a.lse[static_cast<size_t>(w.sm.cus + pos) * H + w.h] = (M + log2f(L)) * kLn2;
+      if (a.lse != nullptr && (lane & 3) == 0 && pos < w.sm.nb && (pos < c_lo || pos >= c_hi))
+        a.lse[static_cast<size_t>(w.sm.cus + pos) * H + w.h] = (M + __log2f(L)) * kLn2;
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = tile_off(mw * 16 + (lane & 15), 2 * kk + (lane >> 4));
+      uint32_t oc[4], out[4];
+      ldmatrix_x4(oc, smem_u32(o_tile) + off);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const __half2 h2 = *reinterpret_cast<const __half2*>(&oc[2 * jj + hr]);
+          const float* on = st.o[2 * kk + jj];
+          out[2 * jj + hr] = pack_bf16x2(wcl[hr] * __low2float(h2) + wni[hr] * on[2 * hr],
+                                         wcl[hr] * __high2float(h2) + wni[hr] * on[2 * hr + 1]);
+        }
+      stmatrix_x4(smem_u32(q_tile) + off, out);
     }
     __syncwarp();
     for (int e = lane; e < 16 * (D / 8); e += 32) {  // coalesced store of this warp's 16 rows
@@ -740,8 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_stream_kernel(
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     named_barrier(3 + grp, 128);  // the group's four warps are done with stage s
     if (leader && wa.valid() && !*reinterpret_cast<volatile int*>(&S.abort_flag)) {
-      issue(wa, j + C::kMStages);
+      issue(wa, wa_raw, j + C::kMStages);
       for (int i = 0; i < NG && wa.valid(); ++i) next_u(wa);
+      if (wa.valid()) wa_raw = page_raw(bt, wa.b, wa.p);
     }
   }
   // every issued copy has landed before the CTA exits (they all have, unless a wait gave up)
@@ -783,7 +817,7 @@ cudaError_t launch_d(const AttnArgs& a, const AttnPlan& plan, cudaStream_t strea
 AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int max_block_len, int total_seq_rows,
                    int total_block_rows, int num_sms, bool block, bool merge) {
   (void)head_dim;
-  (void)max_block_len;
+  const double merge_cost = max_block_len <= 32 ? kMergePageCost32 : kMergePageCost64;
   AttnPlan p = {};
   const long long max_pages = (max_seq_len + kPage - 1) / kPage;
   const long long bh = static_cast<long long>(batch) * n_heads;
@@ -794,7 +828,7 @@ AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int ma
     // every (sequence, head) and owns whole pairs, so with nb CTAs its time is about
     // ceil(pairs / nb) pairs of mean length; the merge role spreads the pages of the invariant
     // rows evenly, a merge page (query page, fp16 O~ / l page, row out) costing
-    // kMergePageCost block pages.  Take the nb with the smallest larger of the two (in block
+    // merge_cost block pages.  Take the nb with the smallest larger of the two (in block
     // pages x 64), the most merge CTAs among equals.
     const double pair_rows = static_cast<double>(total_seq_rows) / batch;
     const double merge_rows = static_cast<double>(total_seq_rows - total_block_rows) * n_heads;
@@ -803,7 +837,7 @@ AttnPlan attn_plan(int batch, int n_heads, int head_dim, int max_seq_len, int ma
     double best = 0.0;
     for (long long nb = 1; nb <= nb_max; ++nb) {
       const double t = std::max(static_cast<double>((bh + nb - 1) / nb) * pair_rows,
-                                kMergePageCost * merge_rows / static_cast<double>(g - nb));
+                                merge_cost * merge_rows / static_cast<double>(g - nb));
       if (nb == 1 || t < best) {
         best = t;
         best_nb = nb;
