@@ -172,8 +172,8 @@ KERNEL_SOURCES = {
 TRAFFIC = {
     # (workload, kernel): (DRAM bytes per launch, sources hash); profiles/attn_stream_stack.md,
     # profiles/qkv_wide_stack.md
-    ("stack", "attention"): (1_176_540_672, "9801264b857656ca"),
-    ("stack", "qkv"): (135_720_960, "eac74e05f86e5bcb"),
+    ("stack", "attention"): (974_173_184, "ad373a2c3fa11099"),
+    ("stack", "qkv"): (131_670_016, "98dfacffcc8a6247"),
 }
 
 
