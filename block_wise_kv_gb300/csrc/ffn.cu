@@ -56,21 +56,28 @@ constexpr int kEpiSwiGLU = 1;   // SiLU(gate) * up of interleaved rows, quantise
 
 // ------------------------------------------------------------ gather
 // Block row j of the attention output: row cu_seq[b] + s_b + i of o_full.
-__global__ void __launch_bounds__(256) ffn_gather_kernel(const FfnArgs a) {
+// The sequence of block row j: the largest b with cu_block[b] <= j, found by the warp 32
+// sequences at a time (cu_block is increasing; every lane gets the same answer).
+__device__ __forceinline__ int warp_find_seq(const int32_t* cu, int batch, int j, int lane) {
+  int count = 0;
+  for (int b0 = 0; b0 < batch; b0 += 32) {
+    const int b = b0 + lane;
+    const unsigned le = __ballot_sync(0xffffffffu, b < batch && __ldg(cu + b) <= j);
+    count += __popc(le);
+    if (le != 0xffffffffu) break;
+  }
+  return count > 0 ? count - 1 : 0;
+}
+
+constexpr int kRowThreads = 128;  // the row kernels: four warps, one row each
+
+__global__ void __launch_bounds__(kRowThreads) ffn_gather_kernel(const FfnArgs a) {
   const int j = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   griddep_wait();
   griddep_launch_dependents();
   const BatchArgs& bt = a.bt;
   if (j >= a.n_rows) return;
-  int lo = 0, hi = bt.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(bt.cu_block + mid) <= j)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const int b = lo, off = j - __ldg(bt.cu_block + b);
+  const int b = warp_find_seq(bt.cu_block, bt.batch, j, lane), off = j - __ldg(bt.cu_block + b);
   const int nb = __ldg(bt.seq_len + b), sb = __ldg(bt.block_start + b), lb = __ldg(bt.block_len + b);
   const int cus = __ldg(bt.cu_seq + b);
   const int nvec = a.hd / 8;
@@ -83,23 +90,81 @@ __global__ void __launch_bounds__(256) ffn_gather_kernel(const FfnArgs a) {
     return;
   }
   const uint4* src = static_cast<const uint4*>(a.o_full) + static_cast<size_t>(cus + sb + off) * nvec;
-  for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+  for (int v0 = 0; v0 < nvec; v0 += 32 * 8) {  // eight 16-byte loads in flight a lane, then the stores
+    uint4 t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = v0 + lane + 32 * i;
+      if (v < nvec) t[i] = __ldg(src + v);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = v0 + lane + 32 * i;
+      if (v < nvec) dst[v] = t[i];
+    }
+  }
 }
 
 // ------------------------------------------------------------ AddNorm + quantisation
 // One warp per row of h1: x2 = RMSNorm(h1) g2 in fp32 (the exact sum of squares and scale of
 // the projection's RMSNorm), then per group of 128 columns scale = max |x2| / 448 and the e4m3
-// codes of x2 / scale (round to nearest even).
-__global__ void __launch_bounds__(256) ffn_addnorm_quant_kernel(const FfnArgs a) {
+// codes of x2 / scale (round to nearest even).  A lane holds the 16-byte pieces lane + 32 i of
+// the row, so a group of 128 columns is the 16 pieces of one half-warp in one round.
+constexpr int kRowPieces = 16;  // pieces a lane keeps in registers (rows up to 4096 wide)
+
+// Eight values of x2 (piece hu of h1, gain piece gu), their group's scale over the half-warp,
+// and their eight e4m3 codes; the lane at the start of the half writes the scale.
+__device__ __forceinline__ uint2 quant_piece(const uint4& hu, const uint4& gu, float inv, float* scale_out,
+                                             bool writes_scale) {
+  const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&hu);
+  const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gu);
+  float v[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 h = __bfloat1622float2(hp[i]), g = __bfloat1622float2(gp[i]);
+    v[2 * i] = h.x * inv * g.x;
+    v[2 * i + 1] = h.y * inv * g.y;
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = amax / kE4m3Max;  // Eq. (8)
+  if (writes_scale) *scale_out = sc;
+  uint32_t w[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {  // Eq. (7)
+    const int c = 4 * k;
+    const uint16_t p0 = sc > 0.f ? cvt_e4m3x2(__fdiv_rn(v[c], sc), __fdiv_rn(v[c + 1], sc)) : 0;
+    const uint16_t p1 = sc > 0.f ? cvt_e4m3x2(__fdiv_rn(v[c + 2], sc), __fdiv_rn(v[c + 3], sc)) : 0;
+    w[k] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+__global__ void __launch_bounds__(kRowThreads) ffn_addnorm_quant_kernel(const FfnArgs a) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   griddep_wait();
   griddep_launch_dependents();
   if (row >= a.n_rows) return;
   const int D = a.d_model, nvec = D / 8, ng = D / 128;
   const uint4* hr = static_cast<const uint4*>(a.h1) + static_cast<size_t>(row) * nvec;
-  float shi = 0.f, slo = 0.f;
-#pragma unroll 4
-  for (int v = lane; v < nvec; v += 32) sumsq_pair_add(hr[v], shi, slo);
+  const uint4* gr = static_cast<const uint4*>(a.gain2);
+  uint2* q = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.x2) + static_cast<size_t>(row) * D);
+  float* scales = a.x2_scale + static_cast<size_t>(row) * ng;
+  const bool held = nvec <= 32 * kRowPieces;
+  uint4 hv[kRowPieces];
+  float shi = 0.f, slo = 0.f;  // exact sum of squares as a float pair, pieces in order
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < kRowPieces; ++i)
+      if (lane + 32 * i < nvec) hv[i] = hr[lane + 32 * i];
+#pragma unroll
+    for (int i = 0; i < kRowPieces; ++i)
+      if (lane + 32 * i < nvec) sumsq_pair_add(hv[i], shi, slo);
+  } else {
+    for (int v = lane; v < nvec; v += 32) sumsq_pair_add(hr[v], shi, slo);
+  }
 #pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) {
     const float oh = __shfl_xor_sync(0xffffffffu, shi, o), ol = __shfl_xor_sync(0xffffffffu, slo, o);
@@ -111,31 +176,25 @@ __global__ void __launch_bounds__(256) ffn_addnorm_quant_kernel(const FfnArgs a)
     rsqrt_pair(shi, slo, D, a.rms_eps, y_hi, y_lo);
   }
   const float inv = __shfl_sync(0xffffffffu, y_hi, 0) + __shfl_sync(0xffffffffu, y_lo, 0);
-  const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.h1) + static_cast<size_t>(row) * D;
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(a.gain2);
-  uint8_t* q = static_cast<uint8_t*>(a.x2) + static_cast<size_t>(row) * D;
-  for (int gi = lane; gi < ng; gi += 32) {  // one lane per group of 128 columns
-    float v[128];
-    float amax = 0.f;
+  // nvec is a multiple of 16, so a half-warp's 16 pieces are all in the row or all past it
+  const bool first_of_group = (lane & 15) == 0;
+  if (held) {
 #pragma unroll
-    for (int c = 0; c < 128; ++c) {
-      v[c] = __bfloat162float(h[gi * 128 + c]) * inv * __bfloat162float(g[gi * 128 + c]);
-      amax = fmaxf(amax, fabsf(v[c]));
+    for (int i = 0; i < kRowPieces; ++i) {
+      if (32 * i >= nvec) break;
+      const int v = lane + 32 * i;
+      const bool on = v < nvec;
+      const uint2 c = quant_piece(on ? hv[i] : make_uint4(0u, 0u, 0u, 0u), on ? __ldg(gr + v) : make_uint4(0u, 0u, 0u, 0u),
+                                  inv, scales + (v >> 4), on && first_of_group);
+      if (on) q[v] = c;
     }
-    const float sc = amax / kE4m3Max;  // Eq. (8)
-    a.x2_scale[static_cast<size_t>(row) * ng + gi] = sc;
-    uint4* dst = reinterpret_cast<uint4*>(q + gi * 128);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {  // Eq. (7): 16 codes per 16-byte store
-      uint32_t w[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = 16 * e + 4 * k;
-        const uint16_t p0 = sc > 0.f ? cvt_e4m3x2(__fdiv_rn(v[c], sc), __fdiv_rn(v[c + 1], sc)) : 0;
-        const uint16_t p1 = sc > 0.f ? cvt_e4m3x2(__fdiv_rn(v[c + 2], sc), __fdiv_rn(v[c + 3], sc)) : 0;
-        w[k] = static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16);
-      }
-      dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    for (int v0 = 0; v0 < nvec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool on = v < nvec;
+      const uint2 c = quant_piece(on ? hr[v] : make_uint4(0u, 0u, 0u, 0u), on ? __ldg(gr + v) : make_uint4(0u, 0u, 0u, 0u),
+                                  inv, scales + (v >> 4), on && first_of_group);
+      if (on) q[v] = c;
     }
   }
 }
@@ -301,10 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mt * kTM + rt;
       const int nblk = nt * 2 + half;   // the weight block (128 rows) of this thread
       const bool row_ok = row < g.M, blk_ok = nblk * 128 < g.N;
+      // The chunk's dequantisation f = row group scale x weight block scale; the pair is
+      // loaded a chunk ahead of its use (its latency would otherwise stall every chunk).
+      auto ld_sa = [&](int ck) { return row_ok && ck < c1 ? g.sa[static_cast<size_t>(row) * nkg + ck] : 0.f; };
+      auto ld_sb = [&](int ck) { return blk_ok && ck < c1 ? g.sb[static_cast<size_t>(nblk) * nkg + ck] : 0.f; };
+      float sa0 = 1.f, sb0 = 1.f;
+      if (FP8) sa0 = ld_sa(c0), sb0 = ld_sb(c0);
       for (int ck = c0; ck < c1; ++ck, ++nc) {
-        float f = 1.f;  // the chunk's dequantisation: row group scale x weight block scale
-        if (FP8) f = (row_ok ? g.sa[static_cast<size_t>(row) * nkg + ck] : 0.f) *
-                     (blk_ok ? g.sb[static_cast<size_t>(nblk) * nkg + ck] : 0.f);
+        float sa1 = 1.f, sb1 = 1.f;
+        if (FP8) sa1 = ld_sa(ck + 1), sb1 = ld_sb(ck + 1);
+        const float f = FP8 ? sa0 * sb0 : 1.f;
         const int b = nc & 1;
         if (ok && !mbar_wait(&tfull_bar[b], (nc >> 1) & 1)) {
           report_error(g.err, kErrTimeout);
@@ -321,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty_bar[b]);
+        sa0 = sa1, sb0 = sb1;
       }
       const int n0 = nblk * 128;
       if (EPI == kEpiPartial) {
@@ -507,9 +573,9 @@ cudaError_t launch_ffn(const FfnArgs& a0, const FfnWeights& w, void* ws, int num
   float* part = reinterpret_cast<float*>(base + p.part);
   uint8_t* a8 = base + p.a8;
   float* as = reinterpret_cast<float*>(base + p.as);
-  const int warp_blocks = (M * 32 + 255) / 256;
+  const int warp_blocks = (M * 32 + kRowThreads - 1) / kRowThreads;  // a warp per row
   // the block rows of the attention output
-  cudaError_t e = launch_ex(ffn_gather_kernel, warp_blocks, 256, 0, stream, a);
+  cudaError_t e = launch_ex(ffn_gather_kernel, warp_blocks, kRowThreads, 0, stream, a);
   if (e != cudaSuccess) return e;
   // h1 = x + O W_o^T
   DenseArgs g = {M, D, HD, p.s_o, nullptr, nullptr, part, nullptr, nullptr, a.bt.err};
@@ -517,7 +583,7 @@ cudaError_t launch_ffn(const FfnArgs& a0, const FfnWeights& w, void* ws, int num
   if (e == cudaSuccess) e = launch_reduce(g, a.x_block, a.h1, stream);
   if (e != cudaSuccess) return e;
   // x2 = quant(RMSNorm(h1) g2)
-  e = launch_ex(ffn_addnorm_quant_kernel, warp_blocks, 256, 0, stream, a);
+  e = launch_ex(ffn_addnorm_quant_kernel, warp_blocks, kRowThreads, 0, stream, a);
   if (e != cudaSuccess) return e;
   // a = quant(SiLU(gate) * up)
   DenseArgs gu = {M, 2 * F, D, 1, a.x2_scale, w.gu_scale, nullptr, a8, as, a.bt.err};
