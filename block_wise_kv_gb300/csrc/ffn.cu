@@ -377,11 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int cq = 0; cq < kColsPerThread; cq += 32) {
-          float v[32];
-          tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(b * kTN + half * kColsPerThread + cq), v);
+        for (int cq = 0; cq < kColsPerThread; cq += 64) {  // two TMEM loads in flight per wait
+          float v[64];
+          tmem_ld_32x32b_x64(lane_base + static_cast<uint32_t>(b * kTN + half * kColsPerThread + cq), v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[cq + i] = fmaf(v[i], f, acc[cq + i]);
+          for (int i = 0; i < 64; ++i) acc[cq + i] = fmaf(v[i], f, acc[cq + i]);
         }
         tc_fence_before();
         __syncwarp();

@@ -424,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < kColsPerThread; c0 += 32)
-        tmem_ld_add_32(lane_base + static_cast<uint32_t>(b * kTN + half * kColsPerThread + c0), acc + c0);
+      for (int c0 = 0; c0 < kColsPerThread; c0 += 64)
+        tmem_ld_add_64(lane_base + static_cast<uint32_t>(b * kTN + half * kColsPerThread + c0), acc + c0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[b]);

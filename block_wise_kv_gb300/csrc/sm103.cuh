@@ -336,6 +336,15 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, float (&v)[64
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Accumulate 64 consecutive TMEM columns of this thread's lane into acc[0..63] (two loads
+// in flight, one wait).
+__device__ __forceinline__ void tmem_ld_add_64(uint32_t taddr, float* acc) {
+  float v[64];
+  tmem_ld_32x32b_x64(taddr, v);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) acc[i] += v[i];
+}
+
 // Accumulate 32 consecutive TMEM columns of this thread's lane into acc[0..31].
 __device__ __forceinline__ void tmem_ld_add_32(uint32_t taddr, float* acc) {
   float v[32];
