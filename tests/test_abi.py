@@ -30,6 +30,34 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def _header_constants():
+    """Every status code (enum) and #define of include/dllm.h with its value."""
+    src = open(os.path.join(ROOT, "include", "dllm.h")).read()
+    consts = {n: int(v) for n, v in re.findall(r"^\s*(DLLM_\w+)\s*=\s*(\d+)", src, re.M)}
+    consts.update({n: int(v) for n, v in re.findall(r"^#define\s+(DLLM_\w+)\s+(\d+)", src, re.M)})
+    return consts
+
+
+def test_binding_constants_match_the_header():
+    consts = _header_constants()
+    assert {"DLLM_OK", "DLLM_DEVERR_RANGE", "DLLM_OP_CACHE_ADVANCE"} <= set(consts)
+    for name, value in consts.items():
+        assert getattr(dllm, name) == value, name
+
+
+def test_device_error_bits_match_the_header():
+    """The kernels OR their own error codes into the caller's word: they are the
+    header's DLLM_DEVERR_* bits."""
+    src = open(os.path.join(ROOT, "block_wise_kv_gb300", "csrc", "sm103.cuh")).read()
+    dev = {n: int(v) for n, v in re.findall(r"^\s*(kErr\w+)\s*=\s*(\d+)", src, re.M)}
+    hdr = _header_constants()
+    pairs = {"kErrTimeout": "DLLM_DEVERR_TIMEOUT", "kErrBadPage": "DLLM_DEVERR_BAD_PAGE",
+             "kErrBadShape": "DLLM_DEVERR_BAD_SHAPE", "kErrRange": "DLLM_DEVERR_RANGE"}
+    assert set(dev) == set(pairs)
+    for k, h in pairs.items():
+        assert dev[k] == hdr[h], (k, h)
+
+
 def _desc(**kw):
     d = dict(d_model=4096, n_heads=32, head_dim=128, rope_theta=5e5)
     d.update(kw)
