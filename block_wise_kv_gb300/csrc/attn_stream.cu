@@ -15,11 +15,14 @@
 //                pages of every sequence: the rows of U in page p, the cached
 //                state (m, l, O~) merged with the fresh partial state over
 //                the block keys (LaCache §3.3.3, Algorithm 1 with GenStep =
-//                False), on mma.sync m16n8k16 (bf16 in, fp32 accumulate); two
-//                groups of 4 warps take alternate pages.
-// At most half of the CTAs (and at most one per (b, h)) take the block role.
-// In both roles one warp streams tiles with TMA (128-byte swizzle) into an
-// mbarrier ring that runs ahead across pages and (b, h) boundaries.
+//                False), on mma.sync m16n8k16 (bf16 in, fp32 accumulate); three
+//                groups of 4 warps take the pages in turn.  The cached O~ is
+//                stored as O~ / l in fp16.
+// The host splits the CTAs between the roles by their work (attn_plan); a
+// (b, h) pair is never split between block-role CTAs.  The tiles are streamed
+// with TMA (128-byte swizzle) into mbarrier rings that run ahead across pages
+// and (b, h) boundaries: by a producer warp in the block role, by the leader
+// of the consuming group (refilling the stage it just freed) in the merge role.
 //
 // Programmatic dependent launch: barrier setup, the metadata prefix and the
 // loads of data the preceding kernel does not write (pages without block
