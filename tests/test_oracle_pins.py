@@ -238,6 +238,26 @@ def test_cached_state_is_online_state_over_U_keys():
     np.testing.assert_allclose(Ot, np.einsum("rhk,khd->rhd", P, v[U]), rtol=1e-11, atol=1e-12)
 
 
+def test_normalised_state_is_a_convex_combination_of_values():
+    """O~ / l of a state is a softmax-weighted average of the value rows of its keys: every
+    column lies between that column's smallest and largest value over U, so it is finite in
+    any format that holds the values (the cached state is stored as O~ / l); with a single
+    key in U it is that key's value row, whatever the query."""
+    g = _rng(33)
+    N, H, d, c_lo, c_hi = 36, 3, 8, 5, 31
+    q, k, v = _qkv(g, N, H, d)
+    q *= 4.0  # peaked weights: the average sits close to single values
+    U = np.r_[0:c_lo, c_hi:N]
+    m, l, Ot = orc.state_build(q[U], k, v, 0.5, c_lo, c_hi, 4)
+    o = Ot / l[..., None]
+    lo, hi = v[U].min(axis=0), v[U].max(axis=0)  # [H, d] over the keys of U
+    assert np.all(o >= lo[None] - 1e-12) and np.all(o <= hi[None] + 1e-12)
+    # one key outside C (C = every row but row 0): the state's O~ / l is v[0] for every row
+    m1, l1, O1 = orc.state_build(q[:1], k, v, 0.5, 1, N, 4)
+    np.testing.assert_allclose(O1 / l1[..., None], np.broadcast_to(v[0], O1.shape), rtol=1e-14)
+    np.testing.assert_allclose(l1, 1.0, rtol=1e-14)
+
+
 def test_merge_invariant_to_reference_max_and_empty_state():
     g = _rng(31)
     N, H, d, c_lo, c_hi = 30, 2, 8, 8, 16
