@@ -173,8 +173,8 @@ KERNEL_SOURCES = {
 TRAFFIC = {
     # (workload, kernel): (DRAM bytes per launch, sources hash); profiles/attn_stream_stack.md,
     # profiles/qkv_wide_stack.md (the DRAM-only capture listed there)
-    ("stack", "attention"): (969_533_696, "47432f11b3637cc5"),
-    ("stack", "qkv"): (134_254_848, "e1d92f88d79d4f44"),
+    ("stack", "attention"): (969_189_632, "47432f11b3637cc5"),
+    ("stack", "qkv"): (135_171_584, "042ebfe49b5f9368"),
 }
 
 

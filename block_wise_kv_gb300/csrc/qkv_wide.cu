@@ -489,13 +489,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kStagingCols; ++i) staging[i * kTM + row] = acc[pc * kStagingCols + i];
         }
+        const int c = at >> 3, jc = at & 7;  // column of the pass, 8-element chunk of the tile's low halves
+        const int col = ph * kColsPerThread + pc * kStagingCols + c;
+        const int hit = jc / chunks_per_half, t0 = (jc % chunks_per_half) * 8;
+        // the (cos, sin) of this thread's 8 pairs depend on the column's position only: loaded
+        // before the barrier, so that their latency overlaps it
+        float4 rope[4];
+        if (which != 2) {
+          const float4* tab =
+              reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[col]) * half_d + t0) * 2);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) rope[e] = __ldg(tab + e);
+        }
         named_barrier(1, kAcc);
         {
-          const int c = at >> 3, jc = at & 7;  // column of the pass, 8-element chunk of the tile's low halves
-          const int col = ph * kColsPerThread + pc * kStagingCols + c;
           const long long kv = tok_kv[col];
           if (kv >= 0) {
-            const int hit = jc / chunks_per_half, t0 = (jc % chunks_per_half) * 8;
             const int row_lo = hit * d + t0, row_hi = row_lo + half_d;
             const float* r = staging + c * kTM;
             float lo[8], hi[8];
@@ -517,11 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (which == 2) {
               out = vpool + kv + static_cast<long long>(head) * kPage * d;
             } else {
-              const float4* tab =
-                  reinterpret_cast<const float4*>(a.rope + (static_cast<size_t>(tok_pos[col]) * half_d + t0) * 2);
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
-                const float4 v = __ldg(tab + e / 2);  // (cos, sin) of t0+e and t0+e+1
+                const float4 v = rope[e / 2];  // (cos, sin) of t0+e and t0+e+1
                 const float l0 = lo[e] * v.x - hi[e] * v.y, h0 = hi[e] * v.x + lo[e] * v.y;
                 const float l1 = lo[e + 1] * v.z - hi[e + 1] * v.w, h1 = hi[e + 1] * v.z + lo[e + 1] * v.w;
                 lo[e] = l0;
