@@ -212,7 +212,7 @@ def step_bytes_flops(cfg, st):
     qkv_flops = 6 * M * D * HD
     att_bytes = int((N * HD * 4).sum()) + 2 * M * HD * 2
     att_flops = int((4 * B * N * HD).sum())
-    mrg_bytes = int((NU * HD * 6).sum()) + int(NU.sum()) * H * 8  # q, O~/l, out (bf16); m, l (fp32)
+    mrg_bytes = int((NU * HD * 6).sum()) + int(NU.sum()) * H * 8  # q, out (bf16), O~/l (fp16); m, l (fp32)
     mrg_flops = int((4 * NU * B * HD).sum())
     return dict(qkv=(qkv_bytes, qkv_flops), attention=(att_bytes, att_flops), merge=(mrg_bytes, mrg_flops))
 
