@@ -234,7 +234,8 @@ dllm_status dllm_cache_build(const dllm_layer_desc* desc, const dllm_batch* batc
  *               over [0, s_b') (the decoded rows);
  *   state'(r) = pre'(r) merged with r's partial state over [s_b' + B_b', N_b)
  * written to m_pre/l_pre/o_pre and m_pool/l_pool/o_pool.  The result equals
- * dllm_cache_build on the same rows up to the rounding order of the sums.
+ * dllm_cache_build on the same rows up to the rounding order of the sums and
+ * the fp16 rounding of the stored O~ / l that the kept rows extend.
  *   ws: dllm_workspace_size(desc, decoded, DLLM_OP_CACHE_ADVANCE) bytes. */
 dllm_status dllm_cache_advance(const dllm_layer_desc* desc, const dllm_batch* batch, const dllm_batch* decoded,
                                const void* x_decoded, const void* rms_gain, const void* w_packed,
