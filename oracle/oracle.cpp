@@ -15,8 +15,9 @@
 //     section "Motivation"; LaCache Appendix B.2, Eq. (9)), written in two
 //     passes (row max, then exp-sum).
 //   * The online softmax state recurrence is LaCache §3.3.3, Eq. (2)-(6).
-//   * The FACache build and reuse follow LaCache §3.3.3 and Algorithm 1
-//     ("the first layer's Flash-Attention").
+//   * The FACache build and reuse follow the definitions of LaCache §3.3.3
+//     (each row's state over the keys of U, merged exactly with the fresh
+//     keys); the tile-granular cache of its Algorithm 1 is restated as sets.
 // Parallelism: OpenMP over independent outputs only; the arithmetic of each
 // output is sequential in the order written.
 #include <math.h>
